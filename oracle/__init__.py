@@ -1,0 +1,44 @@
+"""CPU oracle for the W4A8 grouped-expert MoE prefill path and the dense W8A8 projection.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product library imports, links or calls this
+package: only the test suite, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` use it.
+
+What it is: a plain, slow, float64 restatement of what the method computes, written from
+the source pages ("FP8 grouped-expert prefill with on-chip int4-to-e4m3 dequant" and its
+companion pages on per-tensor FP8 projections, the ``fp8_ffi`` prefill module and the FP8
+vs INT4 comparison).  Each function cites the passage it follows and lists the reading it
+takes where the pages are silent.  numpy matmul is the only library primitive used for a
+contraction; every quantization, rounding and ordering rule is written out here.
+
+It shares no code with the CUDA path (``fp8_grouped_expert_gb300``): the two meet only in
+the seeded input generators of ``workloads``, which hold none of the method's arithmetic.
+
+Pins (tests marked ``not gpu``) tie each function to facts the pages and the mathematics
+fix: the e4m3 code table, int4 exactness in e4m3, exact power-of-two GEMMs, closed forms,
+brute force on tiny inputs, and the permutation invariants.  Functions whose result is only
+checked by a similarity measure say "parity unpinned" in their docstring.
+"""
+
+from .fp8 import (  # noqa: F401
+    E4M3_MAX,
+    e4m3_decode_table,
+    e4m3_decode,
+    e4m3_encode,
+    int4_unpack,
+    bf16_round,
+    bf16_bits_to_f32,
+    quant_act_g128,
+    quant_act_per_tensor,
+)
+from .moe import (  # noqa: F401
+    topk_gate,
+    moe_permute,
+    grouped_gemm_w4a8,
+    linear_w8a8_gemm,
+    swiglu_requant,
+    moe_combine,
+    moe_layer_forward,
+    linear_w8a8,
+)
+from .stack import rmsnorm, router_logits, identity_attention, stacked_prefill  # noqa: F401
