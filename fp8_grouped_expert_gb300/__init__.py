@@ -1,0 +1,344 @@
+"""Thin Python binding of libfge (include/fge.h): W4A8 grouped-expert MoE prefill and dense
+per-tensor W8A8 projections on one GB300 (sm_103a).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.  PyTorch supplies
+device memory (including workspaces, allocated here on the caller's behalf) and the
+current stream.  There is no fallback: if libfge.so is missing or the device is not
+sm_103, calls raise.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfge.so")
+
+# enums of include/fge.h
+OK = 0
+SCALE_PER_TENSOR, SCALE_PER_TOKEN_G128 = 0, 1
+DTYPE_BF16, DTYPE_F32 = 0, 1
+EPI_STORE, EPI_SWIGLU_REQUANT = 0, 1
+W4_LUT, W4_SUBNORMAL = 0, 1
+OP_QUANT_PER_TENSOR, OP_PERMUTE, OP_GROUPED_GEMM, OP_LINEAR_W8A8, OP_MOE_LAYER = range(5)
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+
+# name -> argtypes (restype is int status unless listed in _RESTYPES)
+SIGNATURES = {
+    "fge_version": [],
+    "fge_init": [_I],
+    "fge_status_string": [_I],
+    "fge_workspace_bytes": [_I, _I64, _I64, _I64, _I, _I],
+    "fge_clear_device_status": [_P, _P],
+    "fge_read_device_status": [_P, _P, ctypes.POINTER(ctypes.c_int32)],
+    "fge_fp8_quant_act": [_P, _I64, _I64, _I, _P, _P, _P, _SZ, _P],
+    "fge_moe_topk_gate": [_P, _I64, _I, _I, _P, _P, _P],
+    "fge_moe_permute": [_P, _I64, _I, _I, _P, _P, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P],
+    "fge_w4_prepack": [_P, _P, _I, _I64, _I64, _I, _I, _P, _P, _P],
+    "fge_grouped_gemm_w4a8": [_P, _P, _P, _I64, _P, _P, _I, _I64, _I64, _I, _I, _I, _P, _P, _P,
+                              _SZ, _P],
+    "fge_swiglu_quant": [_P, _I64, _I64, _P, _P, _P],
+    "fge_moe_combine": [_P, _I, _P, _P, _I64, _I, _I64, _I, _P, _P],
+    "fge_gemm_w8a8": [_P, _P, _I64, _I64, _P, _P, _I64, _I, _P, _P, _SZ, _P],
+    "fge_linear_w8a8": [_P, _I64, _I64, _P, _P, _I64, _P, _P, _SZ, _P],
+    "fge_moe_layer_forward": [_P, _P, _I64, _I64, _I, _I, _I64, _P, _P, _P, _P, _I, _I, _P, _P,
+                              _SZ, _P],
+    "fge_rmsnorm": [_P, _I64, _I64, ctypes.c_float, _P, _P],
+    "fge_router_logits": [_P, _P, _I64, _I64, _I, _P, _P],
+    "fge_identity_attention": [_P, _I64, _I, _I, _P, _P],
+    "fge_residual_add": [_P, _P, _I, _I64, _P],
+}
+_RESTYPES = {"fge_version": ctypes.c_int, "fge_status_string": ctypes.c_char_p,
+             "fge_workspace_bytes": ctypes.c_size_t}
+
+_lib = None
+_inited = set()
+
+
+class FgeError(RuntimeError):
+    pass
+
+
+def lib():
+    """The loaded libfge (ctypes).  Raises if the in-tree library has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise FgeError("libfge.so is not built (run fp8_grouped_expert_gb300.build.build())")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, args in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.argtypes = args
+            fn.restype = _RESTYPES.get(name, ctypes.c_int)
+        _lib = handle
+    return _lib
+
+
+def status_string(code):
+    return lib().fge_status_string(code).decode()
+
+
+def _check(code, what):
+    if code != OK:
+        raise FgeError("%s failed: %s (%d)" % (what, status_string(code), code))
+
+
+def _ensure_init(device):
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    if idx not in _inited:
+        _check(lib().fge_init(idx), "fge_init(%d)" % idx)
+        _inited.add(idx)
+
+
+def _stream(t):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _need(t, dtype, name):
+    if not t.is_cuda:
+        raise FgeError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise FgeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise FgeError("%s must be contiguous" % name)
+
+
+def workspace_bytes(op, a=0, b=0, c=0, E=0, k=0):
+    return int(lib().fge_workspace_bytes(op, a, b, c, E, k))
+
+
+def new_workspace(nbytes, device):
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def read_device_status(ws):
+    out = ctypes.c_int32(0)
+    _check(lib().fge_read_device_status(_ptr(ws), _stream(ws), ctypes.byref(out)),
+           "fge_read_device_status")
+    return out.value
+
+
+def clear_device_status(ws):
+    _check(lib().fge_clear_device_status(_ptr(ws), _stream(ws)), "fge_clear_device_status")
+
+
+# ------------------------------------------------------------------------------ ops
+def fp8_quant_act(x, mode="g128", workspace=None):
+    """x: bf16 [M, K] -> (xq uint8 [M, K], xs float32 [M, K/128] or [1])."""
+    _need(x, torch.bfloat16, "x")
+    _ensure_init(x.device)
+    m, k = x.shape
+    xq = torch.empty((m, k), dtype=torch.uint8, device=x.device)
+    if mode == "g128":
+        xs = torch.empty((m, k // 128), dtype=torch.float32, device=x.device)
+        code = lib().fge_fp8_quant_act(_ptr(x), m, k, SCALE_PER_TOKEN_G128, _ptr(xq), _ptr(xs),
+                                       None, 0, _stream(x))
+    else:
+        xs = torch.empty((1,), dtype=torch.float32, device=x.device)
+        ws = workspace if workspace is not None else new_workspace(
+            workspace_bytes(OP_QUANT_PER_TENSOR, m, k), x.device)
+        code = lib().fge_fp8_quant_act(_ptr(x), m, k, SCALE_PER_TENSOR, _ptr(xq), _ptr(xs),
+                                       _ptr(ws), ws.numel(), _stream(x))
+    _check(code, "fge_fp8_quant_act")
+    return xq, xs
+
+
+def moe_topk_gate(logits, k):
+    _need(logits, torch.float32, "logits")
+    _ensure_init(logits.device)
+    t, e = logits.shape
+    ids = torch.empty((t, k), dtype=torch.int32, device=logits.device)
+    gates = torch.empty((t, k), dtype=torch.float32, device=logits.device)
+    _check(lib().fge_moe_topk_gate(_ptr(logits), t, e, k, _ptr(ids), _ptr(gates),
+                                   _stream(logits)), "fge_moe_topk_gate")
+    return ids, gates
+
+
+def moe_permute(ids, num_experts, xq, xs):
+    _need(ids, torch.int32, "ids")
+    _need(xq, torch.uint8, "xq")
+    _need(xs, torch.float32, "xs")
+    _ensure_init(ids.device)
+    t, k = ids.shape
+    h = xq.shape[1]
+    dev = ids.device
+    r = t * k
+    out = dict(
+        offsets=torch.empty(num_experts + 1, dtype=torch.int32, device=dev),
+        row_token=torch.empty(r, dtype=torch.int32, device=dev),
+        token_row=torch.empty((t, k), dtype=torch.int32, device=dev),
+        aq=torch.empty((r, h), dtype=torch.uint8, device=dev),
+        as_=torch.empty((r, h // 128), dtype=torch.float32, device=dev),
+    )
+    ws = new_workspace(workspace_bytes(OP_PERMUTE, t, h, 0, num_experts, k), dev)
+    _check(lib().fge_moe_permute(_ptr(ids), t, k, num_experts, _ptr(xq), _ptr(xs), h,
+                                 _ptr(out["offsets"]), _ptr(out["row_token"]),
+                                 _ptr(out["token_row"]), _ptr(out["aq"]), _ptr(out["as_"]),
+                                 _ptr(ws), ws.numel(), _stream(ids)), "fge_moe_permute")
+    return out
+
+
+def w4_prepack(w_packed, w_scale, gate_up_interleave=False, fmt=W4_SUBNORMAL):
+    """Canonical bank uint8 [E, N, K/2] + scales [E, N, K/128] -> kernel layout
+    (uint8 [E, N, K/2], float32 [E, K/128, N])."""
+    _need(w_packed, torch.uint8, "w_packed")
+    _need(w_scale, torch.float32, "w_scale")
+    _ensure_init(w_packed.device)
+    e, n, kh = w_packed.shape
+    k = kh * 2
+    wd = torch.empty_like(w_packed)
+    sd = torch.empty((e, k // 128, n), dtype=torch.float32, device=w_packed.device)
+    _check(lib().fge_w4_prepack(_ptr(w_packed), _ptr(w_scale), e, n, k,
+                                1 if gate_up_interleave else 0, fmt, _ptr(wd), _ptr(sd),
+                                _stream(w_packed)), "fge_w4_prepack")
+    return wd, sd
+
+
+def grouped_gemm_w4a8(aq, as_, offsets, w_dev, s_dev, fmt=W4_SUBNORMAL, epilogue="store",
+                      out_dtype=torch.float32, workspace=None):
+    """Grouped W4A8 GEMM; epilogue 'store' -> out [R, N]; 'swiglu' -> (hq [R, N/2], hs)."""
+    _need(aq, torch.uint8, "aq")
+    _need(as_, torch.float32, "as_")
+    _need(offsets, torch.int32, "offsets")
+    _ensure_init(aq.device)
+    r, k = aq.shape
+    e, n, _ = w_dev.shape
+    dev = aq.device
+    ws = workspace if workspace is not None else new_workspace(
+        workspace_bytes(OP_GROUPED_GEMM), dev)
+    if epilogue == "swiglu":
+        out = torch.zeros((r, n // 2), dtype=torch.uint8, device=dev)
+        scales = torch.zeros((r, n // 256), dtype=torch.float32, device=dev)
+        epi, od = EPI_SWIGLU_REQUANT, DTYPE_BF16
+    else:
+        out = torch.zeros((r, n), dtype=out_dtype, device=dev)
+        scales = None
+        epi = EPI_STORE
+        od = DTYPE_F32 if out_dtype == torch.float32 else DTYPE_BF16
+    _check(lib().fge_grouped_gemm_w4a8(_ptr(aq), _ptr(as_), _ptr(offsets), r, _ptr(w_dev),
+                                       _ptr(s_dev), e, n, k, fmt, epi, od, _ptr(out),
+                                       _ptr(scales), _ptr(ws), ws.numel(), _stream(aq)),
+           "fge_grouped_gemm_w4a8")
+    return (out, scales) if epilogue == "swiglu" else out
+
+
+def swiglu_quant(c, inter):
+    _need(c, torch.float32, "c")
+    _ensure_init(c.device)
+    r = c.shape[0]
+    hq = torch.empty((r, inter), dtype=torch.uint8, device=c.device)
+    hs = torch.empty((r, inter // 128), dtype=torch.float32, device=c.device)
+    _check(lib().fge_swiglu_quant(_ptr(c), r, inter, _ptr(hq), _ptr(hs), _stream(c)),
+           "fge_swiglu_quant")
+    return hq, hs
+
+
+def moe_combine(y, token_row, gates, out_dtype=torch.bfloat16):
+    _need(token_row, torch.int32, "token_row")
+    _need(gates, torch.float32, "gates")
+    _ensure_init(y.device)
+    t, k = token_row.shape
+    h = y.shape[1]
+    out = torch.empty((t, h), dtype=out_dtype, device=y.device)
+    _check(lib().fge_moe_combine(_ptr(y), DTYPE_F32 if y.dtype == torch.float32 else DTYPE_BF16,
+                                 _ptr(token_row), _ptr(gates), t, k, h,
+                                 DTYPE_F32 if out_dtype == torch.float32 else DTYPE_BF16,
+                                 _ptr(out), _stream(y)), "fge_moe_combine")
+    return out
+
+
+def gemm_w8a8(aq, sa, wq, sw, out_dtype=torch.bfloat16, workspace=None):
+    _need(aq, torch.uint8, "aq")
+    _need(wq, torch.uint8, "wq")
+    _ensure_init(aq.device)
+    m, k = aq.shape
+    n = wq.shape[0]
+    ws = workspace if workspace is not None else new_workspace(
+        workspace_bytes(OP_GROUPED_GEMM), aq.device)
+    y = torch.empty((m, n), dtype=out_dtype, device=aq.device)
+    _check(lib().fge_gemm_w8a8(_ptr(aq), _ptr(sa), m, k, _ptr(wq), _ptr(sw), n,
+                               DTYPE_F32 if out_dtype == torch.float32 else DTYPE_BF16, _ptr(y),
+                               _ptr(ws), ws.numel(), _stream(aq)), "fge_gemm_w8a8")
+    return y
+
+
+def linear_w8a8(x, wq, w_scale, workspace=None, out=None):
+    _need(x, torch.bfloat16, "x")
+    _need(wq, torch.uint8, "wq")
+    _ensure_init(x.device)
+    m, k = x.shape
+    n = wq.shape[0]
+    ws = workspace if workspace is not None else new_workspace(
+        workspace_bytes(OP_LINEAR_W8A8, m, k), x.device)
+    y = out if out is not None else torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
+    _check(lib().fge_linear_w8a8(_ptr(x), m, k, _ptr(wq), _ptr(w_scale), n, _ptr(y), _ptr(ws),
+                                 ws.numel(), _stream(x)), "fge_linear_w8a8")
+    return y
+
+
+def moe_layer_forward(logits, x, k, inter, w_gu_dev, s_gu_dev, w_dn_dev, s_dn_dev,
+                      fmt=W4_SUBNORMAL, out_dtype=torch.bfloat16, workspace=None, out=None):
+    _need(logits, torch.float32, "logits")
+    _need(x, torch.bfloat16, "x")
+    _ensure_init(x.device)
+    t, h = x.shape
+    e = logits.shape[1]
+    ws = workspace if workspace is not None else new_workspace(
+        workspace_bytes(OP_MOE_LAYER, t, h, inter, e, k), x.device)
+    y = out if out is not None else torch.empty((t, h), dtype=out_dtype, device=x.device)
+    _check(lib().fge_moe_layer_forward(_ptr(logits), _ptr(x), t, h, e, k, inter, _ptr(w_gu_dev),
+                                       _ptr(s_gu_dev), _ptr(w_dn_dev), _ptr(s_dn_dev), fmt,
+                                       DTYPE_F32 if out_dtype == torch.float32 else DTYPE_BF16,
+                                       _ptr(y), _ptr(ws), ws.numel(), _stream(x)),
+           "fge_moe_layer_forward")
+    return y
+
+
+def rmsnorm(h, eps=1e-6, out=None):
+    _need(h, torch.float32, "h")
+    _ensure_init(h.device)
+    t, d = h.shape
+    y = out if out is not None else torch.empty((t, d), dtype=torch.bfloat16, device=h.device)
+    _check(lib().fge_rmsnorm(_ptr(h), t, d, eps, _ptr(y), _stream(h)), "fge_rmsnorm")
+    return y
+
+
+def router_logits(xn, w_router, out=None):
+    _need(xn, torch.bfloat16, "xn")
+    _need(w_router, torch.float32, "w_router")
+    _ensure_init(xn.device)
+    t, d = xn.shape
+    e = w_router.shape[0]
+    y = out if out is not None else torch.empty((t, e), dtype=torch.float32, device=xn.device)
+    _check(lib().fge_router_logits(_ptr(xn), _ptr(w_router), t, d, e, _ptr(y), _stream(xn)),
+           "fge_router_logits")
+    return y
+
+
+def identity_attention(v, n_heads, n_kv_heads, out=None):
+    _need(v, torch.bfloat16, "v")
+    _ensure_init(v.device)
+    t = v.shape[0]
+    y = out if out is not None else torch.empty((t, n_heads * 128), dtype=torch.bfloat16,
+                                                device=v.device)
+    _check(lib().fge_identity_attention(_ptr(v), t, n_heads, n_kv_heads, _ptr(y), _stream(v)),
+           "fge_identity_attention")
+    return y
+
+
+def residual_add(h, y):
+    _need(h, torch.float32, "h")
+    _ensure_init(h.device)
+    _check(lib().fge_residual_add(_ptr(h), _ptr(y),
+                                  DTYPE_F32 if y.dtype == torch.float32 else DTYPE_BF16,
+                                  h.numel(), _stream(h)), "fge_residual_add")
+    return h

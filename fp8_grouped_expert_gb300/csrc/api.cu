@@ -1,0 +1,381 @@
+// C ABI of libfge: argument validation, workspace carving and stream-ordered launches.
+// No entry point allocates device memory or synchronises the host (except
+// fge_read_device_status, which exists to read a result back).
+#include <mutex>
+
+#include "fge_internal.h"
+
+namespace fge {
+
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices] = {0};
+bool g_init[kMaxDevices] = {false};
+std::mutex g_mu;
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline fge_status cur_device_ok() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FGE_ERR_CUDA;
+  return g_init[dev] ? FGE_OK : FGE_ERR_NOT_INITIALIZED;
+}
+
+inline fge_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FGE_OK : FGE_ERR_CUDA; }
+
+#define FGE_CHECK(expr)                 \
+  do {                                  \
+    const fge_status st_ = (expr);      \
+    if (st_ != FGE_OK) return st_;      \
+  } while (0)
+
+#define FGE_REQUIRE(cond, code) \
+  do {                          \
+    if (!(cond)) return (code); \
+  } while (0)
+
+// Workspace layout of a full MoE layer.
+struct LayerWs {
+  WsHeader* hdr;
+  uint8_t* xq;
+  float* xs;
+  int32_t* ids;
+  float* gates;
+  void* perm;
+  int32_t* offsets;
+  int32_t* row_token;
+  int32_t* token_row;
+  uint8_t* aq;
+  float* as;
+  uint8_t* hq;
+  float* hs;
+  void* y;
+  size_t bytes;
+};
+
+LayerWs carve_layer(void* base, int64_t T, int64_t H, int64_t I, int E, int k) {
+  LayerWs w{};
+  const int64_t R = T * k;
+  size_t off = 0;
+  auto take = [&](size_t n) {
+    void* p = base ? static_cast<uint8_t*>(base) + off : nullptr;
+    off += align_up(n, 256);
+    return p;
+  };
+  w.hdr = static_cast<WsHeader*>(take(kWsHeaderBytes));
+  w.xq = static_cast<uint8_t*>(take(T * H));
+  w.xs = static_cast<float*>(take(T * (H / 128) * 4));
+  w.ids = static_cast<int32_t*>(take(R * 4));
+  w.gates = static_cast<float*>(take(R * 4));
+  w.perm = take(permute_scratch_bytes(T, E));
+  w.offsets = static_cast<int32_t*>(take((E + 1) * 4));
+  w.row_token = static_cast<int32_t*>(take(R * 4));
+  w.token_row = static_cast<int32_t*>(take(R * 4));
+  w.aq = static_cast<uint8_t*>(take(R * H));
+  w.as = static_cast<float*>(take(R * (H / 128) * 4));
+  w.hq = static_cast<uint8_t*>(take(R * I));
+  w.hs = static_cast<float*>(take(R * (I / 128) * 4));
+  w.y = take(R * H * 4);
+  w.bytes = off;
+  return w;
+}
+
+}  // namespace
+
+int num_sms() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return (dev >= 0 && dev < kMaxDevices && g_sms[dev] > 0) ? g_sms[dev] : 148;
+}
+
+}  // namespace fge
+
+using namespace fge;
+
+extern "C" {
+
+int fge_version(void) { return 100; }
+
+const char* fge_status_string(fge_status s) {
+  switch (s) {
+    case FGE_OK: return "ok";
+    case FGE_ERR_INVALID_ARG: return "invalid argument";
+    case FGE_ERR_BAD_SHAPE: return "bad shape";
+    case FGE_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case FGE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case FGE_ERR_UNSUPPORTED_DEVICE: return "unsupported device or kernel resources";
+    case FGE_ERR_CUDA: return "CUDA error";
+    case FGE_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+    case FGE_ERR_NOT_INITIALIZED: return "fge_init not called for this device";
+  }
+  return "unknown status";
+}
+
+fge_status fge_init(int device) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (device < 0 || device >= kMaxDevices) return FGE_ERR_INVALID_ARG;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return FGE_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return FGE_ERR_UNSUPPORTED_DEVICE;
+  g_sms[device] = prop.multiProcessorCount;
+  g_init[device] = true;
+  return FGE_OK;
+}
+
+size_t fge_workspace_bytes(fge_op op, int64_t a, int64_t b, int64_t c, int E, int k) {
+  switch (op) {
+    case FGE_OP_QUANT_PER_TENSOR: return kWsHeaderBytes;
+    case FGE_OP_PERMUTE: return kWsHeaderBytes + permute_scratch_bytes(a, E);
+    case FGE_OP_GROUPED_GEMM: return kWsHeaderBytes;
+    case FGE_OP_LINEAR_W8A8: return kWsHeaderBytes + align_up(static_cast<size_t>(a * b), 256);
+    case FGE_OP_MOE_LAYER: return carve_layer(nullptr, a, b, c, E, k).bytes;
+  }
+  return 0;
+}
+
+fge_status fge_clear_device_status(void* ws, fge_stream_t stream) {
+  FGE_REQUIRE(ws, FGE_ERR_INVALID_ARG);
+  return from_cuda(cudaMemsetAsync(ws, 0, sizeof(int32_t), stream));
+}
+
+fge_status fge_read_device_status(const void* ws, fge_stream_t stream, int32_t* out) {
+  FGE_REQUIRE(ws && out, FGE_ERR_INVALID_ARG);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FGE_ERR_CUDA;
+  return from_cuda(cudaMemcpy(out, ws, sizeof(int32_t), cudaMemcpyDeviceToHost));
+}
+
+fge_status fge_fp8_quant_act(const void* x, int64_t M, int64_t K, fge_scale_mode mode,
+                             uint8_t* xq, float* xs, void* ws, size_t ws_bytes,
+                             fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(M >= 0 && K > 0 && K % 128 == 0, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(x && xq && xs, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(al16(x) && al16(xq), FGE_ERR_MISALIGNED);
+  if (mode == FGE_SCALE_PER_TOKEN_G128) {
+    return from_cuda(launch_quant_g128(static_cast<const uint16_t*>(x), M, K, xq, xs, stream));
+  }
+  FGE_REQUIRE(mode == FGE_SCALE_PER_TENSOR, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(ws, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(al16(ws), FGE_ERR_MISALIGNED);
+  FGE_REQUIRE(ws_bytes >= kWsHeaderBytes, FGE_ERR_WORKSPACE_TOO_SMALL);
+  return from_cuda(launch_quant_per_tensor(static_cast<const uint16_t*>(x), M, K, xq, xs,
+                                           static_cast<WsHeader*>(ws), stream));
+}
+
+fge_status fge_moe_topk_gate(const float* logits, int64_t T, int E, int k, int32_t* ids,
+                             float* gates, fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(logits && ids && gates, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(T >= 0 && E >= 1 && E <= 1024 && k >= 1 && k <= E && k <= 32, FGE_ERR_BAD_SHAPE);
+  return from_cuda(launch_topk_gate(logits, T, E, k, ids, gates, stream));
+}
+
+fge_status fge_moe_permute(const int32_t* ids, int64_t T, int k, int E, const uint8_t* xq,
+                           const float* xs, int64_t H, int32_t* offsets, int32_t* row_token,
+                           int32_t* token_row, uint8_t* aq, float* as, void* ws,
+                           size_t ws_bytes, fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(ids && xq && xs && offsets && row_token && token_row && aq && as && ws,
+              FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(T >= 0 && E >= 1 && E <= 1024 && k >= 1 && k <= E && k <= 32, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(H > 0 && H % 128 == 0 && T * k < (1LL << 31), FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(al16(xq) && al16(aq) && al16(ws), FGE_ERR_MISALIGNED);
+  FGE_REQUIRE(ws_bytes >= fge_workspace_bytes(FGE_OP_PERMUTE, T, H, 0, E, k),
+              FGE_ERR_WORKSPACE_TOO_SMALL);
+  return from_cuda(launch_permute(ids, T, k, E, xq, xs, H, offsets, row_token, token_row, aq, as,
+                                  static_cast<uint8_t*>(ws) + kWsHeaderBytes, stream));
+}
+
+fge_status fge_w4_prepack(const uint8_t* w, const float* w_scale, int E, int64_t N, int64_t K,
+                          int gate_up_interleave, fge_w4_format format, uint8_t* w_dev,
+                          float* w_scale_dev, fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(w && w_scale && w_dev && w_scale_dev, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(format == FGE_W4_LUT || format == FGE_W4_SUBNORMAL, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(E >= 1 && N > 0 && N % 128 == 0 && K > 0 && K % 128 == 0, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(!gate_up_interleave || N % 256 == 0, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(al16(w) && al16(w_dev) && al16(w_scale_dev), FGE_ERR_MISALIGNED);
+  return from_cuda(launch_w4_prepack(w, w_scale, E, N, K, gate_up_interleave ? 1 : 0,
+                                     static_cast<int>(format), w_dev, w_scale_dev, stream));
+}
+
+static fge_status grouped_common(const uint8_t* aq, const float* as, const int32_t* offsets,
+                                 int64_t R, const uint8_t* w, const float* sw, int E, int64_t N,
+                                 int64_t K, int format, int per_tensor, const float* sa_t,
+                                 int epilogue, void* out, float* out_scales, void* ws,
+                                 size_t ws_bytes, fge_stream_t stream) {
+  FGE_REQUIRE(R >= 0 && R < (1LL << 31) && N > 0 && N % 128 == 0 && N < (1LL << 24) && K > 0 &&
+                  K % 128 == 0 && K < (1LL << 24),
+              FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(E >= 1 && E <= kMaxExperts, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(ws && out && aq && w && sw, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(al16(aq) && al16(w) && al16(out) && al16(ws) && (per_tensor || al16(sw)),
+              FGE_ERR_MISALIGNED);
+  FGE_REQUIRE(ws_bytes >= kWsHeaderBytes, FGE_ERR_WORKSPACE_TOO_SMALL);
+  if (R == 0) return FGE_OK;
+  GroupedGemmArgs a{};
+  a.aq = aq;
+  a.as = as;
+  a.sa_tensor = sa_t;
+  a.offsets = offsets;
+  a.w = w;
+  a.sw = sw;
+  a.E = E;
+  a.N = N;
+  a.K = K;
+  a.R = R;
+  a.bank_format = format;
+  a.per_tensor = per_tensor;
+  a.epilogue = epilogue;
+  a.out = out;
+  a.out_scales = out_scales;
+  a.status = &static_cast<WsHeader*>(ws)->status;
+  fge_status st = FGE_OK;
+  const cudaError_t e = launch_grouped_gemm(a, stream, &st);
+  if (e != cudaSuccess) return FGE_ERR_CUDA;
+  return st;
+}
+
+fge_status fge_grouped_gemm_w4a8(const uint8_t* aq, const float* as, const int32_t* offsets,
+                                 int64_t R, const uint8_t* w_dev, const float* w_scale_dev,
+                                 int E, int64_t N, int64_t K, fge_w4_format format,
+                                 fge_epilogue epilogue, fge_dtype out_dtype, void* out,
+                                 float* out_scales, void* ws, size_t ws_bytes,
+                                 fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(as && offsets, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(format == FGE_W4_LUT || format == FGE_W4_SUBNORMAL, FGE_ERR_INVALID_ARG);
+  int epi;
+  if (epilogue == FGE_EPI_SWIGLU_REQUANT) {
+    FGE_REQUIRE(out_scales, FGE_ERR_INVALID_ARG);
+    FGE_REQUIRE(N % 256 == 0, FGE_ERR_BAD_SHAPE);
+    epi = 2;
+  } else {
+    FGE_REQUIRE(epilogue == FGE_EPI_STORE, FGE_ERR_INVALID_ARG);
+    FGE_REQUIRE(out_dtype == FGE_DTYPE_BF16 || out_dtype == FGE_DTYPE_F32, FGE_ERR_INVALID_ARG);
+    epi = out_dtype == FGE_DTYPE_F32 ? 0 : 1;
+  }
+  return grouped_common(aq, as, offsets, R, w_dev, w_scale_dev, E, N, K, format, 0, nullptr, epi,
+                        out, out_scales, ws, ws_bytes, stream);
+}
+
+fge_status fge_swiglu_quant(const float* c, int64_t R, int64_t I, uint8_t* hq, float* hs,
+                            fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(c && hq && hs, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(R >= 0 && I > 0 && I % 128 == 0, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(al16(c) && al16(hq), FGE_ERR_MISALIGNED);
+  return from_cuda(launch_swiglu_quant(c, R, I, hq, hs, stream));
+}
+
+fge_status fge_moe_combine(const void* y, fge_dtype y_dtype, const int32_t* token_row,
+                           const float* gates, int64_t T, int k, int64_t H,
+                           fge_dtype out_dtype, void* out, fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(y && token_row && gates && out, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE((y_dtype == FGE_DTYPE_BF16 || y_dtype == FGE_DTYPE_F32) &&
+                  (out_dtype == FGE_DTYPE_BF16 || out_dtype == FGE_DTYPE_F32),
+              FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(T >= 0 && k >= 1 && k <= 32 && H > 0 && H % 128 == 0, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(al16(y) && al16(out), FGE_ERR_MISALIGNED);
+  return from_cuda(launch_combine(y, y_dtype == FGE_DTYPE_F32, token_row, gates, T, k, H,
+                                  out_dtype == FGE_DTYPE_F32, out, stream));
+}
+
+fge_status fge_gemm_w8a8(const uint8_t* aq, const float* sa, int64_t M, int64_t K,
+                         const uint8_t* wq, const float* sw, int64_t N, fge_dtype out_dtype,
+                         void* y, void* ws, size_t ws_bytes, fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(sa, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(out_dtype == FGE_DTYPE_BF16 || out_dtype == FGE_DTYPE_F32, FGE_ERR_INVALID_ARG);
+  return grouped_common(aq, nullptr, nullptr, M, wq, sw, 1, N, K, 0, 1, sa,
+                        out_dtype == FGE_DTYPE_F32 ? 0 : 1, y, nullptr, ws, ws_bytes, stream);
+}
+
+fge_status fge_linear_w8a8(const void* x, int64_t M, int64_t K, const uint8_t* wq,
+                           const float* w_scale, int64_t N, void* y, void* ws, size_t ws_bytes,
+                           fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(x && wq && w_scale && y && ws, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(M >= 0 && K > 0 && K % 128 == 0 && N > 0 && N % 128 == 0, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(al16(x) && al16(ws), FGE_ERR_MISALIGNED);
+  FGE_REQUIRE(ws_bytes >= fge_workspace_bytes(FGE_OP_LINEAR_W8A8, M, K, 0, 0, 0),
+              FGE_ERR_WORKSPACE_TOO_SMALL);
+  WsHeader* hdr = static_cast<WsHeader*>(ws);
+  uint8_t* xq = static_cast<uint8_t*>(ws) + kWsHeaderBytes;
+  FGE_CHECK(from_cuda(launch_quant_per_tensor(static_cast<const uint16_t*>(x), M, K, xq,
+                                              &hdr->scale, hdr, stream)));
+  return grouped_common(xq, nullptr, nullptr, M, wq, w_scale, 1, N, K, 0, 1, &hdr->scale, 1, y,
+                        nullptr, ws, ws_bytes, stream);
+}
+
+fge_status fge_moe_layer_forward(const float* logits, const void* x, int64_t T, int64_t H, int E,
+                                 int k, int64_t I, const uint8_t* w_gu, const float* s_gu,
+                                 const uint8_t* w_dn, const float* s_dn, fge_w4_format format,
+                                 fge_dtype out_dtype, void* out, void* ws, size_t ws_bytes,
+                                 fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(logits && x && w_gu && s_gu && w_dn && s_dn && out && ws, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(format == FGE_W4_LUT || format == FGE_W4_SUBNORMAL, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(out_dtype == FGE_DTYPE_BF16 || out_dtype == FGE_DTYPE_F32, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(T >= 0 && H > 0 && H % 128 == 0 && I > 0 && I % 128 == 0, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(E >= 1 && E <= kMaxExperts && k >= 1 && k <= E && k <= 32, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(T * k < (1LL << 31) && (2 * I) % 256 == 0, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(al16(x) && al16(ws) && al16(out) && al16(w_gu) && al16(w_dn) && al16(s_gu) &&
+                  al16(s_dn),
+              FGE_ERR_MISALIGNED);
+  const LayerWs w = carve_layer(ws, T, H, I, E, k);
+  FGE_REQUIRE(ws_bytes >= w.bytes, FGE_ERR_WORKSPACE_TOO_SMALL);
+  if (T == 0) return FGE_OK;
+  const int64_t R = T * k;
+  const int out_f32 = out_dtype == FGE_DTYPE_F32;
+  FGE_CHECK(from_cuda(launch_topk_gate(logits, T, E, k, w.ids, w.gates, stream)));
+  FGE_CHECK(from_cuda(launch_quant_g128(static_cast<const uint16_t*>(x), T, H, w.xq, w.xs, stream)));
+  FGE_CHECK(from_cuda(launch_permute(w.ids, T, k, E, w.xq, w.xs, H, w.offsets, w.row_token,
+                                     w.token_row, w.aq, w.as, w.perm, stream)));
+  FGE_CHECK(grouped_common(w.aq, w.as, w.offsets, R, w_gu, s_gu, E, 2 * I, H, format, 0, nullptr,
+                           2, w.hq, w.hs, ws, ws_bytes, stream));
+  FGE_CHECK(grouped_common(w.hq, w.hs, w.offsets, R, w_dn, s_dn, E, H, I, format, 0, nullptr,
+                           out_f32 ? 0 : 1, w.y, nullptr, ws, ws_bytes, stream));
+  return from_cuda(launch_combine(w.y, out_f32, w.token_row, w.gates, T, k, H, out_f32, out, stream));
+}
+
+fge_status fge_rmsnorm(const float* h, int64_t T, int64_t H, float eps, void* out,
+                       fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(h && out, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(T >= 0 && H > 0 && H % 8 == 0, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(al16(h) && al16(out), FGE_ERR_MISALIGNED);
+  return from_cuda(launch_rmsnorm(h, T, H, eps, static_cast<uint16_t*>(out), stream));
+}
+
+fge_status fge_router_logits(const void* xn, const float* w, int64_t T, int64_t H, int E,
+                             float* logits, fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(xn && w && logits, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(T >= 0 && H > 0 && H % 256 == 0 && E >= 1, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(al16(xn) && al16(w), FGE_ERR_MISALIGNED);
+  return from_cuda(launch_router(static_cast<const uint16_t*>(xn), w, T, H, E, logits, stream));
+}
+
+fge_status fge_identity_attention(const void* v, int64_t T, int n_heads, int n_kv,
+                                  void* attn, fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(v && attn, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(T >= 0 && n_kv >= 1 && n_heads >= n_kv && n_heads % n_kv == 0, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(al16(v) && al16(attn), FGE_ERR_MISALIGNED);
+  return from_cuda(launch_identity_attention(static_cast<const uint16_t*>(v), T, n_heads, n_kv,
+                                             static_cast<uint16_t*>(attn), stream));
+}
+
+fge_status fge_residual_add(float* h, const void* y, fge_dtype y_dtype, int64_t n,
+                            fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(h && y, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(y_dtype == FGE_DTYPE_BF16 || y_dtype == FGE_DTYPE_F32, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(n >= 0 && n % 4 == 0, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(al16(h) && al16(y), FGE_ERR_MISALIGNED);
+  return from_cuda(launch_residual_add(h, y, y_dtype == FGE_DTYPE_F32, n, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,82 @@
+// Internal declarations shared by the CUDA translation units of libfge (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/fge.h"
+
+namespace fge {
+
+constexpr int kGroup = 128;          // K-group of the per-group scales
+constexpr int kMaxExperts = 512;     // grouped GEMM keeps offsets in shared memory
+constexpr size_t kWsHeaderBytes = 256;
+
+// Workspace header (first 256 bytes of every workspace):
+//   int32  status       device-detected error code (0 = none)
+//   uint32 amax_bits    per-tensor amax as float bits (non-negative floats order as uints)
+//   float  scale        per-tensor activation scale written by the cast pass
+struct WsHeader {
+  int32_t status;
+  uint32_t amax_bits;
+  float scale;
+  int32_t pad[61];
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Weight-bank formats of the int4 path (see include/fge.h).
+enum BankFormat { kBankLut = 0, kBankSubnormal = 1 };
+
+// Launchers (return a cudaError_t from the launch; argument checks happen in the API layer).
+cudaError_t launch_quant_g128(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,
+                              cudaStream_t s);
+cudaError_t launch_quant_per_tensor(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq,
+                                    float* xs, WsHeader* hdr, cudaStream_t s);
+cudaError_t launch_topk_gate(const float* logits, int64_t T, int E, int k, int32_t* ids,
+                             float* gates, cudaStream_t s);
+size_t permute_scratch_bytes(int64_t T, int E);
+cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, const uint8_t* xq,
+                           const float* xs, int64_t H, int32_t* offsets, int32_t* row_token,
+                           int32_t* token_row, uint8_t* aq, float* as, void* scratch,
+                           cudaStream_t s);
+cudaError_t launch_combine(const void* y, int y_f32, const int32_t* token_row,
+                           const float* gates, int64_t T, int k, int64_t H, int out_f32,
+                           void* out, cudaStream_t s);
+cudaError_t launch_swiglu_quant(const float* c, int64_t R, int64_t I, uint8_t* hq, float* hs,
+                                cudaStream_t s);
+cudaError_t launch_w4_prepack(const uint8_t* w, const float* sw, int E, int64_t N, int64_t K,
+                              int interleave, int fmt, uint8_t* w_dev, float* sw_dev,
+                              cudaStream_t s);
+
+// Grouped GEMM.  mode: 0 = int4 bank with per-group scales, 1 = e4m3 weights, per-tensor.
+struct GroupedGemmArgs {
+  const uint8_t* aq;        // [R, K] e4m3 codes
+  const float* as;          // [R, K/128] (group mode)
+  const float* sa_tensor;   // device scalar (per-tensor mode)
+  const int32_t* offsets;   // [E+1]
+  const uint8_t* w;         // int4 bank [E, N, K/2] (prepacked) or e4m3 [N, K]
+  const float* sw;          // [E, K/128, N] prepacked group scales, or device scalar
+  int E;
+  int64_t N, K, R;
+  int bank_format;          // BankFormat (int4 mode)
+  int per_tensor;           // 0: int4 + group scales; 1: e4m3 + per-tensor scales
+  int epilogue;             // 0 store f32, 1 store bf16, 2 SwiGLU + e4m3 requant
+  void* out;
+  float* out_scales;
+  int32_t* status;
+};
+cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st);
+
+cudaError_t launch_rmsnorm(const float* h, int64_t T, int64_t H, float eps, uint16_t* out,
+                           cudaStream_t s);
+cudaError_t launch_router(const uint16_t* xn, const float* wr, int64_t T, int64_t H, int E,
+                          float* logits, cudaStream_t s);
+cudaError_t launch_identity_attention(const uint16_t* v, int64_t T, int n_heads, int n_kv,
+                                      uint16_t* attn, cudaStream_t s);
+cudaError_t launch_residual_add(float* h, const void* y, int y_f32, int64_t n, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace fge

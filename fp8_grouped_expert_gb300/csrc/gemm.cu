@@ -1,0 +1,725 @@
+// Grouped expert GEMM for sm_103a: one persistent, warp-specialised kernel that runs the
+// W4A8 expert GEMMs of an MoE layer ("FP8 grouped-expert prefill with on-chip
+// int4-to-e4m3 dequant", section 1) and, run with one expert and per-tensor scales, the
+// dense W8A8 projection ("feat(qwen4_exp): load-time per-tensor FP8 dense projections").
+//
+// Per CTA (one per SM), warp roles:
+//   warps 0-3   unpack: int4 tile (shared memory) -> e4m3 in the 128-byte swizzle layout
+//   warp  4     TMA producer: A tile [128 rows x 128 K] + B tile per K group
+//   warp  5     TMEM allocator and single-thread tcgen05.mma issuer (kind::f8f6f4)
+//   warps 6-7   idle
+//   warps 8..   epilogue warpgroups: per-group fp32 promotion acc += as*sw*P from TMEM,
+//               then the store / SwiGLU + requant epilogue
+// A K group (128 values) is exactly one 128-byte swizzle atom row, so each pipeline
+// stage carries one group and each group is 4 MMAs of K = 32 into a fresh TMEM buffer.
+// Two TMEM buffers (2 x BN columns) let the MMA run one group ahead of the promotion.
+#include <algorithm>
+#include <cudaTypedefs.h>
+
+#include "fge_device.cuh"
+
+namespace fge {
+
+enum { kBfmtInt4Lut = 0, kBfmtInt4Sub = 1, kBfmtE4m3 = 2 };
+enum { kEpiF32 = 0, kEpiBf16 = 1, kEpiSwiglu = 2 };
+
+struct GemmParams {
+  const float* as;         // [R, G] activation group scales
+  const float* sw;         // [E, G, N] prepacked weight group scales
+  const float* sa_tensor;  // per-tensor activation scale (device scalar)
+  const float* sw_tensor;  // per-tensor weight scale (device scalar)
+  const int32_t* offsets;  // [E+1]
+  void* out;
+  float* out_scales;
+  int32_t* status;
+  int E, N, K, G;
+  int dense_rows;          // offsets == nullptr: one expert owning rows [0, dense_rows)
+};
+
+constexpr int align16(int x) { return (x + 15) / 16 * 16; }
+
+template <int BN, int BFMT, int EPI>
+struct Cfg {
+  static constexpr bool kInt4 = BFMT != kBfmtE4m3;
+  static constexpr bool kGroupScale = kInt4;  // int4 path: per-group; e4m3 path: per-tensor
+  static constexpr int kABytes = 128 * 128;
+  static constexpr int kBLoadBytes = kInt4 ? BN * 64 : BN * 128;
+  static constexpr int kBUBytes = BN * 128;
+  static constexpr int kNU = kInt4 ? 2 : 0;
+  static constexpr int kStageBytes = kABytes + kBLoadBytes;
+  static constexpr int kPipeBytes = 192 * 1024;
+  static constexpr int kNS = (kPipeBytes - kNU * kBUBytes) / kStageBytes;
+  static constexpr int kEpiWarps = BN / 32;  // one warpgroup per 128 columns
+  static constexpr int kEpiThreads = kEpiWarps * 32;
+  static constexpr int kThreads = 256 + kEpiThreads;
+  static constexpr int kTmemCols = 2 * BN;
+  // register split (group mode only): WG0/WG1 shrink, epilogue warpgroups grow
+  static constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8;
+  static constexpr int kRegsLow = 80;
+  static constexpr int kRegsHigh0 = (kLaunchRegs * kThreads - 256 * kRegsLow) / kEpiThreads / 8 * 8;
+  static constexpr int kRegsHigh = kRegsHigh0 > 240 ? 240 : kRegsHigh0;
+  // shared memory layout (offsets from a 1024-aligned base)
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kNS * kABytes;
+  static constexpr int kOffBU = kOffB + kNS * kBLoadBytes;
+  static constexpr int kOffBar = kOffBU + kNU * kBUBytes;
+  static constexpr int kNumBars = 2 * kNS + 2 * kNU + 4 + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kOffOffs = align16(kOffMisc + 16);
+  static constexpr int kOffMtp = kOffOffs + (kMaxExperts + 1) * 4;
+  static constexpr int kOffRed = align16(kOffMtp + (kMaxExperts + 1) * 4);
+  static constexpr int kSmemBytes = kOffRed + 2 * 2 * 128 * 4 + 1024;  // + alignment slack
+  static_assert(kNS >= 2, "pipeline needs at least two stages");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// 8 int4 values (two's complement, nibble i = element i) -> e4m3 codes of the integers.
+// Two 8-entry byte-permute tables (codes of 0..7 and of -8..-1) and a per-byte select.
+__device__ __forceinline__ uint2 w4_to_e4m3_lut(uint32_t w) {
+  const uint32_t idx = w & 0x77777777u;
+  const uint32_t t = w & 0x88888888u;
+  const uint32_t msel = t | (t >> 3);  // nibble 0x9 (sign of byte 1 = 0xFF) when negative
+  const uint32_t pl = prmt(0x44403800u, 0x4E4C4A48u, idx);
+  const uint32_t ph = prmt(0x44403800u, 0x4E4C4A48u, idx >> 16);
+  const uint32_t nl = prmt(0xCACCCED0u, 0xB8C0C4C8u, idx);
+  const uint32_t nh = prmt(0xCACCCED0u, 0xB8C0C4C8u, idx >> 16);
+  const uint32_t ml = prmt(0x00008000u, 0u, msel);
+  const uint32_t mh = prmt(0x00008000u, 0u, msel >> 16);
+  return make_uint2((pl & ~ml) | (nl & ml), (ph & ~mh) | (nh & mh));
+}
+
+// 8 int4 values in the subnormal bank order (byte b: low nibble = element b, high nibble =
+// element b+4) -> e4m3 codes of q * 2^-9.  Those codes are the integer in sign-magnitude
+// form: q >= 0 -> q; q < 0 -> 0x80 | -q (for the nibble x = q + 16: 0x90 - x).
+__device__ __forceinline__ uint2 w4_to_e4m3_sub(uint32_t w) {
+  const uint32_t lo = w & 0x0F0F0F0Fu;
+  const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
+  const uint32_t ml = prmt(w << 4, 0u, 0xBA98u);  // 0xFF per negative element 0..3
+  const uint32_t mh = prmt(w, 0u, 0xBA98u);       // 0xFF per negative element 4..7
+  const uint32_t dl = 0x90909090u - lo;
+  const uint32_t dh = 0x90909090u - hi;
+  return make_uint2((lo & ~ml) | (dl & ml), (hi & ~mh) | (dh & mh));
+}
+
+struct TileInfo {
+  int e, row0, rows, n0;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(int t, int nt_count, int bn, const int* s_off,
+                                                const int* s_mtp, int E) {
+  const int mt = t / nt_count;
+  const int nt = t - mt * nt_count;
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_mtp[mid] <= mt) lo = mid; else hi = mid;
+  }
+  TileInfo ti;
+  ti.e = lo;
+  ti.row0 = s_off[lo] + (mt - s_mtp[lo]) * 128;
+  ti.rows = min(128, s_off[lo + 1] - ti.row0);
+  ti.n0 = nt * bn;
+  return ti;
+}
+
+// Wait that ignores the abort flag (used to drain copies/MMAs already in flight).
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitBudgetCycles) return;
+  }
+}
+
+template <int BN, int BFMT, int EPI>
+__global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  using C = Cfg<BN, BFMT, EPI>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  const uint32_t bar_full = smem_u32(bars);
+  const uint32_t bar_empty = bar_full + 8 * C::kNS;
+  const uint32_t bar_ufull = bar_empty + 8 * C::kNS;
+  const uint32_t bar_uempty = bar_ufull + 8 * C::kNU;
+  const uint32_t bar_tfull = bar_uempty + 8 * C::kNU;
+  const uint32_t bar_tempty = bar_tfull + 16;
+  const uint32_t bar_drain = bar_tempty + 16;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  int* s_off = reinterpret_cast<int*>(smem + C::kOffOffs);
+  int* s_mtp = reinterpret_cast<int*>(smem + C::kOffMtp);
+  float* s_red = reinterpret_cast<float*>(smem + C::kOffRed);
+
+  const int E = p.E;
+  const int G = p.G;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kNS; ++i) {
+      mbar_init(bar_full + 8 * i, 1);
+      mbar_init(bar_empty + 8 * i, C::kInt4 ? 5 : 1);
+    }
+    for (int i = 0; i < C::kNU; ++i) {
+      mbar_init(bar_ufull + 8 * i, 4);
+      mbar_init(bar_uempty + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_tfull + 8 * i, 1);
+      mbar_init(bar_tempty + 8 * i, C::kEpiWarps);
+    }
+    mbar_init(bar_drain, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (p.offsets) {
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = p.offsets[i];
+  } else if (threadIdx.x == 0) {
+    s_off[0] = 0;
+    s_off[1] = p.dense_rows;
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(s_tmem), C::kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive prefix of per-expert m-tile counts
+    int carry = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int cnt = e < E ? (s_off[e + 1] - s_off[e] + 127) / 128 : 0;
+      int incl = cnt;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+      }
+      if (e < E) s_mtp[e] = carry + incl - cnt;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) s_mtp[E] = carry;
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int nt_count = p.N / BN;
+  const int total_tiles = s_mtp[E] * nt_count;
+
+  if (warp < 4) {
+    // ------------------------------------------------------------------ unpack (WG0)
+    if constexpr (C::kGroupScale) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsLow));
+    if constexpr (C::kInt4) {
+      const int tid = threadIdx.x;  // 0..127
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        for (int g = 0; g < G; ++g, ++it) {
+          const uint32_t s = it % C::kNS, u = it % C::kNU;
+          if (!mbar_wait(bar_full + 8 * s, (it / C::kNS) & 1, s_abort, p.status) ||
+              !mbar_wait(bar_uempty + 8 * u, ((it / C::kNU) & 1) ^ 1, s_abort, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* src = smem + C::kOffB + s * C::kBLoadBytes;
+          uint8_t* dst = smem + C::kOffBU + u * C::kBUBytes;
+#pragma unroll 4
+          for (int unit = tid; unit < BN * 8; unit += 128) {
+            const int row = unit >> 3, j = unit & 7;
+            const uint2 w = *reinterpret_cast<const uint2*>(src + row * 64 + j * 8);
+            uint2 a, b;
+            if constexpr (BFMT == kBfmtInt4Sub) {
+              a = w4_to_e4m3_sub(w.x);
+              b = w4_to_e4m3_sub(w.y);
+            } else {
+              a = w4_to_e4m3_lut(w.x);
+              b = w4_to_e4m3_lut(w.y);
+            }
+            *reinterpret_cast<uint4*>(dst + row * 128 + ((j ^ (row & 7)) << 4)) =
+                make_uint4(a.x, a.y, b.x, b.y);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(bar_ufull + 8 * u);
+            mbar_arrive(bar_empty + 8 * s);
+          }
+        }
+      }
+    }
+  } else if (warp < 8) {
+    if constexpr (C::kGroupScale) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsLow));
+    if (warp == 4 && lane == 0) {
+      // ---------------------------------------------------------------- TMA producer
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile(t, nt_count, BN, s_off, s_mtp, E);
+        for (int g = 0; g < G; ++g, ++it) {
+          const uint32_t s = it % C::kNS;
+          if (!mbar_wait(bar_empty + 8 * s, ((it / C::kNS) & 1) ^ 1, s_abort, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar_full + 8 * s, C::kStageBytes);
+          tma_load_2d(smem_u32(smem + C::kOffA + s * C::kABytes), &tmA, bar_full + 8 * s,
+                      g * 128, ti.row0);
+          if constexpr (C::kInt4) {
+            tma_load_2d(smem_u32(smem + C::kOffB + s * C::kBLoadBytes), &tmB, bar_full + 8 * s,
+                        g * 64, ti.e * p.N + ti.n0);
+          } else {
+            tma_load_2d(smem_u32(smem + C::kOffB + s * C::kBLoadBytes), &tmB, bar_full + 8 * s,
+                        g * 128, ti.n0);
+          }
+        }
+      }
+      // drain: every issued stage must have landed before the CTA can exit
+      const uint32_t issued = it;
+      const uint32_t first = issued > static_cast<uint32_t>(C::kNS) ? issued - C::kNS : 0;
+      for (uint32_t i = first; i < issued; ++i)
+        mbar_wait_drain(bar_full + 8 * (i % C::kNS), (i / C::kNS) & 1);
+    } else if (warp == 5 && lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = make_idesc_e4m3(128, BN);
+      uint32_t it = 0, ait = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        uint32_t a = ait & 1;
+        if constexpr (!C::kGroupScale) {
+          if (!mbar_wait(bar_tempty + 8 * a, ((ait >> 1) & 1) ^ 1, s_abort, p.status)) break;
+          tc_fence_after();
+        }
+        for (int g = 0; g < G; ++g, ++it) {
+          const uint32_t s = it % C::kNS;
+          if (!mbar_wait(bar_full + 8 * s, (it / C::kNS) & 1, s_abort, p.status)) {
+            ok = false;
+            break;
+          }
+          uint32_t b_base;
+          const uint32_t u = it % (C::kNU ? C::kNU : 1);
+          if constexpr (C::kInt4) {
+            if (!mbar_wait(bar_ufull + 8 * u, (it / C::kNU) & 1, s_abort, p.status)) {
+              ok = false;
+              break;
+            }
+            b_base = smem_u32(smem + C::kOffBU + u * C::kBUBytes);
+          } else {
+            b_base = smem_u32(smem + C::kOffB + s * C::kBLoadBytes);
+          }
+          if constexpr (C::kGroupScale) {
+            a = ait & 1;
+            if (!mbar_wait(bar_tempty + 8 * a, ((ait >> 1) & 1) ^ 1, s_abort, p.status)) {
+              ok = false;
+              break;
+            }
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + C::kOffA + s * C::kABytes);
+          const uint32_t d_tmem = tmem_base + a * BN;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t acc = (kk > 0 || (!C::kGroupScale && g > 0)) ? 1u : 0u;
+            mma_f8f6f4(d_tmem, make_sdesc_sw128(a_base + kk * 32),
+                       make_sdesc_sw128(b_base + kk * 32), idesc, acc);
+          }
+          mma_commit(bar_empty + 8 * s);
+          if constexpr (C::kInt4) mma_commit(bar_uempty + 8 * u);
+          if constexpr (C::kGroupScale) {
+            mma_commit(bar_tfull + 8 * a);
+            ++ait;
+          }
+        }
+        if constexpr (!C::kGroupScale) {
+          if (!ok) break;
+          mma_commit(bar_tfull + 8 * a);
+          ++ait;
+        }
+      }
+      // drain: all MMAs issued by this thread complete before TMEM is released
+      mma_commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0);
+    }
+  } else {
+    // -------------------------------------------------------------------- epilogue
+    if constexpr (C::kGroupScale) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsHigh));
+    const int ewarp = warp - 8;
+    const int wg = ewarp >> 2;
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int r_in = q * 32 + lane;
+    const int col_a = wg * 64, col_b = BN / 2 + wg * 64;
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    float tensor_scale = 1.0f;
+    if constexpr (!C::kGroupScale) tensor_scale = __ldg(p.sa_tensor) * __ldg(p.sw_tensor);
+    uint32_t ait = 0;
+    int tile_parity = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, tile_parity ^= 1) {
+      const TileInfo ti = decode_tile(t, nt_count, BN, s_off, s_mtp, E);
+      const bool valid = r_in < ti.rows;
+      const int row = ti.row0 + r_in;
+      if constexpr (C::kGroupScale) {
+        float acc[128];
+#pragma unroll
+        for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+        for (int g = 0; g < G; ++g) {
+          const uint32_t a = ait & 1;
+          const float sa = valid ? __ldg(p.as + static_cast<size_t>(row) * G + g) : 0.0f;
+          const float* swp = p.sw + (static_cast<size_t>(ti.e) * G + g) * p.N + ti.n0;
+          if (!mbar_wait(bar_tfull + 8 * a, (ait >> 1) & 1, s_abort, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t tb = tmem_base + lane_addr + a * BN;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int col = (c < 4) ? col_a + c * 16 : col_b + (c - 4) * 16;
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(tb + col, v);
+            tmem_wait_ld();
+            const float4* sw4 = reinterpret_cast<const float4*>(swp + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float4 w = __ldg(sw4 + i);
+              float* ac = acc + c * 16 + 4 * i;
+              ac[0] = fmaf(sa * w.x, __uint_as_float(v[4 * i + 0]), ac[0]);
+              ac[1] = fmaf(sa * w.y, __uint_as_float(v[4 * i + 1]), ac[1]);
+              ac[2] = fmaf(sa * w.z, __uint_as_float(v[4 * i + 2]), ac[2]);
+              ac[3] = fmaf(sa * w.w, __uint_as_float(v[4 * i + 3]), ac[3]);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_tempty + 8 * a);
+          ++ait;
+        }
+        if (!ok) break;
+        if constexpr (EPI == kEpiSwiglu) {
+          // columns [col_a, col_a+64) are gate rows i, [col_b, col_b+64) the matching up rows
+          float amax = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            const float gt = acc[i];
+            const float h = __fdiv_rn(gt, 1.0f + expf(-gt)) * acc[64 + i];
+            acc[i] = h;
+            amax = fmaxf(amax, fabsf(h));
+          }
+          float* red = s_red + tile_parity * 256;
+          red[wg * 128 + r_in] = amax;
+          asm volatile("bar.sync 1, %0;" ::"n"(C::kEpiThreads) : "memory");
+          const float amax_all = fmaxf(red[r_in], red[128 + r_in]);
+          const float s = scale_from_amax(amax_all);
+          if (valid) {
+            const int inter = p.N / 2;
+            uint8_t* hq = reinterpret_cast<uint8_t*>(p.out) + static_cast<size_t>(row) * inter +
+                          (ti.n0 / 2) + wg * 64;
+#pragma unroll
+            for (int i = 0; i < 64; i += 16) {
+              uint4 o;
+              o.x = cvt_e4m3x4(__fdiv_rn(acc[i + 0], s), __fdiv_rn(acc[i + 1], s),
+                               __fdiv_rn(acc[i + 2], s), __fdiv_rn(acc[i + 3], s));
+              o.y = cvt_e4m3x4(__fdiv_rn(acc[i + 4], s), __fdiv_rn(acc[i + 5], s),
+                               __fdiv_rn(acc[i + 6], s), __fdiv_rn(acc[i + 7], s));
+              o.z = cvt_e4m3x4(__fdiv_rn(acc[i + 8], s), __fdiv_rn(acc[i + 9], s),
+                               __fdiv_rn(acc[i + 10], s), __fdiv_rn(acc[i + 11], s));
+              o.w = cvt_e4m3x4(__fdiv_rn(acc[i + 12], s), __fdiv_rn(acc[i + 13], s),
+                               __fdiv_rn(acc[i + 14], s), __fdiv_rn(acc[i + 15], s));
+              *reinterpret_cast<uint4*>(hq + i) = o;
+            }
+            if (wg == 0) p.out_scales[static_cast<size_t>(row) * (inter / 128) + ti.n0 / 256] = s;
+          }
+        } else if (valid) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int col = (c < 2) ? col_a + c * 32 : col_b + (c - 2) * 32;
+            if constexpr (EPI == kEpiF32) {
+              float* o = reinterpret_cast<float*>(p.out) + static_cast<size_t>(row) * p.N + ti.n0 + col;
+#pragma unroll
+              for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4*>(o + i) =
+                    make_float4(acc[c * 32 + i], acc[c * 32 + i + 1], acc[c * 32 + i + 2], acc[c * 32 + i + 3]);
+            } else {
+              __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * p.N + ti.n0 + col;
+#pragma unroll
+              for (int i = 0; i < 32; i += 8)
+                *reinterpret_cast<uint4*>(o + i) = make_uint4(
+                    pack_bf16x2(acc[c * 32 + i], acc[c * 32 + i + 1]),
+                    pack_bf16x2(acc[c * 32 + i + 2], acc[c * 32 + i + 3]),
+                    pack_bf16x2(acc[c * 32 + i + 4], acc[c * 32 + i + 5]),
+                    pack_bf16x2(acc[c * 32 + i + 6], acc[c * 32 + i + 7]));
+            }
+          }
+        }
+      } else {
+        // per-tensor scales: the whole K accumulated in TMEM; one scalar in the epilogue
+        const uint32_t a = ait & 1;
+        if (!mbar_wait(bar_tfull + 8 * a, (ait >> 1) & 1, s_abort, p.status)) break;
+        tc_fence_after();
+        const uint32_t tb = tmem_base + lane_addr + a * BN;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          const int col = (c < 2) ? col_a + c * 32 : col_b + (c - 2) * 32;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tb + col, v);
+          tmem_wait_ld();
+          if (valid) {
+            if constexpr (EPI == kEpiF32) {
+              float* o = reinterpret_cast<float*>(p.out) + static_cast<size_t>(row) * p.N + ti.n0 + col;
+#pragma unroll
+              for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4*>(o + i) = make_float4(
+                    tensor_scale * __uint_as_float(v[i]), tensor_scale * __uint_as_float(v[i + 1]),
+                    tensor_scale * __uint_as_float(v[i + 2]), tensor_scale * __uint_as_float(v[i + 3]));
+            } else {
+              __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * p.N + ti.n0 + col;
+#pragma unroll
+              for (int i = 0; i < 32; i += 8)
+                *reinterpret_cast<uint4*>(o + i) = make_uint4(
+                    pack_bf16x2(tensor_scale * __uint_as_float(v[i]), tensor_scale * __uint_as_float(v[i + 1])),
+                    pack_bf16x2(tensor_scale * __uint_as_float(v[i + 2]), tensor_scale * __uint_as_float(v[i + 3])),
+                    pack_bf16x2(tensor_scale * __uint_as_float(v[i + 4]), tensor_scale * __uint_as_float(v[i + 5])),
+                    pack_bf16x2(tensor_scale * __uint_as_float(v[i + 6]), tensor_scale * __uint_as_float(v[i + 7])));
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_tempty + 8 * a);
+        ++ait;
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------------- teardown
+  __syncwarp();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// -------------------------------------------------------------------------------------
+// host side
+// -------------------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+static bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                        uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, int BFMT, int EPI>
+static cudaError_t run(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st) {
+  using C = Cfg<BN, BFMT, EPI>;
+  auto kern = grouped_gemm_kernel<BN, BFMT, EPI>;
+  static bool configured = false;
+  static int regs = 0;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    regs = attr.numRegs;
+    configured = true;
+  }
+  if (C::kGroupScale) {
+    // the register split must fit in what the CTA is launched with, or the growing
+    // warpgroups would wait forever
+    const long need = 256L * C::kRegsLow + static_cast<long>(C::kEpiThreads) * C::kRegsHigh;
+    if (static_cast<long>(regs) * C::kThreads < need || regs < C::kRegsLow) {
+      *st = FGE_ERR_UNSUPPORTED_DEVICE;
+      return cudaSuccess;
+    }
+  }
+  CUtensorMap tmA, tmB;
+  if (!make_map_u8(&tmA, a.aq, a.K, a.R, 128, 128, true)) {
+    *st = FGE_ERR_CUDA;
+    return cudaSuccess;
+  }
+  bool okB;
+  if (C::kInt4)
+    okB = make_map_u8(&tmB, a.w, a.K / 2, static_cast<uint64_t>(a.E) * a.N, 64, BN, false);
+  else
+    okB = make_map_u8(&tmB, a.w, a.K, a.N, 128, BN, true);
+  if (!okB) {
+    *st = FGE_ERR_CUDA;
+    return cudaSuccess;
+  }
+  GemmParams p;
+  p.as = a.as;
+  p.sw = a.per_tensor ? nullptr : a.sw;
+  p.sa_tensor = a.sa_tensor;
+  p.sw_tensor = a.per_tensor ? a.sw : nullptr;
+  p.offsets = a.offsets;
+  p.out = a.out;
+  p.out_scales = a.out_scales;
+  p.status = a.status;
+  p.E = a.E;
+  p.N = static_cast<int>(a.N);
+  p.K = static_cast<int>(a.K);
+  p.G = static_cast<int>(a.K / 128);
+  p.dense_rows = static_cast<int>(a.R);
+  const long tiles_bound = (a.R / 128 + a.E) * (a.N / BN);
+  const int grid = static_cast<int>(std::max<long>(1, std::min<long>(num_sms(), tiles_bound)));
+  kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(tmA, tmB, p);
+  *st = FGE_OK;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st) {
+  const bool bn256 = (a.N % 256) == 0;
+  if (a.per_tensor) {
+    if (a.epilogue == 0) return bn256 ? run<256, kBfmtE4m3, kEpiF32>(a, s, st) : run<128, kBfmtE4m3, kEpiF32>(a, s, st);
+    return bn256 ? run<256, kBfmtE4m3, kEpiBf16>(a, s, st) : run<128, kBfmtE4m3, kEpiBf16>(a, s, st);
+  }
+  if (a.bank_format == kBankSubnormal) {
+    if (a.epilogue == 2) return run<256, kBfmtInt4Sub, kEpiSwiglu>(a, s, st);
+    if (a.epilogue == 0) return bn256 ? run<256, kBfmtInt4Sub, kEpiF32>(a, s, st) : run<128, kBfmtInt4Sub, kEpiF32>(a, s, st);
+    return bn256 ? run<256, kBfmtInt4Sub, kEpiBf16>(a, s, st) : run<128, kBfmtInt4Sub, kEpiBf16>(a, s, st);
+  }
+  if (a.epilogue == 2) return run<256, kBfmtInt4Lut, kEpiSwiglu>(a, s, st);
+  if (a.epilogue == 0) return bn256 ? run<256, kBfmtInt4Lut, kEpiF32>(a, s, st) : run<128, kBfmtInt4Lut, kEpiF32>(a, s, st);
+  return bn256 ? run<256, kBfmtInt4Lut, kEpiBf16>(a, s, st) : run<128, kBfmtInt4Lut, kEpiBf16>(a, s, st);
+}
+
+// -------------------------------------------------------------------------------------
+// Load-time prepack of an int4 bank and its scales.
+// -------------------------------------------------------------------------------------
+__global__ void w4_prepack_kernel(const uint32_t* __restrict__ w, uint32_t* __restrict__ wd,
+                                  int E, int64_t N, int64_t words_per_row, int interleave,
+                                  int fmt) {
+  const int64_t total = static_cast<int64_t>(E) * N * words_per_row;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t wi = i % words_per_row;
+    const int64_t rd = (i / words_per_row) % N;  // destination row
+    const int64_t e = i / (words_per_row * N);
+    int64_t rs = rd;
+    if (interleave) {
+      const int64_t tile = rd / 256, within = rd % 256;
+      rs = within < 128 ? tile * 128 + within : N / 2 + tile * 128 + (within - 128);
+    }
+    uint32_t v = w[(e * N + rs) * words_per_row + wi];
+    if (fmt == kBankSubnormal) {
+      // nibble i holds element i; regroup so byte b holds elements b (low) and b+4 (high)
+      uint32_t o = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        o |= ((v >> (4 * b)) & 0xFu) << (8 * b);
+        o |= ((v >> (4 * (b + 4))) & 0xFu) << (8 * b + 4);
+      }
+      v = o;
+    }
+    wd[i] = v;
+  }
+}
+
+__global__ void w4_prepack_scale_kernel(const float* __restrict__ sw, float* __restrict__ sd,
+                                        int E, int64_t N, int G, int interleave, float mult) {
+  const int64_t total = static_cast<int64_t>(E) * N * G;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t nd = i % N;  // destination layout [E, G, N]
+    const int64_t g = (i / N) % G;
+    const int64_t e = i / (N * G);
+    int64_t rs = nd;
+    if (interleave) {
+      const int64_t tile = nd / 256, within = nd % 256;
+      rs = within < 128 ? tile * 128 + within : N / 2 + tile * 128 + (within - 128);
+    }
+    sd[i] = sw[(e * N + rs) * G + g] * mult;
+  }
+}
+
+cudaError_t launch_w4_prepack(const uint8_t* w, const float* sw, int E, int64_t N, int64_t K,
+                              int interleave, int fmt, uint8_t* w_dev, float* sw_dev,
+                              cudaStream_t s) {
+  const int grid = num_sms() * 4;
+  w4_prepack_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint32_t*>(w),
+                                         reinterpret_cast<uint32_t*>(w_dev), E, N, K / 8,
+                                         interleave, fmt);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  w4_prepack_scale_kernel<<<grid, 256, 0, s>>>(sw, sw_dev, E, N, static_cast<int>(K / 128),
+                                               interleave,
+                                               fmt == kBankSubnormal ? 512.0f : 1.0f);
+  return cudaGetLastError();
+}
+
+// -------------------------------------------------------------------------------------
+// Unfused SwiGLU + requant (parity and ablation of the fused epilogue): one warp per
+// (row, 128-group of I), four values per lane.
+// -------------------------------------------------------------------------------------
+__global__ void swiglu_quant_kernel(const float* __restrict__ c, int64_t R, int64_t I,
+                                    uint8_t* __restrict__ hq, float* __restrict__ hs) {
+  const int lane = threadIdx.x & 31;
+  const int64_t groups = I / 128;
+  const int64_t total = R * groups;
+  const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t item = wid; item < total; item += nw) {
+    const int64_t r = item / groups, g = item % groups;
+    const float* gate = c + r * 2 * I + g * 128 + lane * 4;
+    const float4 gv = *reinterpret_cast<const float4*>(gate);
+    const float4 uv = *reinterpret_cast<const float4*>(gate + I);
+    float h[4] = {__fdiv_rn(gv.x, 1.0f + expf(-gv.x)) * uv.x, __fdiv_rn(gv.y, 1.0f + expf(-gv.y)) * uv.y,
+                  __fdiv_rn(gv.z, 1.0f + expf(-gv.z)) * uv.z, __fdiv_rn(gv.w, 1.0f + expf(-gv.w)) * uv.w};
+    float amax = fmaxf(fmaxf(fabsf(h[0]), fabsf(h[1])), fmaxf(fabsf(h[2]), fabsf(h[3])));
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    const float s = scale_from_amax(amax);
+    *reinterpret_cast<uint32_t*>(hq + r * I + g * 128 + lane * 4) =
+        cvt_e4m3x4(__fdiv_rn(h[0], s), __fdiv_rn(h[1], s), __fdiv_rn(h[2], s), __fdiv_rn(h[3], s));
+    if (lane == 0) hs[r * groups + g] = s;
+  }
+}
+
+cudaError_t launch_swiglu_quant(const float* c, int64_t R, int64_t I, uint8_t* hq, float* hs,
+                                cudaStream_t s) {
+  if (R == 0) return cudaSuccess;
+  const int64_t warps = R * (I / 128);
+  const int grid = static_cast<int>(std::min<int64_t>((warps + 7) / 8, num_sms() * 16));
+  swiglu_quant_kernel<<<grid, 256, 0, s>>>(c, R, I, hq, hs);
+  return cudaGetLastError();
+}
+
+}  // namespace fge

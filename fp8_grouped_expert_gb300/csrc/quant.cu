@@ -1,0 +1,116 @@
+// fp8_quant_act: dynamic e4m3 activation quantization, per (row, 128-element group) or per
+// tensor ("FP8 grouped-expert prefill with on-chip int4-to-e4m3 dequant", section 1;
+// "Module fp8_ffi": amax reduce -> scale finalize -> e4m3 quantize on one stream).
+// HBM-bound: 16-byte vector loads and stores, warp-shuffle amax, grids sized to the SMs.
+#include <algorithm>
+
+#include "fge_device.cuh"
+
+namespace fge {
+
+// One 128-value group per 16 lanes; each lane converts 8 bf16 (one 16-byte load).
+__global__ void quant_g128_kernel(const uint4* __restrict__ x, int64_t groups,
+                                  uint2* __restrict__ xq, float* __restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4, hl = lane & 15;
+  const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t g0 = wid * 2; g0 < groups; g0 += nw * 2) {
+    const int64_t g = g0 + half;
+    const bool valid = g < groups;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (valid) v = __ldcs(x + g * 16 + hl);
+    float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                  bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+    for (int d = 8; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    const float s = scale_from_amax(amax);
+    uint2 q;
+    q.x = cvt_e4m3x4(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
+    q.y = cvt_e4m3x4(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s), __fdiv_rn(f[7], s));
+    if (valid) {
+      xq[g * 16 + hl] = q;
+      if (hl == 0) xs[g] = s;
+    }
+  }
+}
+
+// Per-tensor pass 1: amax over the tensor, combined across blocks with atomicMax on the
+// float bits (|x| >= 0, so the unsigned order of the bits is the float order).
+__global__ void amax_kernel(const uint4* __restrict__ x, int64_t n8, uint32_t* __restrict__ amax_bits) {
+  float m = 0.0f;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 v = __ldg(x + i);
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
+                       fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)))));
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))),
+                       fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)))));
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+  __shared__ float red[32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+    if (threadIdx.x == 0) atomicMax(amax_bits, __float_as_uint(m));
+  }
+}
+
+// Per-tensor pass 2: every thread derives the same scale from the amax word and casts.
+__global__ void cast_per_tensor_kernel(const uint4* __restrict__ x, int64_t n8,
+                                       const uint32_t* __restrict__ amax_bits,
+                                       uint2* __restrict__ xq, float* __restrict__ xs,
+                                       float* __restrict__ scale_out) {
+  const float s = scale_from_amax(__uint_as_float(*amax_bits));
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    xs[0] = s;
+    if (scale_out) *scale_out = s;
+  }
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 v = __ldg(x + i);
+    uint2 q;
+    q.x = cvt_e4m3x4(__fdiv_rn(bf16_lo(v.x), s), __fdiv_rn(bf16_hi(v.x), s),
+                     __fdiv_rn(bf16_lo(v.y), s), __fdiv_rn(bf16_hi(v.y), s));
+    q.y = cvt_e4m3x4(__fdiv_rn(bf16_lo(v.z), s), __fdiv_rn(bf16_hi(v.z), s),
+                     __fdiv_rn(bf16_lo(v.w), s), __fdiv_rn(bf16_hi(v.w), s));
+    xq[i] = q;
+  }
+}
+
+cudaError_t launch_quant_g128(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,
+                              cudaStream_t s) {
+  const int64_t groups = M * (K / 128);
+  if (groups == 0) return cudaSuccess;
+  const int64_t warps = (groups + 1) / 2;
+  const int grid = static_cast<int>(std::min<int64_t>((warps + 7) / 8, num_sms() * 8));
+  quant_g128_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), groups,
+                                         reinterpret_cast<uint2*>(xq), xs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_per_tensor(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq,
+                                    float* xs, WsHeader* hdr, cudaStream_t s) {
+  const int64_t n8 = M * K / 8;
+  cudaError_t e = cudaMemsetAsync(&hdr->amax_bits, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) return e;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((n8 + 255) / 256, num_sms() * 4)));
+  if (n8 > 0) {
+    amax_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), n8, &hdr->amax_bits);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  cast_per_tensor_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), n8,
+                                              &hdr->amax_bits, reinterpret_cast<uint2*>(xq), xs,
+                                              &hdr->scale);
+  return cudaGetLastError();
+}
+
+}  // namespace fge

@@ -1,0 +1,299 @@
+// Routing kernels around the grouped GEMM: top-k gate, the expert permutation (histogram ->
+// exclusive scan -> stable rank -> row copy) and the gate-weighted combine.  The pages
+// replace per-token expert dispatch by one grouped GEMM ("FP8 grouped-expert prefill with
+// on-chip int4-to-e4m3 dequant", section 1); these kernels make the routed rows of each
+// expert contiguous and bring the expert outputs back to token order.  All are
+// deterministic: ranks come from warp-synchronous scans, never from atomic order.
+#include <algorithm>
+#include <cfloat>
+
+#include "fge_device.cuh"
+
+namespace fge {
+
+constexpr int kChunkTokens = 128;  // tokens per permutation chunk
+
+// ------------------------------------------------------------------------------ top-k
+template <int PER>
+__global__ void topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k,
+                            int32_t* __restrict__ ids, float* __restrict__ gates) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t t = wid; t < T; t += nw) {
+    float v[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = e < E ? __ldg(logits + t * E + e) : -FLT_MAX;
+    }
+    uint32_t taken = 0;
+    float my_val = 0.0f;
+    int my_id = 0;
+    for (int j = 0; j < k; ++j) {
+      float best = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && (v[i] > best || (v[i] == best && e < bi))) {
+          best = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best, d);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
+        if (ov > best || (ov == best && oi < bi)) {
+          best = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == j) {
+        my_val = best;
+        my_id = bi;
+      }
+    }
+    const float m = __shfl_sync(0xffffffffu, my_val, 0);
+    const float ex = lane < k ? expf(my_val - m) : 0.0f;
+    float sum = ex;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
+    if (lane < k) {
+      ids[t * k + lane] = my_id;
+      gates[t * k + lane] = __fdiv_rn(ex, sum);
+    }
+  }
+}
+
+cudaError_t launch_topk_gate(const float* logits, int64_t T, int E, int k, int32_t* ids,
+                             float* gates, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int grid = static_cast<int>(std::min<int64_t>((T + 7) / 8, num_sms() * 16));
+  const int per = (E + 31) / 32;
+  if (per <= 1) topk_kernel<1><<<grid, 256, 0, s>>>(logits, T, E, k, ids, gates);
+  else if (per <= 2) topk_kernel<2><<<grid, 256, 0, s>>>(logits, T, E, k, ids, gates);
+  else if (per <= 4) topk_kernel<4><<<grid, 256, 0, s>>>(logits, T, E, k, ids, gates);
+  else if (per <= 8) topk_kernel<8><<<grid, 256, 0, s>>>(logits, T, E, k, ids, gates);
+  else if (per <= 16) topk_kernel<16><<<grid, 256, 0, s>>>(logits, T, E, k, ids, gates);
+  else topk_kernel<32><<<grid, 256, 0, s>>>(logits, T, E, k, ids, gates);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------ permutation
+size_t permute_scratch_bytes(int64_t T, int E) {
+  const int64_t chunks = (T + kChunkTokens - 1) / kChunkTokens;
+  return align_up(static_cast<size_t>(chunks) * E * sizeof(int32_t), 256);
+}
+
+// (1) per-chunk expert histogram
+__global__ void permute_count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int E,
+                                     int32_t* __restrict__ chunk_counts) {
+  extern __shared__ int hist[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kChunkTokens;
+  const int64_t n = (T - t0 < kChunkTokens ? T - t0 : static_cast<int64_t>(kChunkTokens)) * k;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&hist[ids[t0 * k + i]], 1);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    chunk_counts[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
+}
+
+// (2) exclusive scan: offsets[e] and, in place, the first row of (chunk, expert)
+__global__ void permute_scan_kernel(int32_t* __restrict__ chunk_counts, int64_t chunks, int E,
+                                    int32_t* __restrict__ offsets) {
+  __shared__ int totals[1024];
+  __shared__ int warp_sums[32];
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < E) {
+    for (int64_t c = 0; c < chunks; ++c) {
+      const int cnt = chunk_counts[c * E + e];
+      chunk_counts[c * E + e] = run;
+      run += cnt;
+    }
+  }
+  // block-wide exclusive scan of the per-expert totals
+  const int lane = e & 31, w = e >> 5;
+  int incl = run;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) warp_sums[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int ws = lane < (blockDim.x >> 5) ? warp_sums[lane] : 0;
+    int wi = ws;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, wi, d);
+      if (lane >= d) wi += v;
+    }
+    warp_sums[lane] = wi - ws;
+  }
+  __syncthreads();
+  const int excl = warp_sums[w] + incl - run;
+  totals[e] = excl;
+  if (e < E) offsets[e] = excl;
+  if (e == E - 1) offsets[E] = excl + run;
+  __syncthreads();
+  if (e < E) {
+    for (int64_t c = 0; c < chunks; ++c) chunk_counts[c * E + e] += totals[e];
+  }
+}
+
+// (3) stable rank: one warp walks its chunk in (token, slot) order.  Lanes hold
+// consecutive entries; a token's k experts are distinct, so lanes sharing an expert
+// belong to different tokens and their lane order is the token order.
+__global__ void permute_rank_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int E,
+                                    const int32_t* __restrict__ chunk_base,
+                                    int32_t* __restrict__ row_token,
+                                    int32_t* __restrict__ token_row) {
+  extern __shared__ int ctr[];
+  const int lane = threadIdx.x;  // one warp per block
+  const int64_t chunk = blockIdx.x;
+  for (int e = lane; e < E; e += 32) ctr[e] = chunk_base[chunk * E + e];
+  __syncwarp();
+  const int64_t t0 = chunk * kChunkTokens;
+  const int64_t n = (T - t0 < kChunkTokens ? T - t0 : static_cast<int64_t>(kChunkTokens)) * k;
+  const int per = (32 / k) * k;  // lanes used per step: whole tokens only
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int64_t base = 0; base < n; base += per) {
+    const int64_t i = base + lane;
+    const bool active = lane < per && i < n;
+    const int e = active ? ids[t0 * k + i] : -1 - lane;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    int r = 0;
+    if (active) r = ctr[e] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (active && (peers >> lane) == 1u) ctr[e] += __popc(peers);  // highest lane of the group
+    __syncwarp();
+    if (active) {
+      row_token[r] = static_cast<int32_t>(t0 + i / k);
+      token_row[t0 * k + i] = r;
+    }
+  }
+}
+
+// (4) copy each token's e4m3 row and scales to its k expert rows: one warp per token,
+// each 512-byte slice read once and written k times.
+__global__ void permute_copy_kernel(const uint8_t* __restrict__ xq, const float* __restrict__ xs,
+                                    int64_t T, int k, int64_t H,
+                                    const int32_t* __restrict__ token_row,
+                                    uint8_t* __restrict__ aq, float* __restrict__ as) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t G = H / 128;
+  for (int64_t t = wid; t < T; t += nw) {
+    const int my_row = lane < k ? __ldg(token_row + t * k + lane) : 0;
+    const uint4* src = reinterpret_cast<const uint4*>(xq + t * H);
+    for (int64_t c0 = 0; c0 < H / 16; c0 += 32) {  // all lanes iterate; shuffles stay full
+      const int64_t c = c0 + lane;
+      const bool in = c < H / 16;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (in) v = __ldcs(src + c);
+      for (int j = 0; j < k; ++j) {
+        const int r = __shfl_sync(0xffffffffu, my_row, j);
+        if (in) reinterpret_cast<uint4*>(aq + static_cast<int64_t>(r) * H)[c] = v;
+      }
+    }
+    for (int64_t g0 = 0; g0 < G; g0 += 32) {
+      const int64_t g = g0 + lane;
+      const bool in = g < G;
+      const float sv = in ? __ldg(xs + t * G + g) : 0.0f;
+      for (int j = 0; j < k; ++j) {
+        const int r = __shfl_sync(0xffffffffu, my_row, j);
+        if (in) as[static_cast<int64_t>(r) * G + g] = sv;
+      }
+    }
+  }
+}
+
+cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, const uint8_t* xq,
+                           const float* xs, int64_t H, int32_t* offsets, int32_t* row_token,
+                           int32_t* token_row, uint8_t* aq, float* as, void* scratch,
+                           cudaStream_t s) {
+  const int64_t chunks = (T + kChunkTokens - 1) / kChunkTokens;
+  int32_t* cc = reinterpret_cast<int32_t*>(scratch);
+  if (chunks > 0) {
+    permute_count_kernel<<<static_cast<int>(chunks), 256, E * sizeof(int), s>>>(ids, T, k, E, cc);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  permute_scan_kernel<<<1, 1024, 0, s>>>(cc, chunks, E, offsets);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || chunks == 0) return e;
+  permute_rank_kernel<<<static_cast<int>(chunks), 32, E * sizeof(int), s>>>(ids, T, k, E, cc,
+                                                                            row_token, token_row);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int grid = static_cast<int>(std::min<int64_t>((T + 7) / 8, num_sms() * 8));
+  permute_copy_kernel<<<grid, 256, 0, s>>>(xq, xs, T, k, H, token_row, aq, as);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- combine
+template <bool YF32, bool OF32>
+__global__ void combine_kernel(const void* __restrict__ y, const int32_t* __restrict__ token_row,
+                               const float* __restrict__ gates, int64_t T, int k, int64_t H,
+                               void* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t t = wid; t < T; t += nw) {
+    const int my_row = lane < k ? __ldg(token_row + t * k + lane) : 0;
+    const float my_gate = lane < k ? __ldg(gates + t * k + lane) : 0.0f;
+    for (int64_t c0 = 0; c0 < H; c0 += 256) {  // all lanes iterate; shuffles stay full
+      const int64_t c = c0 + lane * 8;
+      const bool in = c < H;
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      for (int j = 0; j < k; ++j) {
+        const int64_t r = __shfl_sync(0xffffffffu, my_row, j);
+        const float g = __shfl_sync(0xffffffffu, my_gate, j);
+        float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (!in) {
+        } else if constexpr (YF32) {
+          const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(y) + r * H + c);
+          const float4 a = __ldcs(p), b = __ldcs(p + 1);
+          v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        } else {
+          const uint4 a = __ldcs(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(y) + r * H + c));
+          v[0] = bf16_lo(a.x); v[1] = bf16_hi(a.x); v[2] = bf16_lo(a.y); v[3] = bf16_hi(a.y);
+          v[4] = bf16_lo(a.z); v[5] = bf16_hi(a.z); v[6] = bf16_lo(a.w); v[7] = bf16_hi(a.w);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, v[i], acc[i]);
+      }
+      if (!in) {
+      } else if constexpr (OF32) {
+        float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + t * H + c);
+        o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      } else {
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + t * H + c) =
+            make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                       pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+      }
+    }
+  }
+}
+
+cudaError_t launch_combine(const void* y, int y_f32, const int32_t* token_row,
+                           const float* gates, int64_t T, int k, int64_t H, int out_f32,
+                           void* out, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int grid = static_cast<int>(std::min<int64_t>((T + 7) / 8, num_sms() * 8));
+  if (y_f32 && out_f32) combine_kernel<true, true><<<grid, 256, 0, s>>>(y, token_row, gates, T, k, H, out);
+  else if (y_f32) combine_kernel<true, false><<<grid, 256, 0, s>>>(y, token_row, gates, T, k, H, out);
+  else if (out_f32) combine_kernel<false, true><<<grid, 256, 0, s>>>(y, token_row, gates, T, k, H, out);
+  else combine_kernel<false, false><<<grid, 256, 0, s>>>(y, token_row, gates, T, k, H, out);
+  return cudaGetLastError();
+}
+
+}  // namespace fge

@@ -1,0 +1,226 @@
+/*
+ * fge.h -- C ABI of libfge: W4A8 grouped-expert MoE prefill and dense per-tensor W8A8
+ * projections on one NVIDIA GB300 (sm_103a).
+ *
+ * Source of the method: "FP8 grouped-expert prefill with on-chip int4-to-e4m3 dequant"
+ * (section 1, Contribution): activations quantized on the fly to e4m3, packed int4 expert
+ * weights dequantized to e4m3 on chip without unpacking the resident bank, one grouped
+ * expert GEMM per layer in place of one dispatch per routed token, and per-(token, group)
+ * activation scales folded into the accumulator path.  The per-tensor W8A8 projection and
+ * the "all device work in one call, no host sync" boundary follow "feat(qwen4_exp):
+ * load-time per-tensor FP8 dense projections (W8A8 via _scaled_mm)" (section "What this
+ * adds") and "Module fp8_ffi" (module documentation and struct Fp8Scratch).
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers unless a parameter says "host".  Every tensor is dense
+ *    row-major with the shape given; every pointer must be 16-byte aligned.
+ *  - Ownership: the caller allocates all buffers, including the workspace whose size the
+ *    matching fge_workspace_bytes() query returns.  The library allocates no device memory
+ *    and keeps no per-call state; it only caches per-device properties in fge_init().
+ *  - Streams: all work is enqueued on `stream` (a cudaStream_t; 0 = legacy default) in
+ *    order, with no host synchronisation and no branch on tensor values (shapes only).
+ *  - Errors: argument, shape and alignment problems return a status before anything is
+ *    enqueued.  A launch failure returns FGE_ERR_CUDA.  Problems detected on the device
+ *    (a pipeline wait that ran out of its time budget) are written to the status word at
+ *    the start of the workspace; read it with fge_read_device_status().
+ *  - Sizes: K, H and I are multiples of 128 (the scale group); N is a multiple of 128.
+ */
+#ifndef FGE_H_
+#define FGE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fge_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  FGE_OK = 0,
+  FGE_ERR_INVALID_ARG = 1,        /* null pointer, bad enum, k > E, ... */
+  FGE_ERR_BAD_SHAPE = 2,          /* a size is not a multiple of 128 or out of range */
+  FGE_ERR_MISALIGNED = 3,         /* a pointer is not 16-byte aligned */
+  FGE_ERR_WORKSPACE_TOO_SMALL = 4,
+  FGE_ERR_UNSUPPORTED_DEVICE = 5, /* not sm_103 / kernel resources unavailable */
+  FGE_ERR_CUDA = 6,               /* a CUDA runtime call or launch failed */
+  FGE_ERR_DEVICE_TIMEOUT = 7,     /* device status only: a pipeline wait ran out */
+  FGE_ERR_NOT_INITIALIZED = 8     /* fge_init() was not called for the current device */
+} fge_status;
+
+typedef enum {
+  FGE_SCALE_PER_TENSOR = 0,     /* one amax over the whole [M, K] tensor */
+  FGE_SCALE_PER_TOKEN_G128 = 1  /* one scale per (row, 128-element K group) */
+} fge_scale_mode;
+
+typedef enum { FGE_DTYPE_BF16 = 0, FGE_DTYPE_F32 = 1 } fge_dtype;
+
+typedef enum {
+  FGE_EPI_STORE = 0,          /* write the GEMM result in out_dtype */
+  FGE_EPI_SWIGLU_REQUANT = 1  /* h = silu(gate) * up, then e4m3 per (row, 128 group) */
+} fge_epilogue;
+
+/* Resident int4 bank formats produced by fge_w4_prepack.  Both hold two int4 values per
+ * byte; they differ in how the kernel turns a nibble into an e4m3 tensor-core operand:
+ *  FGE_W4_LUT:       the e4m3 code of the integer itself (byte-permute table lookup);
+ *  FGE_W4_SUBNORMAL: the e4m3 code of q * 2^-9 (the subnormal/normal code whose bits are
+ *                    the integer in sign-magnitude form), with 2^9 folded into the
+ *                    prepacked weight scales.  Both are exact. */
+typedef enum { FGE_W4_LUT = 0, FGE_W4_SUBNORMAL = 1 } fge_w4_format;
+
+typedef enum {
+  FGE_OP_QUANT_PER_TENSOR = 0, /* args: (M, K) */
+  FGE_OP_PERMUTE = 1,          /* args: (T, H, -, E, k) */
+  FGE_OP_GROUPED_GEMM = 2,     /* args: unused */
+  FGE_OP_LINEAR_W8A8 = 3,      /* args: (M, K) */
+  FGE_OP_MOE_LAYER = 4         /* args: (T, H, I, E, k) */
+} fge_op;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int fge_version(void);
+
+/* Checks that `device` is an sm_103 GPU and caches its SM count; sets kernel attributes.
+ * Idempotent; call once per device before any other call on it. */
+fge_status fge_init(int device);
+
+/* Human-readable name of a status code (static string). */
+const char* fge_status_string(fge_status status);
+
+/* Workspace bytes an operation needs for the given sizes (0 for a bad op). */
+size_t fge_workspace_bytes(fge_op op, int64_t a, int64_t b, int64_t c, int E, int k);
+
+/* Zero the device status word of a workspace (enqueued on `stream`). */
+fge_status fge_clear_device_status(void* workspace, fge_stream_t stream);
+
+/* Synchronises `stream`, then copies the workspace's device status word to *out (host). */
+fge_status fge_read_device_status(const void* workspace, fge_stream_t stream, int32_t* out);
+
+/* fp8_quant_act -- dynamic e4m3 activation quantization.
+ * Per "FP8 grouped-expert prefill ..." section 1 (per-(token, group) scale) and "Module
+ * fp8_ffi" (amax reduce, scale finalize, e4m3 quantize, one stream, no host sync):
+ *   amax = max|x| over the group (G128) or the whole tensor (PER_TENSOR);
+ *   s = amax / 448 (IEEE float division; s = 1 when amax = 0; s >= 2^-126);
+ *   q = e4m3(x / s), round to nearest even, saturating at +-448.
+ * x_bf16: [M, K] bf16.  xq: [M, K] e4m3 codes (out).  xs: [M, K/128] float (G128) or one
+ * float (PER_TENSOR) (out).  PER_TENSOR needs a workspace of
+ * fge_workspace_bytes(FGE_OP_QUANT_PER_TENSOR, M, K, ...); G128 takes none (may be NULL).
+ * M may be 0. */
+fge_status fge_fp8_quant_act(const void* x_bf16, int64_t M, int64_t K, fge_scale_mode mode,
+                             uint8_t* xq, float* xs, void* workspace, size_t workspace_bytes,
+                             fge_stream_t stream);
+
+/* moe_topk_gate -- top-k experts per token and their gates.
+ * The pages route tokens to experts without fixing the rule ("FP8 grouped-expert prefill
+ * ..." section 1); this is standard top-k routing: experts in descending logit order (ties
+ * to the lower id), gate_j = exp(l_j - l_max) / sum over the chosen k of exp(l - l_max).
+ * logits: [T, E] float.  ids: [T, k] int32 (out).  gates: [T, k] float (out).
+ * 1 <= k <= min(E, 32), E <= 1024. */
+fge_status fge_moe_topk_gate(const float* logits, int64_t T, int E, int k, int32_t* ids,
+                             float* gates, fge_stream_t stream);
+
+/* moe_permute -- expert-contiguous rows for the single grouped GEMM ("FP8 grouped-expert
+ * prefill ..." section 1: one grouped expert GEMM per layer instead of one dispatch per
+ * routed token).  Histogram of ids, exclusive scan, stable scatter ordered by (expert,
+ * token, slot), then a copy of each token's e4m3 row and group scales to its k rows.
+ * ids: [T, k] int32 in [0, E) (distinct within a row).  xq: [T, H] codes; xs: [T, H/128].
+ * offsets: [E+1] (out); row_token: [T*k] (out); token_row: [T, k] (out);
+ * aq: [T*k, H] (out); as: [T*k, H/128] (out).  Workspace: FGE_OP_PERMUTE. */
+fge_status fge_moe_permute(const int32_t* ids, int64_t T, int k, int E, const uint8_t* xq,
+                           const float* xs, int64_t H, int32_t* offsets, int32_t* row_token,
+                           int32_t* token_row, uint8_t* aq, float* as, void* workspace,
+                           size_t workspace_bytes, fge_stream_t stream);
+
+/* w4_prepack -- load-time layout of a resident int4 expert bank for the grouped GEMM.
+ * Input (canonical): w [E, N, K/2] bytes, two's-complement nibbles, byte b of a row holds
+ * element 2b in the low nibble and 2b+1 in the high nibble; w_scale [E, N, K/128] float.
+ * Output: w_dev [E, N, K/2] in `format` (nibbles regrouped within each 8-element word for
+ * FGE_W4_SUBNORMAL) and w_scale_dev [E, K/128, N] (transposed; times 2^9 for
+ * FGE_W4_SUBNORMAL).  gate_up_interleave = 1 reorders rows so that every 256-row tile
+ * holds 128 gate rows then the 128 matching up rows (gate = rows [0, N/2), up = rows
+ * [N/2, N) of the input); required by FGE_EPI_SWIGLU_REQUANT.  Not part of the timed path. */
+fge_status fge_w4_prepack(const uint8_t* w, const float* w_scale, int E, int64_t N, int64_t K,
+                          int gate_up_interleave, fge_w4_format format, uint8_t* w_dev,
+                          float* w_scale_dev, fge_stream_t stream);
+
+/* grouped_gemm_w4a8 -- one grouped expert GEMM over all routed rows ("FP8 grouped-expert
+ * prefill ..." section 1).  For expert e and rows r in [offsets[e], offsets[e+1]):
+ *   C[r, n] = sum_g as[r, g] * sw[e, n, g] * sum_{k in group g} aq[r, k] * q[e, n, k]
+ * computed with tcgen05 kind::f8f6f4 MMAs (int4 dequantized to e4m3 in shared memory) and
+ * fp32 promotion per K group.  aq: [R, K] e4m3; as: [R, K/128]; offsets: [E+1] on device
+ * (offsets[E] <= R; the host never reads them); w_dev / w_scale_dev from fge_w4_prepack.
+ * FGE_EPI_STORE: out [R, N] in out_dtype (rows past offsets[E] untouched).
+ * FGE_EPI_SWIGLU_REQUANT (needs N % 256 == 0 and an interleaved bank): out = hq [R, N/2]
+ * e4m3, out_scales = hs [R, N/256].  E <= 512.  Workspace: FGE_OP_GROUPED_GEMM. */
+fge_status fge_grouped_gemm_w4a8(const uint8_t* aq, const float* as, const int32_t* offsets,
+                                 int64_t R, const uint8_t* w_dev, const float* w_scale_dev,
+                                 int E, int64_t N, int64_t K, fge_w4_format format,
+                                 fge_epilogue epilogue, fge_dtype out_dtype, void* out,
+                                 float* out_scales, void* workspace, size_t workspace_bytes,
+                                 fge_stream_t stream);
+
+/* swiglu_quant -- unfused SwiGLU + requant (parity/ablation of the fused epilogue):
+ * h = silu(c[:, i]) * c[:, I + i], silu(g) = g / (1 + exp(-g)), then e4m3 per (row, 128
+ * group) as fp8_quant_act.  c: [R, 2I] float.  hq: [R, I]; hs: [R, I/128]. */
+fge_status fge_swiglu_quant(const float* c, int64_t R, int64_t I, uint8_t* hq, float* hs,
+                            fge_stream_t stream);
+
+/* moe_combine -- out[t] = sum_{j=0..k-1} gates[t, j] * y[token_row[t, j]], accumulated in
+ * fp32 in slot order (deterministic; no atomics).  y: [T*k, H] in y_dtype; token_row,
+ * gates: [T, k]; out: [T, H] in out_dtype. */
+fge_status fge_moe_combine(const void* y, fge_dtype y_dtype, const int32_t* token_row,
+                           const float* gates, int64_t T, int k, int64_t H,
+                           fge_dtype out_dtype, void* out, fge_stream_t stream);
+
+/* gemm_w8a8 -- dense per-tensor W8A8 GEMM, the grouped kernel run with one expert
+ * ("feat(qwen4_exp) ..." section "What this adds"; "Module fp8_ffi": activation scale
+ * folded with the weight scale into one device scalar):  y = (sa * sw) * aq @ wq^T.
+ * aq: [M, K] e4m3; sa, sw: device float scalars; wq: [N, K] e4m3; y: [M, N] in out_dtype.
+ * Workspace: FGE_OP_GROUPED_GEMM. */
+fge_status fge_gemm_w8a8(const uint8_t* aq, const float* sa, int64_t M, int64_t K,
+                         const uint8_t* wq, const float* sw, int64_t N, fge_dtype out_dtype,
+                         void* y, void* workspace, size_t workspace_bytes,
+                         fge_stream_t stream);
+
+/* linear_w8a8 -- the whole dense projection in one call, as the "Module fp8_ffi" prefill
+ * call does it: per-tensor amax, scale, e4m3 cast, then the W8A8 GEMM, one stream, no host
+ * sync.  x_bf16: [M, K]; wq: [N, K] e4m3 with device scalar w_scale; y_bf16: [M, N].
+ * Workspace: FGE_OP_LINEAR_W8A8 (holds the quantized activation and the scale block). */
+fge_status fge_linear_w8a8(const void* x_bf16, int64_t M, int64_t K, const uint8_t* wq,
+                           const float* w_scale, int64_t N, void* y_bf16, void* workspace,
+                           size_t workspace_bytes, fge_stream_t stream);
+
+/* moe_layer_forward -- one MoE FFN prefill layer in one call: top-k gate -> G128 quant ->
+ * permute -> gate_up grouped GEMM with fused SwiGLU + requant -> down grouped GEMM ->
+ * combine.  logits: [T, E] float; x_bf16: [T, H]; w_gu_dev / s_gu_dev: prepacked gate_up
+ * bank ([E, 2I, H/2], interleaved) and scales; w_dn_dev / s_dn_dev: prepacked down bank
+ * ([E, H, I/2]) and scales; out: [T, H] in out_dtype (expert outputs are kept in the same
+ * dtype before the combine).  Workspace: FGE_OP_MOE_LAYER with (T, H, I, E, k). */
+fge_status fge_moe_layer_forward(const float* logits, const void* x_bf16, int64_t T, int64_t H,
+                                 int E, int k, int64_t I, const uint8_t* w_gu_dev,
+                                 const float* s_gu_dev, const uint8_t* w_dn_dev,
+                                 const float* s_dn_dev, fge_w4_format format,
+                                 fge_dtype out_dtype, void* out, void* workspace,
+                                 size_t workspace_bytes, fge_stream_t stream);
+
+/* Glue of the stacked prefill (not page steps; RMSNorm, router, attention stand-in).
+ * rmsnorm: out_bf16[t] = h[t] / sqrt(mean(h[t]^2) + eps), h float [T, H].
+ * router_logits: logits[t, e] = sum_h xn[t, h] * w[e, h] (fp32, sequential in h);
+ *   xn bf16 [T, H], w float [E, H].
+ * identity_attention: attn[t, h*128 + d] = v[t, (h / (n_heads / n_kv_heads))*128 + d];
+ *   v bf16 [T, n_kv_heads*128], attn bf16 [T, n_heads*128].
+ * residual_add: h[i] += y[i] for i < n, h float, y in y_dtype. */
+fge_status fge_rmsnorm(const float* h, int64_t T, int64_t H, float eps, void* out_bf16,
+                       fge_stream_t stream);
+fge_status fge_router_logits(const void* xn_bf16, const float* w_router, int64_t T, int64_t H,
+                             int E, float* logits, fge_stream_t stream);
+fge_status fge_identity_attention(const void* v_bf16, int64_t T, int n_heads, int n_kv_heads,
+                                  void* attn_bf16, fge_stream_t stream);
+fge_status fge_residual_add(float* h, const void* y, fge_dtype y_dtype, int64_t n,
+                            fge_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FGE_H_ */

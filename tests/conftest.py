@@ -18,3 +18,13 @@ def cuda_ok():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     return True
+
+
+@pytest.fixture(scope="session")
+def fge(cuda_ok):
+    """The built binding on a CUDA device (builds libfge.so in-tree if needed)."""
+    from fp8_grouped_expert_gb300 import build as _build
+    _build.build()
+    import fp8_grouped_expert_gb300 as mod
+    mod.lib()
+    return mod
