@@ -1,0 +1,354 @@
+"""Benchmark of the W4A8 grouped-expert MoE prefill layer on GB300.
+
+One step = one MoE FFN prefill layer through the C ABI (fge_moe_layer_forward: top-k gate,
+per-(token, 128) e4m3 quant, permute, gate_up grouped GEMM with fused SwiGLU requant, down
+grouped GEMM, combine) on the mid workload: T=4096 tokens, H=2048, 64 experts, I=768,
+top-8, int4 expert banks with 128-group fp32 scales, bf16 activations ~N(0,1).
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead on a bounded
+sample of the same workload.  Under torchrun (N > 1) every rank runs its own replica of the
+workload (weak scaling, no collective on the data path); the step time is the max over
+ranks.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "mid"
+METRIC = "MoE prefill tokens/s; grouped-GEMM TFLOPS as % of GB300 FP8 peak, 1 GPU"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            mp = json.load(f)
+        return float(mp["hbm_gbs"]), float(mp["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = max(smax, float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": smax or None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------- CPU oracle
+def oracle_tokens_per_s(inp, sample_tokens, seconds, seed=0):
+    """Time the CPU oracle on repeated samples of `sample_tokens` tokens for ~`seconds`."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        rows = np.sort(rng.choice(inp.T, size=sample_tokens, replace=False))
+        oracle.moe_layer_forward(inp.logits[rows], inp.x[rows], inp.k, inp.w_gu, inp.s_gu,
+                                 inp.w_dn, inp.s_dn, inp.I, out_dtype=inp.out)
+        done += sample_tokens
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return done / el, done, el
+
+
+def _blas_threads():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count()
+
+
+def run_reference(args):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return 0
+    from workloads import moe_inputs
+    inp = moe_inputs(WORKLOAD, seed=0)
+    sample = 64
+    for _ in range(args.warmup):
+        oracle_tokens_per_s(inp, sample, 0.0)
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_tokens_per_s(inp, sample, 0.0, seed=i + 1)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = sample / (ms / 1e3)
+    cores = _blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": _config(inp, note="each step: the float64 CPU oracle on %d sampled tokens"
+                          % sample),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": "%d random tokens of the T=4096 layer per step" % sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def _config(inp, note=None):
+    c = {"workload": "mid MoE layer prefill: T=%d tokens, H=%d, E=%d experts, I=%d, top-%d, "
+                     "int4 experts, e4m3 activations" % (inp.T, inp.H, inp.E, inp.I, inp.k),
+         "T": inp.T, "H": inp.H, "E": inp.E, "I": inp.I, "k": inp.k,
+         "global_batch": inp.T, "seq_len": inp.T, "parallelism": "replicas",
+         "l2": "flushed (256 MB write) before every timed step; weights 151 MB > L2"}
+    if note:
+        c["note"] = note
+    return c
+
+
+# ------------------------------------------------------------------------------ GPU arm
+def run_gpu(args):
+    import torch
+    import fp8_grouped_expert_gb300 as fge
+    from fp8_grouped_expert_gb300 import build as fge_build
+    from workloads import moe_inputs
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0 or not os.path.exists(fge.LIB_PATH):
+        fge_build.build()
+    if world > 1:
+        dist.barrier()
+    fge.lib()
+
+    inp = moe_inputs(WORKLOAD, seed=rank)
+    x_host = torch.from_numpy(inp.x_bits.view(np.int16)).view(torch.bfloat16)
+    lg_host = torch.from_numpy(inp.logits)
+    x = x_host.to(dev)
+    logits = lg_host.to(dev)
+    fmt = fge.W4_SUBNORMAL
+    w_gu, s_gu = fge.w4_prepack(torch.from_numpy(inp.w_gu).to(dev),
+                                torch.from_numpy(inp.s_gu).to(dev), True, fmt)
+    w_dn, s_dn = fge.w4_prepack(torch.from_numpy(inp.w_dn).to(dev),
+                                torch.from_numpy(inp.s_dn).to(dev), False, fmt)
+    ws = fge.new_workspace(fge.workspace_bytes(fge.OP_MOE_LAYER, inp.T, inp.H, inp.I, inp.E,
+                                               inp.k), dev)
+    out = torch.empty((inp.T, inp.H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fge.moe_layer_forward(logits, x, inp.k, inp.I, w_gu, s_gu, w_dn, s_dn, fmt=fmt,
+                              workspace=ws, out=out)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    fge.clear_device_status(ws)
+
+    # ---- timed region: K steps, L2 flushed before each, device time by CUDA events
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(step_ms) / len(step_ms)
+    status = fge.read_device_status(ws)
+    if status != 0:
+        raise RuntimeError("device status %d after the timed steps" % status)
+    launches_per_step = 9   # topk, quant, permute x4, gate_up, down, combine
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * inp.T / (ms / 1e3)
+
+    # ---- per-stage breakdown and the dominant kernel (gate_up grouped GEMM) timed alone
+    stages = stage_times(fge, torch, inp, x, logits, w_gu, s_gu, w_dn, s_dn, fmt, flush, dev,
+                         args.steps)
+
+    # ---- end to end through the public API with host buffers
+    x_pin = x_host.pin_memory()
+    lg_pin = lg_host.pin_memory()
+    out_pin = torch.empty((inp.T, inp.H), dtype=torch.bfloat16).pin_memory()
+    for _ in range(2):
+        fge.moe_layer_forward(lg_pin.to(dev, non_blocking=True), x_pin.to(dev, non_blocking=True),
+                              inp.k, inp.I, w_gu, s_gu, w_dn, s_dn, fmt=fmt, workspace=ws,
+                              out=out)
+        out_pin.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        xd = x_pin.to(dev, non_blocking=True)
+        ld = lg_pin.to(dev, non_blocking=True)
+        fge.moe_layer_forward(ld, xd, inp.k, inp.I, w_gu, s_gu, w_dn, s_dn, fmt=fmt,
+                              workspace=ws, out=out)
+        out_pin.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    h2d = x_pin.numel() * 2 + lg_pin.numel() * 4
+    d2h = out_pin.numel() * 2
+
+    hbm, bf16, peak_kind = _peaks()
+    fp8_peak = 2.0 * bf16  # fp8 dense = 2x bf16 dense (nominal ratio 4.5 / 2.25 PFLOP/s)
+    r = inp.T * inp.k
+    gu_flops = 2.0 * r * (2 * inp.I) * inp.H
+    gu_ms = stages["gate_up_gemm"]
+    achieved = gu_flops / (gu_ms / 1e3) / 1e12
+    layer_flops = gu_flops + 2.0 * r * inp.H * inp.I
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rate, done, el = oracle_tokens_per_s(inp, 64, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+               "sample": "%d tokens (random 64-token samples of the T=4096 layer) in %.1f s"
+                         % (done, el)}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3 x int4 -> f32 accumulate", "data": "synthetic",
+        "config": _config(inp),
+        "layer_tflops": layer_flops / (ms / 1e3) / 1e12,
+        "stages_ms": stages,
+        "roofline": {"bound": "tensor", "kernel": "grouped_gemm gate_up (fused SwiGLU requant)",
+                     "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                     "frac": achieved / fp8_peak, "traffic": None,
+                     "peak_source": "%s bf16 burst %.1f TF x 2 (fp8/bf16 nominal ratio)"
+                                    % (peak_kind, bf16),
+                     "algorithmic_flops_per_launch": gu_flops},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * inp.T / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def stage_times(fge, torch, inp, x, logits, w_gu, s_gu, w_dn, s_dn, fmt, flush, dev, steps):
+    """Each stage of the layer through its own C-ABI call, timed with CUDA events on the
+    launching stream, L2 flushed before each stage."""
+    stream = torch.cuda.current_stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    acc = {}
+
+    def timed(name, fn):
+        flush.fill_(7)
+        a, b = ev(), ev()
+        a.record(stream)
+        res = fn()
+        b.record(stream)
+        acc.setdefault(name, []).append((a, b))
+        return res
+
+    out = None
+    for _ in range(steps + 1):
+        ids, gates = timed("topk_gate", lambda: fge.moe_topk_gate(logits, inp.k))
+        xq, xs = timed("quant_g128", lambda: fge.fp8_quant_act(x, "g128"))
+        p = timed("permute", lambda: fge.moe_permute(ids, inp.E, xq, xs))
+        hq, hs = timed("gate_up_gemm", lambda: fge.grouped_gemm_w4a8(
+            p["aq"], p["as_"], p["offsets"], w_gu, s_gu, fmt=fmt, epilogue="swiglu"))
+        y = timed("down_gemm", lambda: fge.grouped_gemm_w4a8(
+            hq, hs, p["offsets"], w_dn, s_dn, fmt=fmt, out_dtype=torch.bfloat16))
+        out = timed("combine", lambda: fge.moe_combine(y, p["token_row"], gates))
+    torch.cuda.synchronize()
+    # the first pass includes allocator warm-up; drop it
+    return {k: sum(a.elapsed_time(b) for a, b in v[1:]) / (len(v) - 1) for k, v in acc.items()}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

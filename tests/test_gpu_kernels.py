@@ -96,7 +96,9 @@ def test_combine(fge, y_dtype, out_dtype):
     if out_dtype == torch.float32:
         np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-6)
     else:
-        assert np.all(np.abs(got - ref) <= bf16_ulp(ref) + 1e-6 * np.abs(ref))
+        # one bf16 ulp of the result plus the fp32 accumulation error of the k terms
+        absref = oracle.moe_combine(np.abs(y), p["token_row"], gates)
+        assert np.all(np.abs(got - ref) <= bf16_ulp(ref) + 1e-6 * absref)
 
 
 def test_swiglu_quant_unfused(fge):
