@@ -28,6 +28,22 @@ WORKLOAD = "mid"
 METRIC = "MoE prefill tokens/s; grouped-GEMM TFLOPS as % of GB300 FP8 peak, 1 GPU"
 L2_FLUSH_BYTES = 256 << 20
 
+# DRAM bytes (read + write) of one gate_up grouped-GEMM launch on this workload, from an
+# ncu capture, keyed by the sha256 prefixes of the kernel sources it was taken on.  A
+# kernel changed since the capture reports traffic = null.
+KNOWN_GATE_UP_TRAFFIC = {
+    "bbab9dbfa1323528:422dc7d17945d077": 194.44e6,
+}
+
+
+def _kernel_key():
+    import hashlib
+    parts = []
+    for f in ("gemm.cu", "fge_device.cuh"):
+        with open(os.path.join(ROOT, "fp8_grouped_expert_gb300", "csrc", f), "rb") as fh:
+            parts.append(hashlib.sha256(fh.read()).hexdigest()[:16])
+    return ":".join(parts)
+
 
 def _dist():
     rank = int(os.environ.get("RANK", "0"))
@@ -291,7 +307,8 @@ def run_gpu(args):
         "stages_ms": stages,
         "roofline": {"bound": "tensor", "kernel": "grouped_gemm gate_up (fused SwiGLU requant)",
                      "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                     "frac": achieved / fp8_peak, "traffic": None,
+                     "frac": achieved / fp8_peak,
+                     "traffic": KNOWN_GATE_UP_TRAFFIC.get(_kernel_key()),
                      "peak_source": "%s bf16 burst %.1f TF x 2 (fp8/bf16 nominal ratio)"
                                     % (peak_kind, bf16),
                      "algorithmic_flops_per_launch": gu_flops},
