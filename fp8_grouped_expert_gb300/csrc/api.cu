@@ -107,6 +107,7 @@ const char* fge_status_string(fge_status s) {
     case FGE_ERR_CUDA: return "CUDA error";
     case FGE_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
     case FGE_ERR_NOT_INITIALIZED: return "fge_init not called for this device";
+    case FGE_ERR_EXCEEDS_STATIC_SCRATCH: return "size exceeds the fixed scratch of the no-alloc call";
   }
   return "unknown status";
 }

@@ -46,7 +46,8 @@ typedef enum {
   FGE_ERR_UNSUPPORTED_DEVICE = 5, /* not sm_103 / kernel resources unavailable */
   FGE_ERR_CUDA = 6,               /* a CUDA runtime call or launch failed */
   FGE_ERR_DEVICE_TIMEOUT = 7,     /* device status only: a pipeline wait ran out */
-  FGE_ERR_NOT_INITIALIZED = 8     /* fge_init() was not called for the current device */
+  FGE_ERR_NOT_INITIALIZED = 8,    /* fge_init() was not called for the current device */
+  FGE_ERR_EXCEEDS_STATIC_SCRATCH = 9 /* fge_linear_w8a8_noalloc: M*K beyond its fixed scratch */
 } fge_status;
 
 typedef enum {
@@ -189,6 +190,26 @@ fge_status fge_gemm_w8a8(const uint8_t* aq, const float* sa, int64_t M, int64_t 
 fge_status fge_linear_w8a8(const void* x_bf16, int64_t M, int64_t K, const uint8_t* wq,
                            const float* w_scale, int64_t N, void* y_bf16, void* workspace,
                            size_t workspace_bytes, fge_stream_t stream);
+
+/* linear_w8a8_noalloc -- the same projection as fge_linear_w8a8 for callers that cannot
+ * allocate device memory: hosts that own all device memory through their own pool and forbid
+ * other allocations while serving, latency-critical paths where a cudaMalloc (which may
+ * synchronise the device) is not allowed, and foreign-language hosts that can pass device
+ * pointers for inputs and outputs but have no device allocator for a workspace.  The pages
+ * have no counterpart of this call; it is an addition of this library.
+ * Scratch: a fixed 16 MiB device array inside libfge (held by every GPU that loads the
+ * library until the process exits), so M*K must not exceed 16 MiB - 256 bytes (for example
+ * M <= 6553 at K = 2560); larger sizes return FGE_ERR_EXCEEDS_STATIC_SCRATCH.  The call
+ * allocates nothing and needs no fge_init().  Its first call on a device looks up the
+ * array's device address on that device (make that first call before any stream capture).
+ * All calls share the one array and it keeps the last call's contents (the call clears what
+ * must start at zero itself), so calls whose GPU work overlaps -- on different streams, or
+ * from several host threads -- race on it; issue them on one stream or serialise them.
+ * Arguments as fge_linear_w8a8: x_bf16 [M, K], wq [N, K] e4m3, w_scale device scalar,
+ * y_bf16 [M, N]. */
+fge_status fge_linear_w8a8_noalloc(const void* x_bf16, int64_t M, int64_t K, const uint8_t* wq,
+                                   const float* w_scale, int64_t N, void* y_bf16,
+                                   fge_stream_t stream);
 
 /* moe_layer_forward -- one MoE FFN prefill layer in one call: top-k gate -> G128 quant ->
  * permute -> gate_up grouped GEMM with fused SwiGLU + requant -> down grouped GEMM ->
