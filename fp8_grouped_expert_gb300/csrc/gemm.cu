@@ -55,15 +55,18 @@ struct Cfg {
   static constexpr int kTmemCols = 2 * BN;
   // register split (group mode only): WG0/WG1 shrink, epilogue warpgroups grow
   static constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8;
-  static constexpr int kRegsLow = 80;
+  static constexpr int kRegsLow = 64;
   static constexpr int kRegsHigh0 = (kLaunchRegs * kThreads - 256 * kRegsLow) / kEpiThreads / 8 * 8;
   static constexpr int kRegsHigh = kRegsHigh0 > 240 ? 240 : kRegsHigh0;
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kNS * kABytes;
   static constexpr int kOffBU = kOffB + kNS * kBLoadBytes;
-  static constexpr int kOffBar = kOffBU + kNU * kBUBytes;
-  static constexpr int kNumBars = 2 * kNS + 2 * kNU + 4 + 1;
+  static constexpr int kNSW = kGroupScale ? 4 : 0;  // weight-scale ring (one K group each)
+  static constexpr int kSWBytes = BN * 4;
+  static constexpr int kOffSW = kOffBU + kNU * kBUBytes;
+  static constexpr int kOffBar = kOffSW + kNSW * kSWBytes;
+  static constexpr int kNumBars = 2 * kNS + 2 * kNU + 4 + 1 + 2 * kNSW;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffOffs = align16(kOffMisc + 16);
   static constexpr int kOffMtp = kOffOffs + (kMaxExperts + 1) * 4;
@@ -77,6 +80,41 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
+}
+
+// 1-D bulk copy global -> shared, completion counted on an mbarrier (16-byte multiples).
+__device__ __forceinline__ void bulk_load(uint32_t smem_dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  return static_cast<uint64_t>(__float_as_uint(lo)) |
+         (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
+}
+
+// (acc0, acc1) += (sa * w0, sa * w1) * (p0, p1) with packed f32x2 multiply and FMA.
+__device__ __forceinline__ void fma2_scaled(float& acc0, float& acc1, uint64_t sa2, float w0,
+                                            float w1, uint32_t p0, uint32_t p1) {
+  uint64_t s2, acc = pack_f32x2(acc0, acc1);
+  const uint64_t w2 = pack_f32x2(w0, w1);
+  const uint64_t pv = static_cast<uint64_t>(p0) | (static_cast<uint64_t>(p1) << 32);
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(s2) : "l"(sa2), "l"(w2));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(s2), "l"(pv));
+  acc0 = __uint_as_float(static_cast<uint32_t>(acc));
+  acc1 = __uint_as_float(static_cast<uint32_t>(acc >> 32));
+}
+
+// Values loaded from TMEM may only be used after tcgen05.wait::ld; this empty volatile asm,
+// ordered after the wait, makes every later use depend on it.
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
 }
 
 // 8 int4 values (two's complement, nibble i = element i) -> e4m3 codes of the integers.
@@ -156,6 +194,8 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
   const uint32_t bar_tfull = bar_uempty + 8 * C::kNU;
   const uint32_t bar_tempty = bar_tfull + 16;
   const uint32_t bar_drain = bar_tempty + 16;
+  const uint32_t bar_swfull = bar_drain + 8;
+  const uint32_t bar_swempty = bar_swfull + 8 * C::kNSW;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   int* s_off = reinterpret_cast<int*>(smem + C::kOffOffs);
@@ -179,6 +219,10 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
       mbar_init(bar_tempty + 8 * i, C::kEpiWarps);
     }
     mbar_init(bar_drain, 1);
+    for (int i = 0; i < C::kNSW; ++i) {
+      mbar_init(bar_swfull + 8 * i, 1);
+      mbar_init(bar_swempty + 8 * i, C::kEpiWarps);
+    }
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -274,6 +318,18 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
             ok = false;
             break;
           }
+          if constexpr (C::kGroupScale) {
+            // the tile's weight scales of this K group: BN contiguous floats
+            const uint32_t w = it % C::kNSW;
+            if (!mbar_wait(bar_swempty + 8 * w, ((it / C::kNSW) & 1) ^ 1, s_abort, p.status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar_swfull + 8 * w, C::kSWBytes);
+            bulk_load(smem_u32(smem + C::kOffSW + w * C::kSWBytes),
+                      p.sw + (static_cast<size_t>(ti.e) * G + g) * p.N + ti.n0, C::kSWBytes,
+                      bar_swfull + 8 * w);
+          }
           mbar_arrive_expect_tx(bar_full + 8 * s, C::kStageBytes);
           tma_load_2d(smem_u32(smem + C::kOffA + s * C::kABytes), &tmA, bar_full + 8 * s,
                       g * 128, ti.row0);
@@ -291,6 +347,11 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
       const uint32_t first = issued > static_cast<uint32_t>(C::kNS) ? issued - C::kNS : 0;
       for (uint32_t i = first; i < issued; ++i)
         mbar_wait_drain(bar_full + 8 * (i % C::kNS), (i / C::kNS) & 1);
+      if constexpr (C::kGroupScale) {
+        const uint32_t first_w = issued > static_cast<uint32_t>(C::kNSW) ? issued - C::kNSW : 0;
+        for (uint32_t i = first_w; i < issued; ++i)
+          mbar_wait_drain(bar_swfull + 8 * (i % C::kNSW), (i / C::kNSW) & 1);
+      }
     } else if (warp == 5 && lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc = make_idesc_e4m3(128, BN);
@@ -374,37 +435,57 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
         float acc[128];
 #pragma unroll
         for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+        // activation scales run two groups ahead of their use (global-load latency)
+        const float* as_row = p.as + static_cast<size_t>(valid ? row : 0) * G;
+        float sa0 = valid ? __ldg(as_row) : 0.0f;
+        float sa1 = (valid && G > 1) ? __ldg(as_row + 1) : 0.0f;
         for (int g = 0; g < G; ++g) {
           const uint32_t a = ait & 1;
-          const float sa = valid ? __ldg(p.as + static_cast<size_t>(row) * G + g) : 0.0f;
-          const float* swp = p.sw + (static_cast<size_t>(ti.e) * G + g) * p.N + ti.n0;
-          if (!mbar_wait(bar_tfull + 8 * a, (ait >> 1) & 1, s_abort, p.status)) {
+          const uint32_t w = ait % C::kNSW;
+          const float sa2 = (valid && g + 2 < G) ? __ldg(as_row + g + 2) : 0.0f;
+          if (!mbar_wait(bar_swfull + 8 * w, (ait / C::kNSW) & 1, s_abort, p.status) ||
+              !mbar_wait(bar_tfull + 8 * a, (ait >> 1) & 1, s_abort, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          const float* sws = reinterpret_cast<const float*>(smem + C::kOffSW + w * C::kSWBytes);
           const uint32_t tb = tmem_base + lane_addr + a * BN;
+          const uint64_t sa2x = pack_f32x2(sa0, sa0);
+          uint32_t v[2][16];
+          tmem_ld_32x32b_x16(tb + col_a, v[0]);
+          tmem_wait_ld();
+          reg_fence16(v[0]);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
+            if (c + 1 < 8) {
+              const int coln = (c + 1 < 4) ? col_a + (c + 1) * 16 : col_b + (c - 3) * 16;
+              tmem_ld_32x32b_x16(tb + coln, v[(c + 1) & 1]);
+            }
             const int col = (c < 4) ? col_a + c * 16 : col_b + (c - 4) * 16;
-            uint32_t v[16];
-            tmem_ld_32x32b_x16(tb + col, v);
-            tmem_wait_ld();
-            const float4* sw4 = reinterpret_cast<const float4*>(swp + col);
+            const float4* sw4 = reinterpret_cast<const float4*>(sws + col);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float4 w = __ldg(sw4 + i);
+              const float4 wv = sw4[i];
               float* ac = acc + c * 16 + 4 * i;
-              ac[0] = fmaf(sa * w.x, __uint_as_float(v[4 * i + 0]), ac[0]);
-              ac[1] = fmaf(sa * w.y, __uint_as_float(v[4 * i + 1]), ac[1]);
-              ac[2] = fmaf(sa * w.z, __uint_as_float(v[4 * i + 2]), ac[2]);
-              ac[3] = fmaf(sa * w.w, __uint_as_float(v[4 * i + 3]), ac[3]);
+              const uint32_t* vv = v[c & 1] + 4 * i;
+              fma2_scaled(ac[0], ac[1], sa2x, wv.x, wv.y, vv[0], vv[1]);
+              fma2_scaled(ac[2], ac[3], sa2x, wv.z, wv.w, vv[2], vv[3]);
+            }
+            if (c + 1 < 8) {
+              tmem_wait_ld();
+              reg_fence16(v[(c + 1) & 1]);
             }
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_tempty + 8 * a);
+          if (lane == 0) {
+            mbar_arrive(bar_tempty + 8 * a);
+            mbar_arrive(bar_swempty + 8 * w);
+          }
           ++ait;
+          sa0 = sa1;
+          sa1 = sa2;
         }
         if (!ok) break;
         if constexpr (EPI == kEpiSwiglu) {
@@ -469,30 +550,40 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
         if (!mbar_wait(bar_tfull + 8 * a, (ait >> 1) & 1, s_abort, p.status)) break;
         tc_fence_after();
         const uint32_t tb = tmem_base + lane_addr + a * BN;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          const int col = (c < 2) ? col_a + c * 32 : col_b + (c - 2) * 32;
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tb + col, v);
-          tmem_wait_ld();
+        uint32_t v[2][16];
+        tmem_ld_32x32b_x16(tb + col_a, v[0]);
+        tmem_wait_ld();
+        reg_fence16(v[0]);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          if (c + 1 < 8) {
+            const int coln = (c + 1 < 4) ? col_a + (c + 1) * 16 : col_b + (c - 3) * 16;
+            tmem_ld_32x32b_x16(tb + coln, v[(c + 1) & 1]);
+          }
+          const int col = (c < 4) ? col_a + c * 16 : col_b + (c - 4) * 16;
+          const uint32_t* vv = v[c & 1];
           if (valid) {
             if constexpr (EPI == kEpiF32) {
               float* o = reinterpret_cast<float*>(p.out) + static_cast<size_t>(row) * p.N + ti.n0 + col;
 #pragma unroll
-              for (int i = 0; i < 32; i += 4)
+              for (int i = 0; i < 16; i += 4)
                 *reinterpret_cast<float4*>(o + i) = make_float4(
-                    tensor_scale * __uint_as_float(v[i]), tensor_scale * __uint_as_float(v[i + 1]),
-                    tensor_scale * __uint_as_float(v[i + 2]), tensor_scale * __uint_as_float(v[i + 3]));
+                    tensor_scale * __uint_as_float(vv[i]), tensor_scale * __uint_as_float(vv[i + 1]),
+                    tensor_scale * __uint_as_float(vv[i + 2]), tensor_scale * __uint_as_float(vv[i + 3]));
             } else {
               __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * p.N + ti.n0 + col;
 #pragma unroll
-              for (int i = 0; i < 32; i += 8)
+              for (int i = 0; i < 16; i += 8)
                 *reinterpret_cast<uint4*>(o + i) = make_uint4(
-                    pack_bf16x2(tensor_scale * __uint_as_float(v[i]), tensor_scale * __uint_as_float(v[i + 1])),
-                    pack_bf16x2(tensor_scale * __uint_as_float(v[i + 2]), tensor_scale * __uint_as_float(v[i + 3])),
-                    pack_bf16x2(tensor_scale * __uint_as_float(v[i + 4]), tensor_scale * __uint_as_float(v[i + 5])),
-                    pack_bf16x2(tensor_scale * __uint_as_float(v[i + 6]), tensor_scale * __uint_as_float(v[i + 7])));
+                    pack_bf16x2(tensor_scale * __uint_as_float(vv[i]), tensor_scale * __uint_as_float(vv[i + 1])),
+                    pack_bf16x2(tensor_scale * __uint_as_float(vv[i + 2]), tensor_scale * __uint_as_float(vv[i + 3])),
+                    pack_bf16x2(tensor_scale * __uint_as_float(vv[i + 4]), tensor_scale * __uint_as_float(vv[i + 5])),
+                    pack_bf16x2(tensor_scale * __uint_as_float(vv[i + 6]), tensor_scale * __uint_as_float(vv[i + 7])));
             }
+          }
+          if (c + 1 < 8) {
+            tmem_wait_ld();
+            reg_fence16(v[(c + 1) & 1]);
           }
         }
         tc_fence_before();
