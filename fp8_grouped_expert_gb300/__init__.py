@@ -343,3 +343,70 @@ def residual_add(h, y):
                                   DTYPE_F32 if y.dtype == torch.float32 else DTYPE_BF16,
                                   h.numel(), _stream(h)), "fge_residual_add")
     return h
+
+
+# --------------------------------------------------------------------- stacked prefill
+class StackedPrefill:
+    """L pre-norm blocks of the stacked prefill workload, every step a C-ABI call:
+    RMSNorm -> per-tensor W8A8 q/k/v -> identity attention on v -> W8A8 o -> fp32 residual
+    -> RMSNorm -> fp32 router -> MoE layer (top-k, quant, permute, grouped GEMMs, combine)
+    -> fp32 residual.
+
+    layers: list of dicts with bf16 projection weights (wq_bits, wk_bits, wv_bits, wo_bits as
+    uint16 numpy [rows, H]), fp32 w_router [E, H] and canonical int4 banks w_gu/s_gu,
+    w_dn/s_dn.  Projection weights are quantized per tensor to e4m3 at load by the
+    library's own quantizer; int4 banks are prepacked at load.
+    """
+
+    def __init__(self, layers, T, H, E, I, k, n_heads, n_kv_heads, device, fmt=W4_SUBNORMAL):
+        import numpy as np
+        self.T, self.H, self.E, self.I, self.k = T, H, E, I, k
+        self.n_heads, self.n_kv = n_heads, n_kv_heads
+        self.fmt = fmt
+        self.dev = torch.device(device)
+        _ensure_init(self.dev)
+        self.layers = []
+        for lw in layers:
+            d = {}
+            for name in ("q", "k", "v", "o"):
+                wb = torch.from_numpy(np.ascontiguousarray(lw["w" + name + "_bits"]).view(np.int16))
+                wq, ws = fp8_quant_act(wb.view(torch.bfloat16).to(self.dev), "tensor")
+                d["w" + name], d["s" + name] = wq, ws
+            d["w_router"] = torch.from_numpy(lw["w_router"]).to(self.dev)
+            d["w_gu"], d["s_gu"] = w4_prepack(torch.from_numpy(lw["w_gu"]).to(self.dev),
+                                              torch.from_numpy(lw["s_gu"]).to(self.dev), True, fmt)
+            d["w_dn"], d["s_dn"] = w4_prepack(torch.from_numpy(lw["w_dn"]).to(self.dev),
+                                              torch.from_numpy(lw["s_dn"]).to(self.dev), False, fmt)
+            self.layers.append(d)
+        dev = self.dev
+        kv = n_kv_heads * 128
+        self.ws_lin = new_workspace(workspace_bytes(OP_LINEAR_W8A8, T, H), dev)
+        self.ws_moe = new_workspace(workspace_bytes(OP_MOE_LAYER, T, H, I, E, k), dev)
+        self.xn = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.q = torch.empty((T, n_heads * 128), dtype=torch.bfloat16, device=dev)
+        self.kk = torch.empty((T, kv), dtype=torch.bfloat16, device=dev)
+        self.v = torch.empty((T, kv), dtype=torch.bfloat16, device=dev)
+        self.attn = torch.empty((T, n_heads * 128), dtype=torch.bfloat16, device=dev)
+        self.o = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+        self.y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+
+    def forward(self, h, layers=None):
+        """h: float32 [T, H] on the device, updated in place and returned.  ``layers``
+        selects which layer indices to run (all, in order, by default)."""
+        for li in (range(len(self.layers)) if layers is None else layers):
+            d = self.layers[li]
+            rmsnorm(h, out=self.xn)
+            linear_w8a8(self.xn, d["wq"], d["sq"], workspace=self.ws_lin, out=self.q)
+            linear_w8a8(self.xn, d["wk"], d["sk"], workspace=self.ws_lin, out=self.kk)
+            linear_w8a8(self.xn, d["wv"], d["sv"], workspace=self.ws_lin, out=self.v)
+            identity_attention(self.v, self.n_heads, self.n_kv, out=self.attn)
+            linear_w8a8(self.attn, d["wo"], d["so"], workspace=self.ws_lin, out=self.o)
+            residual_add(h, self.o)
+            rmsnorm(h, out=self.xn)
+            router_logits(self.xn, d["w_router"], out=self.logits)
+            moe_layer_forward(self.logits, self.xn, self.k, self.I, d["w_gu"], d["s_gu"],
+                              d["w_dn"], d["s_dn"], fmt=self.fmt, workspace=self.ws_moe,
+                              out=self.y)
+            residual_add(h, self.y)
+        return h

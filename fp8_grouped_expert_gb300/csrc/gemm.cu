@@ -96,16 +96,22 @@ __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
          (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
 }
 
-// (acc0, acc1) += (sa * w0, sa * w1) * (p0, p1) with packed f32x2 multiply and FMA.
-__device__ __forceinline__ void fma2_scaled(float& acc0, float& acc1, uint64_t sa2, float w0,
-                                            float w1, uint32_t p0, uint32_t p1) {
-  uint64_t s2, acc = pack_f32x2(acc0, acc1);
-  const uint64_t w2 = pack_f32x2(w0, w1);
-  const uint64_t pv = static_cast<uint64_t>(p0) | (static_cast<uint64_t>(p1) << 32);
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(s2) : "l"(sa2), "l"(w2));
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(s2), "l"(pv));
-  acc0 = __uint_as_float(static_cast<uint32_t>(acc));
-  acc1 = __uint_as_float(static_cast<uint32_t>(acc >> 32));
+// acc2 (two fp32 in a 64-bit register) += (sa2 * w2) * (p0, p1), packed f32x2 math.
+__device__ __forceinline__ void fma2_pair(uint64_t& acc2, uint64_t sa2, uint64_t w2, uint32_t p0,
+                                          uint32_t p1) {
+  asm("{\n\t.reg .b64 pp, ss;\n\t"
+      "mov.b64 pp, {%1, %2};\n\t"
+      "mul.rn.f32x2 ss, %3, %4;\n\t"
+      "fma.rn.f32x2 %0, ss, pp, %0;\n\t}"
+      : "+l"(acc2)
+      : "r"(p0), "r"(p1), "l"(sa2), "l"(w2));
+}
+
+__device__ __forceinline__ float lo_f32(uint64_t v) {
+  return __uint_as_float(static_cast<uint32_t>(v));
+}
+__device__ __forceinline__ float hi_f32(uint64_t v) {
+  return __uint_as_float(static_cast<uint32_t>(v >> 32));
 }
 
 // Values loaded from TMEM may only be used after tcgen05.wait::ld; this empty volatile asm,
@@ -276,12 +282,14 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
             ok = false;
             break;
           }
-          const uint8_t* src = smem + C::kOffB + s * C::kBLoadBytes;
-          uint8_t* dst = smem + C::kOffBU + u * C::kBUBytes;
-#pragma unroll 4
-          for (int unit = tid; unit < BN * 8; unit += 128) {
-            const int row = unit >> 3, j = unit & 7;
-            const uint2 w = *reinterpret_cast<const uint2*>(src + row * 64 + j * 8);
+          // unit i of this thread: row (tid/8) + 16 i, 16-byte chunk j = tid%8.  Row & 7 and
+          // j do not depend on i, so source and swizzled destination advance by constants.
+          const uint8_t* src = smem + C::kOffB + s * C::kBLoadBytes + (tid >> 3) * 64 + (tid & 7) * 8;
+          uint8_t* dst = smem + C::kOffBU + u * C::kBUBytes + (tid >> 3) * 128 +
+                         (((tid & 7) ^ ((tid >> 3) & 7)) << 4);
+#pragma unroll
+          for (int i = 0; i < BN / 16; ++i) {
+            const uint2 w = *reinterpret_cast<const uint2*>(src + i * 1024);
             uint2 a, b;
             if constexpr (BFMT == kBfmtInt4Sub) {
               a = w4_to_e4m3_sub(w.x);
@@ -290,8 +298,7 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
               a = w4_to_e4m3_lut(w.x);
               b = w4_to_e4m3_lut(w.y);
             }
-            *reinterpret_cast<uint4*>(dst + row * 128 + ((j ^ (row & 7)) << 4)) =
-                make_uint4(a.x, a.y, b.x, b.y);
+            *reinterpret_cast<uint4*>(dst + i * 2048) = make_uint4(a.x, a.y, b.x, b.y);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -432,9 +439,9 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
       const bool valid = r_in < ti.rows;
       const int row = ti.row0 + r_in;
       if constexpr (C::kGroupScale) {
-        float acc[128];
+        uint64_t acc2[64];  // acc2[j] holds columns 2j, 2j+1 of the thread's 128
 #pragma unroll
-        for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 64; ++i) acc2[i] = 0;
         // activation scales run two groups ahead of their use (global-load latency)
         const float* as_row = p.as + static_cast<size_t>(valid ? row : 0) * G;
         float sa0 = valid ? __ldg(as_row) : 0.0f;
@@ -463,14 +470,13 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
               tmem_ld_32x32b_x16(tb + coln, v[(c + 1) & 1]);
             }
             const int col = (c < 4) ? col_a + c * 16 : col_b + (c - 4) * 16;
-            const float4* sw4 = reinterpret_cast<const float4*>(sws + col);
+            const ulonglong2* sw2 = reinterpret_cast<const ulonglong2*>(sws + col);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float4 wv = sw4[i];
-              float* ac = acc + c * 16 + 4 * i;
+              const ulonglong2 wv = sw2[i];  // 4 weight scales as two f32x2 pairs
               const uint32_t* vv = v[c & 1] + 4 * i;
-              fma2_scaled(ac[0], ac[1], sa2x, wv.x, wv.y, vv[0], vv[1]);
-              fma2_scaled(ac[2], ac[3], sa2x, wv.z, wv.w, vv[2], vv[3]);
+              fma2_pair(acc2[c * 8 + 2 * i], sa2x, wv.x, vv[0], vv[1]);
+              fma2_pair(acc2[c * 8 + 2 * i + 1], sa2x, wv.y, vv[2], vv[3]);
             }
             if (c + 1 < 8) {
               tmem_wait_ld();
@@ -490,12 +496,14 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
         if (!ok) break;
         if constexpr (EPI == kEpiSwiglu) {
           // columns [col_a, col_a+64) are gate rows i, [col_b, col_b+64) the matching up rows
+          float hv[64];
           float amax = 0.0f;
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
-            const float gt = acc[i];
-            const float h = __fdiv_rn(gt, 1.0f + expf(-gt)) * acc[64 + i];
-            acc[i] = h;
+            const float gt = (i & 1) ? hi_f32(acc2[i >> 1]) : lo_f32(acc2[i >> 1]);
+            const float up = (i & 1) ? hi_f32(acc2[32 + (i >> 1)]) : lo_f32(acc2[32 + (i >> 1)]);
+            const float h = __fdiv_rn(gt, 1.0f + expf(-gt)) * up;
+            hv[i] = h;
             amax = fmaxf(amax, fabsf(h));
           }
           float* red = s_red + tile_parity * 256;
@@ -510,14 +518,14 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 64; i += 16) {
               uint4 o;
-              o.x = cvt_e4m3x4(__fdiv_rn(acc[i + 0], s), __fdiv_rn(acc[i + 1], s),
-                               __fdiv_rn(acc[i + 2], s), __fdiv_rn(acc[i + 3], s));
-              o.y = cvt_e4m3x4(__fdiv_rn(acc[i + 4], s), __fdiv_rn(acc[i + 5], s),
-                               __fdiv_rn(acc[i + 6], s), __fdiv_rn(acc[i + 7], s));
-              o.z = cvt_e4m3x4(__fdiv_rn(acc[i + 8], s), __fdiv_rn(acc[i + 9], s),
-                               __fdiv_rn(acc[i + 10], s), __fdiv_rn(acc[i + 11], s));
-              o.w = cvt_e4m3x4(__fdiv_rn(acc[i + 12], s), __fdiv_rn(acc[i + 13], s),
-                               __fdiv_rn(acc[i + 14], s), __fdiv_rn(acc[i + 15], s));
+              o.x = cvt_e4m3x4(__fdiv_rn(hv[i + 0], s), __fdiv_rn(hv[i + 1], s),
+                               __fdiv_rn(hv[i + 2], s), __fdiv_rn(hv[i + 3], s));
+              o.y = cvt_e4m3x4(__fdiv_rn(hv[i + 4], s), __fdiv_rn(hv[i + 5], s),
+                               __fdiv_rn(hv[i + 6], s), __fdiv_rn(hv[i + 7], s));
+              o.z = cvt_e4m3x4(__fdiv_rn(hv[i + 8], s), __fdiv_rn(hv[i + 9], s),
+                               __fdiv_rn(hv[i + 10], s), __fdiv_rn(hv[i + 11], s));
+              o.w = cvt_e4m3x4(__fdiv_rn(hv[i + 12], s), __fdiv_rn(hv[i + 13], s),
+                               __fdiv_rn(hv[i + 14], s), __fdiv_rn(hv[i + 15], s));
               *reinterpret_cast<uint4*>(hq + i) = o;
             }
             if (wg == 0) p.out_scales[static_cast<size_t>(row) * (inter / 128) + ti.n0 / 256] = s;
@@ -531,16 +539,17 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
 #pragma unroll
               for (int i = 0; i < 32; i += 4)
                 *reinterpret_cast<float4*>(o + i) =
-                    make_float4(acc[c * 32 + i], acc[c * 32 + i + 1], acc[c * 32 + i + 2], acc[c * 32 + i + 3]);
+                    make_float4(lo_f32(acc2[(c * 32 + i) / 2]), hi_f32(acc2[(c * 32 + i) / 2]),
+                                lo_f32(acc2[(c * 32 + i) / 2 + 1]), hi_f32(acc2[(c * 32 + i) / 2 + 1]));
             } else {
               __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * p.N + ti.n0 + col;
 #pragma unroll
               for (int i = 0; i < 32; i += 8)
                 *reinterpret_cast<uint4*>(o + i) = make_uint4(
-                    pack_bf16x2(acc[c * 32 + i], acc[c * 32 + i + 1]),
-                    pack_bf16x2(acc[c * 32 + i + 2], acc[c * 32 + i + 3]),
-                    pack_bf16x2(acc[c * 32 + i + 4], acc[c * 32 + i + 5]),
-                    pack_bf16x2(acc[c * 32 + i + 6], acc[c * 32 + i + 7]));
+                    pack_bf16x2(lo_f32(acc2[(c * 32 + i) / 2]), hi_f32(acc2[(c * 32 + i) / 2])),
+                    pack_bf16x2(lo_f32(acc2[(c * 32 + i) / 2 + 1]), hi_f32(acc2[(c * 32 + i) / 2 + 1])),
+                    pack_bf16x2(lo_f32(acc2[(c * 32 + i) / 2 + 2]), hi_f32(acc2[(c * 32 + i) / 2 + 2])),
+                    pack_bf16x2(lo_f32(acc2[(c * 32 + i) / 2 + 3]), hi_f32(acc2[(c * 32 + i) / 2 + 3])));
             }
           }
         }

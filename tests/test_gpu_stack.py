@@ -1,0 +1,116 @@
+"""GPU parity of the stacked-prefill glue (RMSNorm, fp32 router, identity attention,
+residual add) and of the stacked prefill itself against the oracle.
+
+The stack is compared layer by layer: each GPU layer and the oracle layer run on the same
+input (the GPU's hidden state) and their outputs and updates must have cosine >= 0.9999.
+Free-running trajectories are compared too (cosine >= 0.9999 at depth 4, reported at 8 and
+12): dynamic per-tensor and per-group e4m3 quantization makes a layer discontinuous in its
+input (one ulp on a tensor's amax element moves every code of the tensor), so fp32 and
+float64 accumulations that agree per layer drift apart with depth."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from util import bf16_dev, bf16_ulp, cosine, host, to_dev
+from workloads import stacked_inputs, to_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def test_rmsnorm(fge):
+    rng = np.random.default_rng(61)
+    h = (rng.standard_normal((300, 2048)) * np.exp(rng.uniform(-3, 3, (300, 1)))).astype(np.float32)
+    got = host(fge.rmsnorm(to_dev(h))).astype(np.float64)
+    ref = oracle.rmsnorm(h).astype(np.float64)
+    # fp32 on the GPU vs float64 rounded to bf16: at most one bf16 step apart
+    assert np.all(np.abs(got - ref) <= bf16_ulp(ref) * 1.0001)
+
+
+def test_router_logits(fge):
+    rng = np.random.default_rng(62)
+    bits, xn = to_bf16(rng.standard_normal((257, 2048)).astype(np.float32))
+    w = (rng.standard_normal((64, 2048)) * 0.02).astype(np.float32)
+    got = host(fge.router_logits(bf16_dev(bits), to_dev(w))).astype(np.float64)
+    ref = xn.astype(np.float64) @ w.astype(np.float64).T
+    absref = np.abs(xn.astype(np.float64)) @ np.abs(w.astype(np.float64)).T
+    assert np.all(np.abs(got - ref) <= 1e-5 * absref + 1e-7)
+
+
+def test_identity_attention_exact(fge):
+    rng = np.random.default_rng(63)
+    bits, v = to_bf16(rng.standard_normal((100, 512)).astype(np.float32))
+    got = host(fge.identity_attention(bf16_dev(bits), 16, 4))
+    assert np.array_equal(got, oracle.identity_attention(v, 16, 4))
+
+
+def test_residual_add_exact(fge):
+    rng = np.random.default_rng(64)
+    h = rng.standard_normal((64, 512)).astype(np.float32)
+    bits, y = to_bf16(rng.standard_normal((64, 512)).astype(np.float32))
+    ht = to_dev(h)
+    fge.residual_add(ht, bf16_dev(bits))
+    assert np.array_equal(host(ht), h + y)
+
+
+def _oracle_layer(h, lw, sh, rows):
+    """Oracle layer on input h [T, H] for the given token rows.  The per-tensor scales need
+    whole tensors: xn and v are computed for every row, o and the MoE only for `rows`."""
+    wv, sv = oracle.quant_act_per_tensor(lw["wv_f32"])
+    wo, so = oracle.quant_act_per_tensor(lw["wo_f32"])
+    xn = oracle.rmsnorm(h)
+    xq, sa = oracle.quant_act_per_tensor(xn)
+    v = oracle.bf16_bits_to_f32(oracle.bf16_round(oracle.linear_w8a8_gemm(xq, sa, wv, sv)))
+    attn = oracle.identity_attention(v, sh["n_heads"], sh["n_kv_heads"])
+    aq, sa2 = oracle.quant_act_per_tensor(attn)
+    o = oracle.bf16_bits_to_f32(oracle.bf16_round(oracle.linear_w8a8_gemm(aq[rows], sa2, wo, so)))
+    h1 = (h[rows].astype(np.float64) + o).astype(np.float32)
+    xn2 = oracle.rmsnorm(h1)
+    lg = oracle.router_logits(xn2, lw["w_router"])
+    y, d = oracle.moe_layer_forward(lg, xn2, sh["k"], lw["w_gu"], lw["s_gu"], lw["w_dn"],
+                                    lw["s_dn"], sh["I"], out_dtype="bf16")
+    return (h1.astype(np.float64) + y).astype(np.float32), d["ids"]
+
+
+def _model(fge, st):
+    sh = st["shape"]
+    return fge.StackedPrefill(st["layers"], sh["T"], sh["H"], sh["E"], sh["I"], sh["k"],
+                              sh["n_heads"], sh["n_kv_heads"], "cuda")
+
+
+def test_stacked_prefill_layer_by_layer_full_size(fge):
+    # T = 2048 tokens, 12 layers; each layer checked on 48 sampled tokens
+    st = stacked_inputs(12, seed=2)
+    sh = st["shape"]
+    model = _model(fge, st)
+    rng = np.random.default_rng(7)
+    h = st["h0"].copy()
+    for li, lw in enumerate(st["layers"]):
+        hg = host(model.forward(to_dev(h), layers=[li]))
+        rows = np.sort(rng.choice(sh["T"], size=48, replace=False))
+        ref, _ = _oracle_layer(h, lw, sh, rows)
+        assert np.all(np.isfinite(hg))
+        c_out = cosine(hg[rows], ref)
+        c_upd = cosine(hg[rows] - h[rows], ref - h[rows])
+        assert c_out >= 0.9999 and c_upd >= 0.9999, (li, c_out, c_upd)
+        h = hg
+
+
+def test_stacked_prefill_free_running_depths(fge):
+    T = 256
+    st = stacked_inputs(12, seed=1, T=T)
+    sh = st["shape"]
+    model = _model(fge, st)
+    hg = to_dev(st["h0"])
+    ho = st["h0"].copy()
+    rows = np.arange(T)
+    cos = {}
+    for li, lw in enumerate(st["layers"]):
+        model.forward(hg, layers=[li])
+        ho, _ = _oracle_layer(ho, lw, sh, rows)
+        if li + 1 in (4, 8, 12):
+            cos[li + 1] = cosine(host(hg), ho)
+    print("free-running final-state cosine by depth:", cos)
+    assert cos[4] >= 0.9999, cos
+    assert cos[8] >= 0.999 and cos[12] >= 0.995, cos
