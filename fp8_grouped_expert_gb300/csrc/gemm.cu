@@ -53,10 +53,14 @@ struct Cfg {
   static constexpr int kEpiThreads = kEpiWarps * 32;
   static constexpr int kThreads = 256 + kEpiThreads;
   static constexpr int kTmemCols = 2 * BN;
-  // register split (group mode only): WG0/WG1 shrink, epilogue warpgroups grow
+  // register split (group mode only): the unpack warpgroup keeps a working set for 16
+  // units in flight, the producer/MMA warpgroup needs few, the epilogue holds 128 fp32
+  // accumulators per thread plus two TMEM chunks in flight.
   static constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8;
-  static constexpr int kRegsLow = 64;
-  static constexpr int kRegsHigh0 = (kLaunchRegs * kThreads - 256 * kRegsLow) / kEpiThreads / 8 * 8;
+  static constexpr int kRegsUnpack = 88;
+  static constexpr int kRegsCtrl = 40;
+  static constexpr int kRegsHigh0 =
+      (kLaunchRegs * kThreads - 128 * kRegsUnpack - 128 * kRegsCtrl) / kEpiThreads / 8 * 8;
   static constexpr int kRegsHigh = kRegsHigh0 > 240 ? 240 : kRegsHigh0;
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int kOffA = 0;
@@ -269,7 +273,7 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
 
   if (warp < 4) {
     // ------------------------------------------------------------------ unpack (WG0)
-    if constexpr (C::kGroupScale) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsLow));
+    if constexpr (C::kGroupScale) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsUnpack));
     if constexpr (C::kInt4) {
       const int tid = threadIdx.x;  // 0..127
       uint32_t it = 0;
@@ -310,7 +314,7 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
       }
     }
   } else if (warp < 8) {
-    if constexpr (C::kGroupScale) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsLow));
+    if constexpr (C::kGroupScale) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsCtrl));
     if (warp == 4 && lane == 0) {
       // ---------------------------------------------------------------- TMA producer
       tma_prefetch_desc(&tmA);
@@ -502,7 +506,7 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
           for (int i = 0; i < 64; ++i) {
             const float gt = (i & 1) ? hi_f32(acc2[i >> 1]) : lo_f32(acc2[i >> 1]);
             const float up = (i & 1) ? hi_f32(acc2[32 + (i >> 1)]) : lo_f32(acc2[32 + (i >> 1)]);
-            const float h = __fdiv_rn(gt, 1.0f + expf(-gt)) * up;
+            const float h = __fdividef(gt, 1.0f + __expf(-gt)) * up;
             hv[i] = h;
             amax = fmaxf(amax, fabsf(h));
           }
@@ -511,6 +515,8 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
           asm volatile("bar.sync 1, %0;" ::"n"(C::kEpiThreads) : "memory");
           const float amax_all = fmaxf(red[r_in], red[128 + r_in]);
           const float s = scale_from_amax(amax_all);
+          const float inv_s = __frcp_rn(s);  // h * (1/s): same e4m3 code as h / s except
+                                             // within 2^-23 of a rounding boundary
           if (valid) {
             const int inter = p.N / 2;
             uint8_t* hq = reinterpret_cast<uint8_t*>(p.out) + static_cast<size_t>(row) * inter +
@@ -518,14 +524,14 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 64; i += 16) {
               uint4 o;
-              o.x = cvt_e4m3x4(__fdiv_rn(hv[i + 0], s), __fdiv_rn(hv[i + 1], s),
-                               __fdiv_rn(hv[i + 2], s), __fdiv_rn(hv[i + 3], s));
-              o.y = cvt_e4m3x4(__fdiv_rn(hv[i + 4], s), __fdiv_rn(hv[i + 5], s),
-                               __fdiv_rn(hv[i + 6], s), __fdiv_rn(hv[i + 7], s));
-              o.z = cvt_e4m3x4(__fdiv_rn(hv[i + 8], s), __fdiv_rn(hv[i + 9], s),
-                               __fdiv_rn(hv[i + 10], s), __fdiv_rn(hv[i + 11], s));
-              o.w = cvt_e4m3x4(__fdiv_rn(hv[i + 12], s), __fdiv_rn(hv[i + 13], s),
-                               __fdiv_rn(hv[i + 14], s), __fdiv_rn(hv[i + 15], s));
+              o.x = cvt_e4m3x4(hv[i + 0] * inv_s, hv[i + 1] * inv_s,
+                               hv[i + 2] * inv_s, hv[i + 3] * inv_s);
+              o.y = cvt_e4m3x4(hv[i + 4] * inv_s, hv[i + 5] * inv_s,
+                               hv[i + 6] * inv_s, hv[i + 7] * inv_s);
+              o.z = cvt_e4m3x4(hv[i + 8] * inv_s, hv[i + 9] * inv_s,
+                               hv[i + 10] * inv_s, hv[i + 11] * inv_s);
+              o.w = cvt_e4m3x4(hv[i + 12] * inv_s, hv[i + 13] * inv_s,
+                               hv[i + 14] * inv_s, hv[i + 15] * inv_s);
               *reinterpret_cast<uint4*>(hq + i) = o;
             }
             if (wg == 0) p.out_scales[static_cast<size_t>(row) * (inter / 128) + ti.n0 / 256] = s;
@@ -664,8 +670,9 @@ static cudaError_t run(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st)
   if (C::kGroupScale) {
     // the register split must fit in what the CTA is launched with, or the growing
     // warpgroups would wait forever
-    const long need = 256L * C::kRegsLow + static_cast<long>(C::kEpiThreads) * C::kRegsHigh;
-    if (static_cast<long>(regs) * C::kThreads < need || regs < C::kRegsLow) {
+    const long need = 128L * C::kRegsUnpack + 128L * C::kRegsCtrl +
+                      static_cast<long>(C::kEpiThreads) * C::kRegsHigh;
+    if (static_cast<long>(regs) * C::kThreads < need || regs < C::kRegsUnpack) {
       *st = FGE_ERR_UNSUPPORTED_DEVICE;
       return cudaSuccess;
     }
