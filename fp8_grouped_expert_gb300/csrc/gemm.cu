@@ -291,16 +291,20 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
           const uint8_t* src = smem + C::kOffB + s * C::kBLoadBytes + (tid >> 3) * 64 + (tid & 7) * 8;
           uint8_t* dst = smem + C::kOffBU + u * C::kBUBytes + (tid >> 3) * 128 +
                          (((tid & 7) ^ ((tid >> 3) & 7)) << 4);
+          // all loads first: source and destination are both shared memory, so a store
+          // in between would keep every later load waiting behind it
+          uint2 wv[BN / 16];
+#pragma unroll
+          for (int i = 0; i < BN / 16; ++i) wv[i] = *reinterpret_cast<const uint2*>(src + i * 1024);
 #pragma unroll
           for (int i = 0; i < BN / 16; ++i) {
-            const uint2 w = *reinterpret_cast<const uint2*>(src + i * 1024);
             uint2 a, b;
             if constexpr (BFMT == kBfmtInt4Sub) {
-              a = w4_to_e4m3_sub(w.x);
-              b = w4_to_e4m3_sub(w.y);
+              a = w4_to_e4m3_sub(wv[i].x);
+              b = w4_to_e4m3_sub(wv[i].y);
             } else {
-              a = w4_to_e4m3_lut(w.x);
-              b = w4_to_e4m3_lut(w.y);
+              a = w4_to_e4m3_lut(wv[i].x);
+              b = w4_to_e4m3_lut(wv[i].y);
             }
             *reinterpret_cast<uint4*>(dst + i * 2048) = make_uint4(a.x, a.y, b.x, b.y);
           }
