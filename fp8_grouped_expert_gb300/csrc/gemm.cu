@@ -53,6 +53,9 @@ struct Cfg {
   static constexpr int kEpiThreads = kEpiWarps * 32;
   static constexpr int kThreads = 256 + kEpiThreads;
   static constexpr int kTmemCols = 2 * BN;
+  // group mode: each epilogue warpgroup owns 128 columns ("half") of every TMEM buffer with
+  // its own full/empty barriers, so the halves pipeline independently of each other
+  static constexpr int kHalves = kGroupScale ? BN / 128 : 1;
   // register split (group mode only): the unpack warpgroup keeps a working set for 16
   // units in flight, the producer/MMA warpgroup needs few, the epilogue holds 128 fp32
   // accumulators per thread plus two TMEM chunks in flight.
@@ -70,7 +73,7 @@ struct Cfg {
   static constexpr int kSWBytes = BN * 4;
   static constexpr int kOffSW = kOffBU + kNU * kBUBytes;
   static constexpr int kOffBar = kOffSW + kNSW * kSWBytes;
-  static constexpr int kNumBars = 2 * kNS + 2 * kNU + 4 + 1 + 2 * kNSW;
+  static constexpr int kNumBars = 2 * kNS + 2 * kNU + 4 * kHalves + 1 + 2 * kNSW;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffOffs = align16(kOffMisc + 16);
   static constexpr int kOffMtp = kOffOffs + (kMaxExperts + 1) * 4;
@@ -202,8 +205,8 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
   const uint32_t bar_ufull = bar_empty + 8 * C::kNS;
   const uint32_t bar_uempty = bar_ufull + 8 * C::kNU;
   const uint32_t bar_tfull = bar_uempty + 8 * C::kNU;
-  const uint32_t bar_tempty = bar_tfull + 16;
-  const uint32_t bar_drain = bar_tempty + 16;
+  const uint32_t bar_tempty = bar_tfull + 16 * C::kHalves;
+  const uint32_t bar_drain = bar_tempty + 16 * C::kHalves;
   const uint32_t bar_swfull = bar_drain + 8;
   const uint32_t bar_swempty = bar_swfull + 8 * C::kNSW;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -224,9 +227,9 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
       mbar_init(bar_ufull + 8 * i, 4);
       mbar_init(bar_uempty + 8 * i, 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 2 * C::kHalves; ++i) {
       mbar_init(bar_tfull + 8 * i, 1);
-      mbar_init(bar_tempty + 8 * i, C::kEpiWarps);
+      mbar_init(bar_tempty + 8 * i, C::kEpiWarps / C::kHalves);
     }
     mbar_init(bar_drain, 1);
     for (int i = 0; i < C::kNSW; ++i) {
@@ -370,6 +373,7 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
     } else if (warp == 5 && lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc = make_idesc_e4m3(128, BN);
+      constexpr uint32_t idesc_half = make_idesc_e4m3(128, 128);
       uint32_t it = 0, ait = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
@@ -395,28 +399,38 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
           } else {
             b_base = smem_u32(smem + C::kOffB + s * C::kBLoadBytes);
           }
-          if constexpr (C::kGroupScale) {
-            a = ait & 1;
-            if (!mbar_wait(bar_tempty + 8 * a, ((ait >> 1) & 1) ^ 1, s_abort, p.status)) {
-              ok = false;
-              break;
-            }
-          }
-          tc_fence_after();
           const uint32_t a_base = smem_u32(smem + C::kOffA + s * C::kABytes);
-          const uint32_t d_tmem = tmem_base + a * BN;
+          if constexpr (C::kGroupScale) {
+            // one fresh partial per K group, written half by half (N = 128 each), each half
+            // handed to its epilogue warpgroup as soon as its 4 MMAs complete
+            a = ait & 1;
+            for (int h = 0; h < C::kHalves; ++h) {
+              const uint32_t slot = a * C::kHalves + h;
+              if (!mbar_wait(bar_tempty + 8 * slot, ((ait >> 1) & 1) ^ 1, s_abort, p.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t d_tmem = tmem_base + a * BN + h * 128;
+              const uint32_t b_half = b_base + h * 128 * 128;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t acc = (kk > 0 || (!C::kGroupScale && g > 0)) ? 1u : 0u;
-            mma_f8f6f4(d_tmem, make_sdesc_sw128(a_base + kk * 32),
-                       make_sdesc_sw128(b_base + kk * 32), idesc, acc);
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f8f6f4(d_tmem, make_sdesc_sw128(a_base + kk * 32),
+                           make_sdesc_sw128(b_half + kk * 32), idesc_half, kk > 0 ? 1u : 0u);
+              mma_commit(bar_tfull + 8 * slot);
+            }
+            if (!ok) break;
+            ++ait;
+          } else {
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + a * BN;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f8f6f4(d_tmem, make_sdesc_sw128(a_base + kk * 32),
+                         make_sdesc_sw128(b_base + kk * 32), idesc, (kk > 0 || g > 0) ? 1u : 0u);
           }
           mma_commit(bar_empty + 8 * s);
           if constexpr (C::kInt4) mma_commit(bar_uempty + 8 * u);
-          if constexpr (C::kGroupScale) {
-            mma_commit(bar_tfull + 8 * a);
-            ++ait;
-          }
         }
         if constexpr (!C::kGroupScale) {
           if (!ok) break;
@@ -435,7 +449,9 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
     const int wg = ewarp >> 2;
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int r_in = q * 32 + lane;
-    const int col_a = wg * 64, col_b = BN / 2 + wg * 64;
+    // warpgroup wg owns columns [wg*128, wg*128 + 128) of the tile: col_a.. and col_b..
+    const int col_a = wg * 128, col_b = wg * 128 + 64;
+    const uint32_t half_slot = C::kGroupScale ? static_cast<uint32_t>(wg) : 0u;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     float tensor_scale = 1.0f;
     if constexpr (!C::kGroupScale) tensor_scale = __ldg(p.sa_tensor) * __ldg(p.sw_tensor);
@@ -459,7 +475,8 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
           const uint32_t w = ait % C::kNSW;
           const float sa2 = (valid && g + 2 < G) ? __ldg(as_row + g + 2) : 0.0f;
           if (!mbar_wait(bar_swfull + 8 * w, (ait / C::kNSW) & 1, s_abort, p.status) ||
-              !mbar_wait(bar_tfull + 8 * a, (ait >> 1) & 1, s_abort, p.status)) {
+              !mbar_wait(bar_tfull + 8 * (a * C::kHalves + half_slot), (ait >> 1) & 1, s_abort,
+                         p.status)) {
             ok = false;
             break;
           }
@@ -494,7 +511,7 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(bar_tempty + 8 * a);
+            mbar_arrive(bar_tempty + 8 * (a * C::kHalves + half_slot));
             mbar_arrive(bar_swempty + 8 * w);
           }
           ++ait;
@@ -503,7 +520,8 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
         }
         if (!ok) break;
         if constexpr (EPI == kEpiSwiglu) {
-          // columns [col_a, col_a+64) are gate rows i, [col_b, col_b+64) the matching up rows
+          // columns [col_a, col_a+64) are gate rows i = wg*64.., [col_b, col_b+64) the matching
+          // up rows (the bank interleaves gate and up in blocks of 64 rows)
           float hv[64];
           float amax = 0.0f;
 #pragma unroll
@@ -735,6 +753,14 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s, fge_st
 // -------------------------------------------------------------------------------------
 // Load-time prepack of an int4 bank and its scales.
 // -------------------------------------------------------------------------------------
+// Row order of an interleaved gate_up bank: destination rows come in blocks of 128, each
+// 64 gate rows followed by the 64 matching up rows (gate = source rows [0, N/2), up =
+// [N/2, N)), so one 128-column half of a 256-column tile holds gate and up of 64 rows of I.
+__device__ __forceinline__ int64_t interleaved_source_row(int64_t rd, int64_t N) {
+  const int64_t blk = rd / 128, within = rd % 128;
+  return within < 64 ? blk * 64 + within : N / 2 + blk * 64 + (within - 64);
+}
+
 __global__ void w4_prepack_kernel(const uint32_t* __restrict__ w, uint32_t* __restrict__ wd,
                                   int E, int64_t N, int64_t words_per_row, int interleave,
                                   int fmt) {
@@ -745,10 +771,7 @@ __global__ void w4_prepack_kernel(const uint32_t* __restrict__ w, uint32_t* __re
     const int64_t rd = (i / words_per_row) % N;  // destination row
     const int64_t e = i / (words_per_row * N);
     int64_t rs = rd;
-    if (interleave) {
-      const int64_t tile = rd / 256, within = rd % 256;
-      rs = within < 128 ? tile * 128 + within : N / 2 + tile * 128 + (within - 128);
-    }
+    if (interleave) rs = interleaved_source_row(rd, N);
     uint32_t v = w[(e * N + rs) * words_per_row + wi];
     if (fmt == kBankSubnormal) {
       // nibble i holds element i; regroup so byte b holds elements b (low) and b+4 (high)
@@ -773,10 +796,7 @@ __global__ void w4_prepack_scale_kernel(const float* __restrict__ sw, float* __r
     const int64_t g = (i / N) % G;
     const int64_t e = i / (N * G);
     int64_t rs = nd;
-    if (interleave) {
-      const int64_t tile = nd / 256, within = nd % 256;
-      rs = within < 128 ? tile * 128 + within : N / 2 + tile * 128 + (within - 128);
-    }
+    if (interleave) rs = interleaved_source_row(nd, N);
     sd[i] = sw[(e * N + rs) * G + g] * mult;
   }
 }

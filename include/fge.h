@@ -137,9 +137,9 @@ fge_status fge_moe_permute(const int32_t* ids, int64_t T, int k, int E, const ui
  * element 2b in the low nibble and 2b+1 in the high nibble; w_scale [E, N, K/128] float.
  * Output: w_dev [E, N, K/2] in `format` (nibbles regrouped within each 8-element word for
  * FGE_W4_SUBNORMAL) and w_scale_dev [E, K/128, N] (transposed; times 2^9 for
- * FGE_W4_SUBNORMAL).  gate_up_interleave = 1 reorders rows so that every 256-row tile
- * holds 128 gate rows then the 128 matching up rows (gate = rows [0, N/2), up = rows
- * [N/2, N) of the input); required by FGE_EPI_SWIGLU_REQUANT.  Not part of the timed path. */
+ * FGE_W4_SUBNORMAL).  gate_up_interleave = 1 reorders rows in blocks of 128: 64 gate rows
+ * then the 64 matching up rows (gate = rows [0, N/2), up = rows [N/2, N) of the input);
+ * required by FGE_EPI_SWIGLU_REQUANT.  Not part of the timed path. */
 fge_status fge_w4_prepack(const uint8_t* w, const float* w_scale, int E, int64_t N, int64_t K,
                           int gate_up_interleave, fge_w4_format format, uint8_t* w_dev,
                           float* w_scale_dev, fge_stream_t stream);
