@@ -60,8 +60,8 @@ struct Cfg {
   // units in flight, the producer/MMA warpgroup needs few, the epilogue holds 128 fp32
   // accumulators per thread plus two TMEM chunks in flight.
   static constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8;
-  static constexpr int kRegsUnpack = 88;
-  static constexpr int kRegsCtrl = 40;
+  static constexpr int kRegsUnpack = 64;
+  static constexpr int kRegsCtrl = 32;
   static constexpr int kRegsHigh0 =
       (kLaunchRegs * kThreads - 128 * kRegsUnpack - 128 * kRegsCtrl) / kEpiThreads / 8 * 8;
   static constexpr int kRegsHigh = kRegsHigh0 > 240 ? 240 : kRegsHigh0;
@@ -128,6 +128,16 @@ __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
                  "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
                  "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+
+__device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31]));
 }
 
 // 8 int4 values (two's complement, nibble i = element i) -> e4m3 codes of the integers.
@@ -294,22 +304,26 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
           const uint8_t* src = smem + C::kOffB + s * C::kBLoadBytes + (tid >> 3) * 64 + (tid & 7) * 8;
           uint8_t* dst = smem + C::kOffBU + u * C::kBUBytes + (tid >> 3) * 128 +
                          (((tid & 7) ^ ((tid >> 3) & 7)) << 4);
-          // all loads first: source and destination are both shared memory, so a store
-          // in between would keep every later load waiting behind it
-          uint2 wv[BN / 16];
+          // loads are batched ahead of the stores: source and destination are both shared
+          // memory, so a store in between would keep every later load waiting behind it
 #pragma unroll
-          for (int i = 0; i < BN / 16; ++i) wv[i] = *reinterpret_cast<const uint2*>(src + i * 1024);
+          for (int i0 = 0; i0 < BN / 16; i0 += 8) {
+            uint2 wv[8];
 #pragma unroll
-          for (int i = 0; i < BN / 16; ++i) {
-            uint2 a, b;
-            if constexpr (BFMT == kBfmtInt4Sub) {
-              a = w4_to_e4m3_sub(wv[i].x);
-              b = w4_to_e4m3_sub(wv[i].y);
-            } else {
-              a = w4_to_e4m3_lut(wv[i].x);
-              b = w4_to_e4m3_lut(wv[i].y);
+            for (int i = 0; i < 8; ++i)
+              wv[i] = *reinterpret_cast<const uint2*>(src + (i0 + i) * 1024);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              uint2 a, b;
+              if constexpr (BFMT == kBfmtInt4Sub) {
+                a = w4_to_e4m3_sub(wv[i].x);
+                b = w4_to_e4m3_sub(wv[i].y);
+              } else {
+                a = w4_to_e4m3_lut(wv[i].x);
+                b = w4_to_e4m3_lut(wv[i].y);
+              }
+              *reinterpret_cast<uint4*>(dst + (i0 + i) * 2048) = make_uint4(a.x, a.y, b.x, b.y);
             }
-            *reinterpret_cast<uint4*>(dst + i * 2048) = make_uint4(a.x, a.y, b.x, b.y);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -484,28 +498,26 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
           const float* sws = reinterpret_cast<const float*>(smem + C::kOffSW + w * C::kSWBytes);
           const uint32_t tb = tmem_base + lane_addr + a * BN;
           const uint64_t sa2x = pack_f32x2(sa0, sa0);
-          uint32_t v[2][16];
-          tmem_ld_32x32b_x16(tb + col_a, v[0]);
+          // the warpgroup's 128 columns in 4 loads of 32, double-buffered: tcgen05.wait::ld
+          // waits for every outstanding load, so fewer and larger loads expose less latency
+          uint32_t v[2][32];
+          tmem_ld_32x32b_x32(tb + col_a, v[0]);
           tmem_wait_ld();
-          reg_fence16(v[0]);
+          reg_fence32(v[0]);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            if (c + 1 < 8) {
-              const int coln = (c + 1 < 4) ? col_a + (c + 1) * 16 : col_b + (c - 3) * 16;
-              tmem_ld_32x32b_x16(tb + coln, v[(c + 1) & 1]);
-            }
-            const int col = (c < 4) ? col_a + c * 16 : col_b + (c - 4) * 16;
-            const ulonglong2* sw2 = reinterpret_cast<const ulonglong2*>(sws + col);
+          for (int c = 0; c < 4; ++c) {
+            if (c + 1 < 4) tmem_ld_32x32b_x32(tb + col_a + (c + 1) * 32, v[(c + 1) & 1]);
+            const ulonglong2* sw2 = reinterpret_cast<const ulonglong2*>(sws + col_a + c * 32);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 8; ++i) {
               const ulonglong2 wv = sw2[i];  // 4 weight scales as two f32x2 pairs
               const uint32_t* vv = v[c & 1] + 4 * i;
-              fma2_pair(acc2[c * 8 + 2 * i], sa2x, wv.x, vv[0], vv[1]);
-              fma2_pair(acc2[c * 8 + 2 * i + 1], sa2x, wv.y, vv[2], vv[3]);
+              fma2_pair(acc2[c * 16 + 2 * i], sa2x, wv.x, vv[0], vv[1]);
+              fma2_pair(acc2[c * 16 + 2 * i + 1], sa2x, wv.y, vv[2], vv[3]);
             }
-            if (c + 1 < 8) {
+            if (c + 1 < 4) {
               tmem_wait_ld();
-              reg_fence16(v[(c + 1) & 1]);
+              reg_fence32(v[(c + 1) & 1]);
             }
           }
           tc_fence_before();
