@@ -45,6 +45,24 @@ def _kernel_key():
     return ":".join(parts)
 
 
+def job_step_ms(local_ms, device=None):
+    """Step time of the whole job: the max over ranks (the slowest replica sets the pace).
+    Uses the default torch.distributed group when one is initialised."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(local_ms)
+    t = torch.tensor([float(local_ms)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(tokens_per_rank, world, step_ms):
+    """Whole-job throughput: every rank processes its own tokens_per_rank per step."""
+    return world * tokens_per_rank / (step_ms / 1e3)
+
+
 def _dist():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -142,8 +160,8 @@ def run_reference(args):
     if rank != 0:
         return 0
     from workloads import moe_inputs
-    inp = moe_inputs(WORKLOAD, seed=0)
-    sample = 64
+    inp = moe_inputs(args.workload, seed=0)
+    sample = 64 if args.workload == "mid" else 16
     for _ in range(args.warmup):
         oracle_tokens_per_s(inp, sample, 0.0)
     times = []
@@ -162,7 +180,8 @@ def run_reference(args):
         "config": _config(inp, note="each step: the float64 CPU oracle on %d sampled tokens"
                           % sample),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": "%d random tokens of the T=4096 layer per step" % sample},
+                         "sample": "%d random tokens of the T=%d layer per step"
+                                   % (sample, inp.T)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -171,11 +190,14 @@ def run_reference(args):
 
 
 def _config(inp, note=None):
-    c = {"workload": "mid MoE layer prefill: T=%d tokens, H=%d, E=%d experts, I=%d, top-%d, "
-                     "int4 experts, e4m3 activations" % (inp.T, inp.H, inp.E, inp.I, inp.k),
+    c = {"workload": "%s MoE layer prefill: T=%d tokens, H=%d, E=%d experts, I=%d, top-%d, "
+                     "int4 experts, e4m3 activations"
+                     % (inp.name, inp.T, inp.H, inp.E, inp.I, inp.k),
          "T": inp.T, "H": inp.H, "E": inp.E, "I": inp.I, "k": inp.k,
          "global_batch": inp.T, "seq_len": inp.T, "parallelism": "replicas",
-         "l2": "flushed (256 MB write) before every timed step; weights 151 MB > L2"}
+         "l2": "flushed (256 MB write) before every timed step; resident int4 banks + "
+               "scales %.0f MB" % ((inp.w_gu.nbytes + inp.w_dn.nbytes + inp.s_gu.nbytes
+                                   + inp.s_dn.nbytes) / 1e6)}
     if note:
         c["note"] = note
     return c
@@ -200,7 +222,7 @@ def run_gpu(args):
         dist.barrier()
     fge.lib()
 
-    inp = moe_inputs(WORKLOAD, seed=rank)
+    inp = moe_inputs(args.workload, seed=rank)
     x_host = torch.from_numpy(inp.x_bits.view(np.int16)).view(torch.bfloat16)
     lg_host = torch.from_numpy(inp.logits)
     x = x_host.to(dev)
@@ -247,11 +269,8 @@ def run_gpu(args):
     if status != 0:
         raise RuntimeError("device status %d after the timed steps" % status)
     launches_per_step = 9   # topk, quant, permute x4, gate_up, down, combine
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * inp.T / (ms / 1e3)
+    ms = job_step_ms(ms, dev)
+    value = job_value(inp.T, world, ms)
 
     # ---- per-stage breakdown and the dominant kernel (gate_up grouped GEMM) timed alone
     stages = stage_times(fge, torch, inp, x, logits, w_gu, s_gu, w_dn, s_dn, fmt, flush, dev,
@@ -295,8 +314,8 @@ def run_gpu(args):
     if world == 1 and not args.no_cpu_baseline:
         rate, done, el = oracle_tokens_per_s(inp, 64, args.cpu_seconds)
         cpu = {"value": rate, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
-               "sample": "%d tokens (random 64-token samples of the T=4096 layer) in %.1f s"
-                         % (done, el)}
+               "sample": "%d tokens (random 64-token samples of the T=%d layer) in %.1f s"
+                         % (done, inp.T, el)}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -359,6 +378,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD, choices=["mid", "large", "tiny"],
+                    help="MoE layer workload (the headline line uses mid)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

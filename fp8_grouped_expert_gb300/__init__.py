@@ -49,6 +49,7 @@ SIGNATURES = {
     "fge_linear_w8a8_noalloc": [_P, _I64, _I64, _P, _P, _I64, _P, _P],
     "fge_moe_layer_forward": [_P, _P, _I64, _I64, _I, _I, _I64, _P, _P, _P, _P, _I, _I, _P, _P,
                               _SZ, _P],
+    "fge_selftest_wait_timeout": [_P, _I64, _P],
     "fge_rmsnorm": [_P, _I64, _I64, ctypes.c_float, _P, _P],
     "fge_router_logits": [_P, _P, _I64, _I64, _I, _P, _P],
     "fge_identity_attention": [_P, _I64, _I, _I, _P, _P],

@@ -62,7 +62,7 @@ constexpr long long kWaitBudgetCycles = 2000000000LL;
 // Bounded wait.  Returns false when the budget ran out or another role raised the CTA's
 // abort flag; the caller then stops issuing work and proceeds to the teardown.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* status) {
+                                          int32_t* status, long long budget = kWaitBudgetCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   uint32_t spins = 0;
@@ -70,7 +70,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     if (mbar_try_wait(bar, parity)) return true;
     if ((++spins & 63u) == 0) {
       if (*abort_flag) return false;
-      if (clock64() - t0 > kWaitBudgetCycles) {
+      if (clock64() - t0 > budget) {
         *abort_flag = 1;
         set_device_error(status, FGE_ERR_DEVICE_TIMEOUT);
         return false;

@@ -224,6 +224,15 @@ fge_status fge_moe_layer_forward(const float* logits, const void* x_bf16, int64_
                                  fge_dtype out_dtype, void* out, void* workspace,
                                  size_t workspace_bytes, fge_stream_t stream);
 
+/* selftest_wait_timeout -- exercises the device failure path without faulting anything: a
+ * one-warp kernel waits on an mbarrier that is never arrived on, with a budget of
+ * budget_cycles (1 .. 2^32) SM clock cycles; the wait gives up, writes
+ * FGE_ERR_DEVICE_TIMEOUT into the workspace status word and the kernel returns.  Read the
+ * result with fge_read_device_status.  The pipeline kernels use the same bounded wait with
+ * a budget of about one second. */
+fge_status fge_selftest_wait_timeout(void* workspace, int64_t budget_cycles,
+                                     fge_stream_t stream);
+
 /* Glue of the stacked prefill (not page steps; RMSNorm, router, attention stand-in).
  * rmsnorm: out_bf16[t] = h[t] / sqrt(mean(h[t]^2) + eps), h float [T, H].
  * router_logits: logits[t, e] = sum_h xn[t, h] * w[e, h] (fp32, sequential in h);
