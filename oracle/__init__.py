@@ -40,5 +40,7 @@ from .moe import (  # noqa: F401
     moe_combine,
     moe_layer_forward,
     linear_w8a8,
+    dequant_int4_bank,
+    moe_layer_int4_baseline,
 )
 from .stack import rmsnorm, router_logits, identity_attention, stacked_prefill  # noqa: F401

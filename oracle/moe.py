@@ -205,3 +205,33 @@ def linear_w8a8(x_f32, wq, sw, out_dtype="bf16"):
     xq, sa = quant_act_per_tensor(x_f32)
     y = linear_w8a8_gemm(xq, sa, wq, sw)
     return _round_out(y, out_dtype), xq, sa
+
+
+def dequant_int4_bank(w_packed, w_scale, k):
+    """Dequantized expert bank in float64: W[e, n, kk] = q[e, n, kk] * sw[e, n, kk // 128]."""
+    q = int4_unpack(w_packed, k).astype(np.float64)
+    s = np.repeat(np.asarray(w_scale, dtype=np.float64), GROUP, axis=-1)
+    return q * s
+
+
+def moe_layer_int4_baseline(logits, x_f32, k, w_gate_up, s_gate_up, w_down, s_down, inter,
+                            out_dtype="bf16"):
+    """The per-token int4 expert dispatch that the grouped GEMM replaces ("FP8 grouped-expert
+    prefill with on-chip int4-to-e4m3 dequant", section 1: its baseline runs one dispatch per
+    routed token with the int4 weights).  Reading: activations are not quantized; for each
+    routed (token, slot) the expert FFN is y = W_down (silu(W_gate x) * (W_up x)) with the
+    dequantized int4 weights, in float64; out[t] = sum_j gate_j * y_j, rounded to out_dtype.
+    Returns (out float32 values [T, H], ids)."""
+    ids, gates = topk_gate(logits, k)
+    x = np.asarray(x_f32, dtype=np.float64)
+    t_count, h = x.shape
+    out = np.zeros((t_count, h), dtype=np.float64)
+    for e in np.unique(ids):
+        tok, slot = np.nonzero(ids == e)
+        wgu = dequant_int4_bank(w_gate_up[e:e + 1], s_gate_up[e:e + 1], h)[0]
+        wdn = dequant_int4_bank(w_down[e:e + 1], s_down[e:e + 1], inter)[0]
+        c = x[tok] @ wgu.T
+        g, u = c[:, :inter], c[:, inter:2 * inter]
+        y = (g / (1.0 + np.exp(-g)) * u) @ wdn.T
+        out[tok] += gates[tok, slot].astype(np.float64)[:, None] * y
+    return _round_out(out, out_dtype), ids

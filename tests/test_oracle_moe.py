@@ -258,3 +258,41 @@ def test_rmsnorm_closed_form_and_identity_attention():
     for head in range(16):
         assert np.array_equal(a[:, head * 128:(head + 1) * 128],
                               v[:, (head // 4) * 128:(head // 4 + 1) * 128])
+
+
+# --- per-token int4 baseline ------------------------------------------------------------
+
+def test_dequant_bank_matches_grouped_gemm_on_exact_activations():
+    # integer activations (exact in e4m3) with unit activation scales: the grouped GEMM's
+    # definition and a plain matmul with the dequantized bank must agree
+    rng = np.random.default_rng(71)
+    e, n, kdim, r = 2, 6, 256, 5
+    a = rng.integers(-16, 17, size=(r, kdim)).astype(np.float32)
+    q = rng.integers(-8, 8, size=(e, n, kdim))
+    ws = rng.uniform(0.002, 0.02, size=(e, n, 2)).astype(np.float32)
+    wp = pack_int4(q)
+    offs = np.array([0, 3, 5], np.int32)
+    got = oracle.grouped_gemm_w4a8(oracle.e4m3_encode(a), np.ones((r, 2), np.float32), offs,
+                                   wp, ws)
+    w = oracle.dequant_int4_bank(wp, ws, kdim)
+    ref = np.concatenate([a[:3].astype(np.float64) @ w[0].T, a[3:].astype(np.float64) @ w[1].T])
+    assert np.allclose(got, ref, rtol=1e-13)
+    assert np.array_equal(w[1, 2, :128], q[1, 2, :128] * float(ws[1, 2, 0]))
+
+
+def test_int4_baseline_single_expert_closed_form():
+    # one expert, k = 1: the baseline is the expert FFN on each token with gate 1
+    rng = np.random.default_rng(72)
+    t, h, inter = 4, 128, 128
+    x = rng.standard_normal((t, h)).astype(np.float32)
+    q_gu = rng.integers(-8, 8, size=(1, 2 * inter, h))
+    q_dn = rng.integers(-8, 8, size=(1, h, inter))
+    s_gu = np.full((1, 2 * inter, 1), 0.01, np.float32)
+    s_dn = np.full((1, h, 1), 0.02, np.float32)
+    out, ids = oracle.moe_layer_int4_baseline(np.zeros((t, 1), np.float32), x, 1, pack_int4(q_gu),
+                                              s_gu, pack_int4(q_dn), s_dn, inter, out_dtype="f32")
+    c = x.astype(np.float64) @ (q_gu[0] * 0.01).T
+    hh = c[:, :inter] / (1 + np.exp(-c[:, :inter])) * c[:, inter:]
+    ref = hh @ (q_dn[0] * float(np.float32(0.02))).T
+    assert np.all(ids == 0)
+    assert np.allclose(out, ref.astype(np.float32), rtol=1e-6)
