@@ -228,10 +228,9 @@ def run_gpu(args):
     x = x_host.to(dev)
     logits = lg_host.to(dev)
     fmt = fge.W4_SUBNORMAL
-    w_gu, s_gu = fge.w4_prepack(torch.from_numpy(inp.w_gu).to(dev),
-                                torch.from_numpy(inp.s_gu).to(dev), True, fmt)
-    w_dn, s_dn = fge.w4_prepack(torch.from_numpy(inp.w_dn).to(dev),
-                                torch.from_numpy(inp.s_dn).to(dev), False, fmt)
+    canon = [torch.from_numpy(a).to(dev) for a in (inp.w_gu, inp.s_gu, inp.w_dn, inp.s_dn)]
+    w_gu, s_gu = fge.w4_prepack(canon[0], canon[1], True, fmt)
+    w_dn, s_dn = fge.w4_prepack(canon[2], canon[3], False, fmt)
     ws = fge.new_workspace(fge.workspace_bytes(fge.OP_MOE_LAYER, inp.T, inp.H, inp.I, inp.E,
                                                inp.k), dev)
     out = torch.empty((inp.T, inp.H), dtype=torch.bfloat16, device=dev)
@@ -275,6 +274,18 @@ def run_gpu(args):
     # ---- per-stage breakdown and the dominant kernel (gate_up grouped GEMM) timed alone
     stages = stage_times(fge, torch, inp, x, logits, w_gu, s_gu, w_dn, s_dn, fmt, flush, dev,
                          args.steps)
+
+    # ---- the per-token int4 dispatch that the grouped GEMM replaces (context, untimed)
+    base_ms = None
+    if not args.no_baseline:
+        fge.moe_layer_per_token_dispatch(logits, x, inp.k, inp.I, *canon)
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for _ in range(2):
+            fge.moe_layer_per_token_dispatch(logits, x, inp.k, inp.I, *canon)
+        b1.record(stream)
+        torch.cuda.synchronize()
+        base_ms = b0.elapsed_time(b1) / 2
 
     # ---- end to end through the public API with host buffers
     x_pin = x_host.pin_memory()
@@ -335,6 +346,10 @@ def run_gpu(args):
         "e2e": {"value": world * inp.T / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step * args.steps,
+        "per_token_dispatch_baseline": None if base_ms is None else {
+            "ms_per_step": base_ms, "grouped_speedup": base_ms / ms,
+            "what": "same layer, one CTA per routed token: int4 weights dequantized in "
+                    "registers, fp32 activations, no grouped GEMM"},
         "clocks": clocks.summary(),
     }
     print(json.dumps(line))
@@ -382,6 +397,8 @@ def main():
                     help="MoE layer workload (the headline line uses mid)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-baseline", action="store_true",
+                    help="skip the per-token int4 dispatch comparison")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

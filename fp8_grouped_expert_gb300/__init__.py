@@ -22,6 +22,7 @@ DTYPE_BF16, DTYPE_F32 = 0, 1
 EPI_STORE, EPI_SWIGLU_REQUANT = 0, 1
 W4_LUT, W4_SUBNORMAL = 0, 1
 OP_QUANT_PER_TENSOR, OP_PERMUTE, OP_GROUPED_GEMM, OP_LINEAR_W8A8, OP_MOE_LAYER = range(5)
+OP_DISPATCH_BASELINE = 5
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -46,6 +47,8 @@ SIGNATURES = {
     "fge_moe_combine": [_P, _I, _P, _P, _I64, _I, _I64, _I, _P, _P],
     "fge_gemm_w8a8": [_P, _P, _I64, _I64, _P, _P, _I64, _I, _P, _P, _SZ, _P],
     "fge_linear_w8a8": [_P, _I64, _I64, _P, _P, _I64, _P, _P, _SZ, _P],
+    "fge_moe_layer_per_token_dispatch": [_P, _P, _I64, _I64, _I, _I, _I64, _P, _P, _P, _P, _I,
+                                         _P, _P, _SZ, _P],
     "fge_linear_w8a8_noalloc": [_P, _I64, _I64, _P, _P, _I64, _P, _P],
     "fge_moe_layer_forward": [_P, _P, _I64, _I64, _I, _I, _I64, _P, _P, _P, _P, _I, _I, _P, _P,
                               _SZ, _P],
@@ -302,6 +305,24 @@ def moe_layer_forward(logits, x, k, inter, w_gu_dev, s_gu_dev, w_dn_dev, s_dn_de
                                        DTYPE_F32 if out_dtype == torch.float32 else DTYPE_BF16,
                                        _ptr(y), _ptr(ws), ws.numel(), _stream(x)),
            "fge_moe_layer_forward")
+    return y
+
+
+def moe_layer_per_token_dispatch(logits, x, k, inter, w_gu, s_gu, w_dn, s_dn,
+                                 out_dtype=torch.bfloat16, workspace=None, out=None):
+    """Per-token int4 dispatch baseline (canonical, unprepacked int4 banks)."""
+    _need(logits, torch.float32, "logits")
+    _need(x, torch.bfloat16, "x")
+    _ensure_init(x.device)
+    t, h = x.shape
+    e = logits.shape[1]
+    ws = workspace if workspace is not None else new_workspace(
+        workspace_bytes(OP_DISPATCH_BASELINE, t, h, inter, e, k), x.device)
+    y = out if out is not None else torch.empty((t, h), dtype=out_dtype, device=x.device)
+    _check(lib().fge_moe_layer_per_token_dispatch(
+        _ptr(logits), _ptr(x), t, h, e, k, inter, _ptr(w_gu), _ptr(s_gu), _ptr(w_dn), _ptr(s_dn),
+        DTYPE_F32 if out_dtype == torch.float32 else DTYPE_BF16, _ptr(y), _ptr(ws), ws.numel(),
+        _stream(x)), "fge_moe_layer_per_token_dispatch")
     return y
 
 

@@ -130,6 +130,10 @@ size_t fge_workspace_bytes(fge_op op, int64_t a, int64_t b, int64_t c, int E, in
     case FGE_OP_GROUPED_GEMM: return kWsHeaderBytes;
     case FGE_OP_LINEAR_W8A8: return kWsHeaderBytes + align_up(static_cast<size_t>(a * b), 256);
     case FGE_OP_MOE_LAYER: return carve_layer(nullptr, a, b, c, E, k).bytes;
+    case FGE_OP_DISPATCH_BASELINE: {
+      const size_t r = static_cast<size_t>(a) * k;
+      return kWsHeaderBytes + 3 * align_up(r * 4, 256) + align_up(r * b * 4, 256);
+    }
   }
   return 0;
 }
@@ -339,6 +343,37 @@ fge_status fge_moe_layer_forward(const float* logits, const void* x, int64_t T, 
   FGE_CHECK(grouped_common(w.hq, w.hs, w.offsets, R, w_dn, s_dn, E, H, I, format, 0, nullptr,
                            out_f32 ? 0 : 1, w.y, nullptr, ws, ws_bytes, stream));
   return from_cuda(launch_combine(w.y, out_f32, w.token_row, w.gates, T, k, H, out_f32, out, stream));
+}
+
+fge_status fge_moe_layer_per_token_dispatch(const float* logits, const void* x, int64_t T,
+                                            int64_t H, int E, int k, int64_t I,
+                                            const uint8_t* w_gu, const float* s_gu,
+                                            const uint8_t* w_dn, const float* s_dn,
+                                            fge_dtype out_dtype, void* out, void* ws,
+                                            size_t ws_bytes, fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(logits && x && w_gu && s_gu && w_dn && s_dn && out && ws, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(out_dtype == FGE_DTYPE_BF16 || out_dtype == FGE_DTYPE_F32, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(T >= 0 && H > 0 && H % 128 == 0 && H <= 8192 && I > 0 && I % 128 == 0 &&
+                  I <= 8192,
+              FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(E >= 1 && E <= 1024 && k >= 1 && k <= E && k <= 32 && T * k < (1LL << 31),
+              FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(al16(x) && al16(ws) && al16(out) && al16(w_gu) && al16(w_dn), FGE_ERR_MISALIGNED);
+  FGE_REQUIRE(ws_bytes >= fge_workspace_bytes(FGE_OP_DISPATCH_BASELINE, T, H, I, E, k),
+              FGE_ERR_WORKSPACE_TOO_SMALL);
+  if (T == 0) return FGE_OK;
+  const size_t r = static_cast<size_t>(T) * k;
+  uint8_t* base = static_cast<uint8_t*>(ws) + kWsHeaderBytes;
+  int32_t* ids = reinterpret_cast<int32_t*>(base);
+  float* gates = reinterpret_cast<float*>(base + align_up(r * 4, 256));
+  int32_t* token_row = reinterpret_cast<int32_t*>(base + 2 * align_up(r * 4, 256));
+  float* y = reinterpret_cast<float*>(base + 3 * align_up(r * 4, 256));
+  FGE_CHECK(from_cuda(launch_topk_gate(logits, T, E, k, ids, gates, stream)));
+  FGE_CHECK(from_cuda(launch_per_token_dispatch(static_cast<const uint16_t*>(x), ids, T, k, H, I,
+                                                w_gu, s_gu, w_dn, s_dn, y, token_row, stream)));
+  return from_cuda(launch_combine(y, 1, token_row, gates, T, k, H,
+                                  out_dtype == FGE_DTYPE_F32, out, stream));
 }
 
 fge_status fge_rmsnorm(const float* h, int64_t T, int64_t H, float eps, void* out,

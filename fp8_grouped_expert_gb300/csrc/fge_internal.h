@@ -77,6 +77,11 @@ cudaError_t launch_identity_attention(const uint16_t* v, int64_t T, int n_heads,
                                       uint16_t* attn, cudaStream_t s);
 cudaError_t launch_residual_add(float* h, const void* y, int y_f32, int64_t n, cudaStream_t s);
 
+cudaError_t launch_per_token_dispatch(const uint16_t* x, const int32_t* ids, int64_t T, int k,
+                                      int64_t H, int64_t I, const uint8_t* w_gu,
+                                      const float* s_gu, const uint8_t* w_dn, const float* s_dn,
+                                      float* y, int32_t* token_row, cudaStream_t s);
+
 int num_sms();
 
 }  // namespace fge

@@ -75,7 +75,8 @@ typedef enum {
   FGE_OP_PERMUTE = 1,          /* args: (T, H, -, E, k) */
   FGE_OP_GROUPED_GEMM = 2,     /* args: unused */
   FGE_OP_LINEAR_W8A8 = 3,      /* args: (M, K) */
-  FGE_OP_MOE_LAYER = 4         /* args: (T, H, I, E, k) */
+  FGE_OP_MOE_LAYER = 4,        /* args: (T, H, I, E, k) */
+  FGE_OP_DISPATCH_BASELINE = 5 /* args: (T, H, I, E, k) */
 } fge_op;
 
 /* Library version (major*10000 + minor*100 + patch). */
@@ -190,6 +191,21 @@ fge_status fge_gemm_w8a8(const uint8_t* aq, const float* sa, int64_t M, int64_t 
 fge_status fge_linear_w8a8(const void* x_bf16, int64_t M, int64_t K, const uint8_t* wq,
                            const float* w_scale, int64_t N, void* y_bf16, void* workspace,
                            size_t workspace_bytes, fge_stream_t stream);
+
+/* moe_layer_per_token_dispatch -- the baseline the grouped GEMM replaces ("FP8
+ * grouped-expert prefill ..." section 1: one dispatch per routed token per layer): one CTA
+ * per routed (token, slot) runs that expert's FFN on the token with int4 weights
+ * dequantized in registers (q * per-group scale), bf16 activations in fp32, SwiGLU in fp32
+ * and no activation quantization; then the combine.  Same routing as
+ * fge_moe_layer_forward.  Weights in the canonical layout of fge_w4_prepack's input
+ * (w_gu [E, 2I, H/2] with gate rows then up rows, s_gu [E, 2I, H/128], w_dn [E, H, I/2],
+ * s_dn [E, H, I/128]).  Workspace: FGE_OP_DISPATCH_BASELINE with (T, H, I, E, k). */
+fge_status fge_moe_layer_per_token_dispatch(const float* logits, const void* x_bf16, int64_t T,
+                                            int64_t H, int E, int k, int64_t I,
+                                            const uint8_t* w_gu, const float* s_gu,
+                                            const uint8_t* w_dn, const float* s_dn,
+                                            fge_dtype out_dtype, void* out, void* workspace,
+                                            size_t workspace_bytes, fge_stream_t stream);
 
 /* linear_w8a8_noalloc -- the same projection as fge_linear_w8a8 for callers that cannot
  * allocate device memory: hosts that own all device memory through their own pool and forbid
