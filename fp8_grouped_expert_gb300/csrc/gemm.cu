@@ -5,9 +5,9 @@
 //
 // Per CTA (one per SM), warp roles:
 //   warps 0-3   unpack: int4 tile (shared memory) -> e4m3 in the 128-byte swizzle layout
-//   warp  4     TMA producer: A tile [128 rows x 128 K] + B tile per K group
-//   warp  5     TMEM allocator and single-thread tcgen05.mma issuer (kind::f8f6f4)
-//   warps 6-7   idle
+//   warp  6     TMA producer: A tile [128 rows x 128 K] + B tile per K group
+//   warp  7     TMEM allocator and single-thread tcgen05.mma issuer (kind::f8f6f4)
+//   warps 4-5   idle
 //   warps 8..   epilogue warpgroups: per-group fp32 promotion acc += as*sw*P from TMEM,
 //               then the store / SwiGLU + requant epilogue
 // A K group (128 values) is exactly one 128-byte swizzle atom row, so each pipeline
@@ -22,6 +22,8 @@ namespace fge {
 
 enum { kBfmtInt4Lut = 0, kBfmtInt4Sub = 1, kBfmtE4m3 = 2 };
 enum { kEpiF32 = 0, kEpiBf16 = 1, kEpiSwiglu = 2 };
+// control warps (warpgroup 1); epilogue warps 8..15 keep their lane quarters
+constexpr int kProducerWarp = 6, kMmaWarp = 7;
 
 struct GemmParams {
   const float* as;         // [R, G] activation group scales
@@ -55,7 +57,7 @@ struct Cfg {
   static constexpr int kTmemCols = 2 * BN;
   // group mode: each epilogue warpgroup owns 128 columns ("half") of every TMEM buffer with
   // its own full/empty barriers, so the halves pipeline independently of each other
-  static constexpr int kHalves = kGroupScale ? BN / 128 : 1;
+  static constexpr int kHalves = 1;  // one hand-off per buffer: N = BN per MMA instruction
   // register split (group mode only): the unpack warpgroup keeps a working set for 16
   // units in flight, the producer/MMA warpgroup needs few, the epilogue holds 128 fp32
   // accumulators per thread plus two TMEM chunks in flight.
@@ -255,7 +257,7 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
     s_off[0] = 0;
     s_off[1] = p.dense_rows;
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(s_tmem), C::kTmemCols);
     tmem_relinquish();
     tc_fence_before();
@@ -336,7 +338,7 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
     }
   } else if (warp < 8) {
     if constexpr (C::kGroupScale) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsCtrl));
-    if (warp == 4 && lane == 0) {
+    if (warp == kProducerWarp && lane == 0) {
       // ---------------------------------------------------------------- TMA producer
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
@@ -384,10 +386,10 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
         for (uint32_t i = first_w; i < issued; ++i)
           mbar_wait_drain(bar_swfull + 8 * (i % C::kNSW), (i / C::kNSW) & 1);
       }
-    } else if (warp == 5 && lane == 0) {
+    } else if (warp == kMmaWarp && lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc = make_idesc_e4m3(128, BN);
-      constexpr uint32_t idesc_half = make_idesc_e4m3(128, 128);
+      constexpr uint32_t idesc_half = make_idesc_e4m3(128, BN / C::kHalves);
       uint32_t it = 0, ait = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
@@ -425,8 +427,9 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
                 break;
               }
               tc_fence_after();
-              const uint32_t d_tmem = tmem_base + a * BN + h * 128;
-              const uint32_t b_half = b_base + h * 128 * 128;
+              constexpr int kHalfN = BN / C::kHalves;
+              const uint32_t d_tmem = tmem_base + a * BN + h * kHalfN;
+              const uint32_t b_half = b_base + h * kHalfN * 128;
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
                 mma_f8f6f4(d_tmem, make_sdesc_sw128(a_base + kk * 32),
@@ -465,7 +468,7 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
     const int r_in = q * 32 + lane;
     // warpgroup wg owns columns [wg*128, wg*128 + 128) of the tile: col_a.. and col_b..
     const int col_a = wg * 128, col_b = wg * 128 + 64;
-    const uint32_t half_slot = C::kGroupScale ? static_cast<uint32_t>(wg) : 0u;
+    const uint32_t half_slot = C::kHalves > 1 ? static_cast<uint32_t>(wg) : 0u;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     float tensor_scale = 1.0f;
     if constexpr (!C::kGroupScale) tensor_scale = __ldg(p.sa_tensor) * __ldg(p.sw_tensor);
@@ -646,7 +649,7 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
   // ---------------------------------------------------------------------- teardown
   __syncwarp();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
