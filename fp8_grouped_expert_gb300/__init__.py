@@ -17,12 +17,13 @@ LIB_PATH = os.path.join(_PKG, "libfge.so")
 
 # enums of include/fge.h
 OK = 0
-SCALE_PER_TENSOR, SCALE_PER_TOKEN_G128 = 0, 1
+SCALE_PER_TENSOR, SCALE_PER_TOKEN_G128, SCALE_PER_ROW = 0, 1, 2
 DTYPE_BF16, DTYPE_F32 = 0, 1
 EPI_STORE, EPI_SWIGLU_REQUANT = 0, 1
 W4_LUT, W4_SUBNORMAL = 0, 1
 OP_QUANT_PER_TENSOR, OP_PERMUTE, OP_GROUPED_GEMM, OP_LINEAR_W8A8, OP_MOE_LAYER = range(5)
 OP_DISPATCH_BASELINE = 5
+OP_LINEAR_W8A8_ROWS = 6
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -47,6 +48,8 @@ SIGNATURES = {
     "fge_moe_combine": [_P, _I, _P, _P, _I64, _I, _I64, _I, _P, _P],
     "fge_gemm_w8a8": [_P, _P, _I64, _I64, _P, _P, _I64, _I, _P, _P, _SZ, _P],
     "fge_linear_w8a8": [_P, _I64, _I64, _P, _P, _I64, _P, _P, _SZ, _P],
+    "fge_gemm_w8a8_rows": [_P, _P, _I64, _I64, _P, _P, _I64, _I, _P, _P, _SZ, _P],
+    "fge_linear_w8a8_rows": [_P, _I64, _I64, _P, _P, _I64, _P, _P, _SZ, _P],
     "fge_moe_layer_per_token_dispatch": [_P, _P, _I64, _I64, _I, _I, _I64, _P, _P, _P, _P, _I,
                                          _P, _P, _SZ, _P],
     "fge_linear_w8a8_noalloc": [_P, _I64, _I64, _P, _P, _I64, _P, _P],
@@ -138,7 +141,8 @@ def clear_device_status(ws):
 
 # ------------------------------------------------------------------------------ ops
 def fp8_quant_act(x, mode="g128", workspace=None):
-    """x: bf16 [M, K] -> (xq uint8 [M, K], xs float32 [M, K/128] or [1])."""
+    """x: bf16 [M, K] -> (xq uint8 [M, K], xs float32 [M, K/128] ("g128"), [M] ("row") or
+    [1] ("tensor"))."""
     _need(x, torch.bfloat16, "x")
     _ensure_init(x.device)
     m, k = x.shape
@@ -146,6 +150,10 @@ def fp8_quant_act(x, mode="g128", workspace=None):
     if mode == "g128":
         xs = torch.empty((m, k // 128), dtype=torch.float32, device=x.device)
         code = lib().fge_fp8_quant_act(_ptr(x), m, k, SCALE_PER_TOKEN_G128, _ptr(xq), _ptr(xs),
+                                       None, 0, _stream(x))
+    elif mode == "row":
+        xs = torch.empty((m,), dtype=torch.float32, device=x.device)
+        code = lib().fge_fp8_quant_act(_ptr(x), m, k, SCALE_PER_ROW, _ptr(xq), _ptr(xs),
                                        None, 0, _stream(x))
     else:
         xs = torch.empty((1,), dtype=torch.float32, device=x.device)
@@ -287,6 +295,39 @@ def linear_w8a8(x, wq, w_scale, workspace=None, out=None):
     y = out if out is not None else torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
     _check(lib().fge_linear_w8a8(_ptr(x), m, k, _ptr(wq), _ptr(w_scale), n, _ptr(y), _ptr(ws),
                                  ws.numel(), _stream(x)), "fge_linear_w8a8")
+    return y
+
+
+def gemm_w8a8_rows(aq, sa_rows, wq, sw, out_dtype=torch.bfloat16, workspace=None):
+    """One-group W8A8 GEMM with one activation scale per row: sa_rows float32 [M]."""
+    _need(aq, torch.uint8, "aq")
+    _need(wq, torch.uint8, "wq")
+    _need(sa_rows, torch.float32, "sa_rows")
+    _ensure_init(aq.device)
+    m, k = aq.shape
+    n = wq.shape[0]
+    ws = workspace if workspace is not None else new_workspace(
+        workspace_bytes(OP_GROUPED_GEMM), aq.device)
+    y = torch.empty((m, n), dtype=out_dtype, device=aq.device)
+    _check(lib().fge_gemm_w8a8_rows(_ptr(aq), _ptr(sa_rows), m, k, _ptr(wq), _ptr(sw), n,
+                                    DTYPE_F32 if out_dtype == torch.float32 else DTYPE_BF16,
+                                    _ptr(y), _ptr(ws), ws.numel(), _stream(aq)),
+           "fge_gemm_w8a8_rows")
+    return y
+
+
+def linear_w8a8_rows(x, wq, w_scale, workspace=None, out=None):
+    """Dense projection with row-wise activation scales (per-row quant + GEMM), bf16 out."""
+    _need(x, torch.bfloat16, "x")
+    _need(wq, torch.uint8, "wq")
+    _ensure_init(x.device)
+    m, k = x.shape
+    n = wq.shape[0]
+    ws = workspace if workspace is not None else new_workspace(
+        workspace_bytes(OP_LINEAR_W8A8_ROWS, m, k), x.device)
+    y = out if out is not None else torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
+    _check(lib().fge_linear_w8a8_rows(_ptr(x), m, k, _ptr(wq), _ptr(w_scale), n, _ptr(y),
+                                      _ptr(ws), ws.numel(), _stream(x)), "fge_linear_w8a8_rows")
     return y
 
 

@@ -130,6 +130,9 @@ size_t fge_workspace_bytes(fge_op op, int64_t a, int64_t b, int64_t c, int E, in
     case FGE_OP_GROUPED_GEMM: return kWsHeaderBytes;
     case FGE_OP_LINEAR_W8A8: return kWsHeaderBytes + align_up(static_cast<size_t>(a * b), 256);
     case FGE_OP_MOE_LAYER: return carve_layer(nullptr, a, b, c, E, k).bytes;
+    case FGE_OP_LINEAR_W8A8_ROWS:
+      return kWsHeaderBytes + align_up(static_cast<size_t>(a * b), 256) +
+             align_up(static_cast<size_t>(a) * 4, 256);
     case FGE_OP_DISPATCH_BASELINE: {
       const size_t r = static_cast<size_t>(a) * k;
       return kWsHeaderBytes + 3 * align_up(r * 4, 256) + align_up(r * b * 4, 256);
@@ -158,6 +161,9 @@ fge_status fge_fp8_quant_act(const void* x, int64_t M, int64_t K, fge_scale_mode
   FGE_REQUIRE(al16(x) && al16(xq), FGE_ERR_MISALIGNED);
   if (mode == FGE_SCALE_PER_TOKEN_G128) {
     return from_cuda(launch_quant_g128(static_cast<const uint16_t*>(x), M, K, xq, xs, stream));
+  }
+  if (mode == FGE_SCALE_PER_ROW) {
+    return from_cuda(launch_quant_rows(static_cast<const uint16_t*>(x), M, K, xq, xs, stream));
   }
   FGE_REQUIRE(mode == FGE_SCALE_PER_TENSOR, FGE_ERR_INVALID_ARG);
   FGE_REQUIRE(ws, FGE_ERR_INVALID_ARG);
@@ -208,7 +214,8 @@ static fge_status grouped_common(const uint8_t* aq, const float* as, const int32
                                  int64_t R, const uint8_t* w, const float* sw, int E, int64_t N,
                                  int64_t K, int format, int per_tensor, const float* sa_t,
                                  int epilogue, void* out, float* out_scales, void* ws,
-                                 size_t ws_bytes, fge_stream_t stream) {
+                                 size_t ws_bytes, fge_stream_t stream,
+                                 const float* sa_rows = nullptr) {
   FGE_REQUIRE(R >= 0 && R < (1LL << 31) && N > 0 && N % 128 == 0 && N < (1LL << 24) && K > 0 &&
                   K % 128 == 0 && K < (1LL << 24),
               FGE_ERR_BAD_SHAPE);
@@ -222,6 +229,7 @@ static fge_status grouped_common(const uint8_t* aq, const float* as, const int32
   a.aq = aq;
   a.as = as;
   a.sa_tensor = sa_t;
+  a.sa_rows = sa_rows;
   a.offsets = offsets;
   a.w = w;
   a.sw = sw;
@@ -312,6 +320,32 @@ fge_status fge_linear_w8a8(const void* x, int64_t M, int64_t K, const uint8_t* w
                                               &hdr->scale, hdr, stream)));
   return grouped_common(xq, nullptr, nullptr, M, wq, w_scale, 1, N, K, 0, 1, &hdr->scale, 1, y,
                         nullptr, ws, ws_bytes, stream);
+}
+
+fge_status fge_gemm_w8a8_rows(const uint8_t* aq, const float* sa, int64_t M, int64_t K,
+                              const uint8_t* wq, const float* sw, int64_t N, fge_dtype out_dtype,
+                              void* y, void* ws, size_t ws_bytes, fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(sa, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(out_dtype == FGE_DTYPE_BF16 || out_dtype == FGE_DTYPE_F32, FGE_ERR_INVALID_ARG);
+  return grouped_common(aq, nullptr, nullptr, M, wq, sw, 1, N, K, 0, 1, nullptr,
+                        out_dtype == FGE_DTYPE_F32 ? 0 : 1, y, nullptr, ws, ws_bytes, stream, sa);
+}
+
+fge_status fge_linear_w8a8_rows(const void* x, int64_t M, int64_t K, const uint8_t* wq,
+                                const float* w_scale, int64_t N, void* y, void* ws,
+                                size_t ws_bytes, fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(x && wq && w_scale && y && ws, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(M >= 0 && K > 0 && K % 128 == 0 && N > 0 && N % 128 == 0, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(al16(x) && al16(ws), FGE_ERR_MISALIGNED);
+  FGE_REQUIRE(ws_bytes >= fge_workspace_bytes(FGE_OP_LINEAR_W8A8_ROWS, M, K, 0, 0, 0),
+              FGE_ERR_WORKSPACE_TOO_SMALL);
+  uint8_t* xq = static_cast<uint8_t*>(ws) + kWsHeaderBytes;
+  float* xs = reinterpret_cast<float*>(xq + align_up(static_cast<size_t>(M * K), 256));
+  FGE_CHECK(from_cuda(launch_quant_rows(static_cast<const uint16_t*>(x), M, K, xq, xs, stream)));
+  return grouped_common(xq, nullptr, nullptr, M, wq, w_scale, 1, N, K, 0, 1, nullptr, 1, y,
+                        nullptr, ws, ws_bytes, stream, xs);
 }
 
 fge_status fge_moe_layer_forward(const float* logits, const void* x, int64_t T, int64_t H, int E,

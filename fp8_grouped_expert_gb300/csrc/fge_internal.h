@@ -32,6 +32,8 @@ enum BankFormat { kBankLut = 0, kBankSubnormal = 1 };
 // Launchers (return a cudaError_t from the launch; argument checks happen in the API layer).
 cudaError_t launch_quant_g128(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,
                               cudaStream_t s);
+cudaError_t launch_quant_rows(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,
+                              cudaStream_t s);
 cudaError_t launch_quant_per_tensor(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq,
                                     float* xs, WsHeader* hdr, cudaStream_t s);
 cudaError_t launch_topk_gate(const float* logits, int64_t T, int E, int k, int32_t* ids,
@@ -55,6 +57,7 @@ struct GroupedGemmArgs {
   const uint8_t* aq;        // [R, K] e4m3 codes
   const float* as;          // [R, K/128] (group mode)
   const float* sa_tensor;   // device scalar (per-tensor mode)
+  const float* sa_rows;     // [R] per-row activation scales (per-tensor mode), or null
   const int32_t* offsets;   // [E+1]
   const uint8_t* w;         // int4 bank [E, N, K/2] (prepacked) or e4m3 [N, K]
   const float* sw;          // [E, K/128, N] prepacked group scales, or device scalar

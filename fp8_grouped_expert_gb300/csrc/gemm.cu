@@ -29,6 +29,7 @@ struct GemmParams {
   const float* as;         // [R, G] activation group scales
   const float* sw;         // [E, G, N] prepacked weight group scales
   const float* sa_tensor;  // per-tensor activation scale (device scalar)
+  const float* sa_rows;    // per-row activation scales [rows] (one-group path), or null
   const float* sw_tensor;  // per-tensor weight scale (device scalar)
   const int32_t* offsets;  // [E+1]
   void* out;
@@ -471,7 +472,8 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
     const uint32_t half_slot = C::kHalves > 1 ? static_cast<uint32_t>(wg) : 0u;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     float tensor_scale = 1.0f;
-    if constexpr (!C::kGroupScale) tensor_scale = __ldg(p.sa_tensor) * __ldg(p.sw_tensor);
+    if constexpr (!C::kGroupScale)
+      tensor_scale = p.sa_rows ? __ldg(p.sw_tensor) : __ldg(p.sa_tensor) * __ldg(p.sw_tensor);
     uint32_t ait = 0;
     int tile_parity = 0;
     bool ok = true;
@@ -598,6 +600,9 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
         }
       } else {
         // per-tensor scales: the whole K accumulated in TMEM; one scalar in the epilogue
+        // (per-row activation scales: that row's scale times the weight scale)
+        const float rs = p.sa_rows ? (valid ? __ldg(p.sa_rows + row) : 0.0f) * tensor_scale
+                                   : tensor_scale;
         const uint32_t a = ait & 1;
         if (!mbar_wait(bar_tfull + 8 * a, (ait >> 1) & 1, s_abort, p.status)) break;
         tc_fence_after();
@@ -620,17 +625,17 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
 #pragma unroll
               for (int i = 0; i < 16; i += 4)
                 *reinterpret_cast<float4*>(o + i) = make_float4(
-                    tensor_scale * __uint_as_float(vv[i]), tensor_scale * __uint_as_float(vv[i + 1]),
-                    tensor_scale * __uint_as_float(vv[i + 2]), tensor_scale * __uint_as_float(vv[i + 3]));
+                    rs * __uint_as_float(vv[i]), rs * __uint_as_float(vv[i + 1]),
+                    rs * __uint_as_float(vv[i + 2]), rs * __uint_as_float(vv[i + 3]));
             } else {
               __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * p.N + ti.n0 + col;
 #pragma unroll
               for (int i = 0; i < 16; i += 8)
                 *reinterpret_cast<uint4*>(o + i) = make_uint4(
-                    pack_bf16x2(tensor_scale * __uint_as_float(vv[i]), tensor_scale * __uint_as_float(vv[i + 1])),
-                    pack_bf16x2(tensor_scale * __uint_as_float(vv[i + 2]), tensor_scale * __uint_as_float(vv[i + 3])),
-                    pack_bf16x2(tensor_scale * __uint_as_float(vv[i + 4]), tensor_scale * __uint_as_float(vv[i + 5])),
-                    pack_bf16x2(tensor_scale * __uint_as_float(vv[i + 6]), tensor_scale * __uint_as_float(vv[i + 7])));
+                    pack_bf16x2(rs * __uint_as_float(vv[i]), rs * __uint_as_float(vv[i + 1])),
+                    pack_bf16x2(rs * __uint_as_float(vv[i + 2]), rs * __uint_as_float(vv[i + 3])),
+                    pack_bf16x2(rs * __uint_as_float(vv[i + 4]), rs * __uint_as_float(vv[i + 5])),
+                    pack_bf16x2(rs * __uint_as_float(vv[i + 6]), rs * __uint_as_float(vv[i + 7])));
             }
           }
           if (c + 1 < 8) {
@@ -732,6 +737,7 @@ static cudaError_t run(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st)
   p.as = a.as;
   p.sw = a.per_tensor ? nullptr : a.sw;
   p.sa_tensor = a.sa_tensor;
+  p.sa_rows = a.sa_rows;
   p.sw_tensor = a.per_tensor ? a.sw : nullptr;
   p.offsets = a.offsets;
   p.out = a.out;

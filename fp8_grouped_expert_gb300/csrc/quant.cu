@@ -1,5 +1,5 @@
-// fp8_quant_act: dynamic e4m3 activation quantization, per (row, 128-element group) or per
-// tensor ("FP8 grouped-expert prefill with on-chip int4-to-e4m3 dequant", section 1;
+// fp8_quant_act: dynamic e4m3 activation quantization, per (row, 128-element group), per row
+// or per tensor ("FP8 grouped-expert prefill with on-chip int4-to-e4m3 dequant", section 1;
 // "Module fp8_ffi": amax reduce -> scale finalize -> e4m3 quantize on one stream).
 // HBM-bound: 16-byte vector loads and stores, warp-shuffle amax, grids sized to the SMs.
 #include <algorithm>
@@ -83,6 +83,49 @@ __global__ void cast_per_tensor_kernel(const uint4* __restrict__ x, int64_t n8,
                      __fdiv_rn(bf16_lo(v.w), s), __fdiv_rn(bf16_hi(v.w), s));
     xq[i] = q;
   }
+}
+
+// One scale per row (token): one warp per row, two passes over the row (amax, then the
+// cast; the second pass reads the row back from L1/L2).
+__global__ void quant_row_kernel(const uint4* __restrict__ x, int64_t M, int64_t n8_row,
+                                 uint2* __restrict__ xq, float* __restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t r = wid; r < M; r += nw) {
+    const uint4* xr = x + r * n8_row;
+    float amax = 0.0f;
+    for (int64_t i = lane; i < n8_row; i += 32) {
+      const uint4 v = __ldg(xr + i);
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
+                               fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)))));
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))),
+                               fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)))));
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    const float s = scale_from_amax(amax);
+    uint2* qr = xq + r * n8_row;
+    for (int64_t i = lane; i < n8_row; i += 32) {
+      const uint4 v = __ldg(xr + i);
+      uint2 q;
+      q.x = cvt_e4m3x4(__fdiv_rn(bf16_lo(v.x), s), __fdiv_rn(bf16_hi(v.x), s),
+                       __fdiv_rn(bf16_lo(v.y), s), __fdiv_rn(bf16_hi(v.y), s));
+      q.y = cvt_e4m3x4(__fdiv_rn(bf16_lo(v.z), s), __fdiv_rn(bf16_hi(v.z), s),
+                       __fdiv_rn(bf16_lo(v.w), s), __fdiv_rn(bf16_hi(v.w), s));
+      qr[i] = q;
+    }
+    if (lane == 0) xs[r] = s;
+  }
+}
+
+cudaError_t launch_quant_rows(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,
+                              cudaStream_t s) {
+  if (M == 0) return cudaSuccess;
+  const int grid = static_cast<int>(std::min<int64_t>((M + 7) / 8, num_sms() * 8));
+  quant_row_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), M, K / 8,
+                                        reinterpret_cast<uint2*>(xq), xs);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_quant_g128(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,

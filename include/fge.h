@@ -52,7 +52,8 @@ typedef enum {
 
 typedef enum {
   FGE_SCALE_PER_TENSOR = 0,     /* one amax over the whole [M, K] tensor */
-  FGE_SCALE_PER_TOKEN_G128 = 1  /* one scale per (row, 128-element K group) */
+  FGE_SCALE_PER_TOKEN_G128 = 1, /* one scale per (row, 128-element K group) */
+  FGE_SCALE_PER_ROW = 2         /* one scale per row (token) over its K elements */
 } fge_scale_mode;
 
 typedef enum { FGE_DTYPE_BF16 = 0, FGE_DTYPE_F32 = 1 } fge_dtype;
@@ -76,7 +77,8 @@ typedef enum {
   FGE_OP_GROUPED_GEMM = 2,     /* args: unused */
   FGE_OP_LINEAR_W8A8 = 3,      /* args: (M, K) */
   FGE_OP_MOE_LAYER = 4,        /* args: (T, H, I, E, k) */
-  FGE_OP_DISPATCH_BASELINE = 5 /* args: (T, H, I, E, k) */
+  FGE_OP_DISPATCH_BASELINE = 5, /* args: (T, H, I, E, k) */
+  FGE_OP_LINEAR_W8A8_ROWS = 6   /* args: (M, K) */
 } fge_op;
 
 /* Library version (major*10000 + minor*100 + patch). */
@@ -104,9 +106,12 @@ fge_status fge_read_device_status(const void* workspace, fge_stream_t stream, in
  *   amax = max|x| over the group (G128) or the whole tensor (PER_TENSOR);
  *   s = amax / 448 (IEEE float division; s = 1 when amax = 0; s >= 2^-126);
  *   q = e4m3(x / s), round to nearest even, saturating at +-448.
- * x_bf16: [M, K] bf16.  xq: [M, K] e4m3 codes (out).  xs: [M, K/128] float (G128) or one
- * float (PER_TENSOR) (out).  PER_TENSOR needs a workspace of
- * fge_workspace_bytes(FGE_OP_QUANT_PER_TENSOR, M, K, ...); G128 takes none (may be NULL).
+ * PER_ROW takes the amax over each row's K elements (the row-wise activation scales that
+ * "feat(qwen4_exp) ..." measures against per-tensor, section "Limits").
+ * x_bf16: [M, K] bf16.  xq: [M, K] e4m3 codes (out).  xs: [M, K/128] float (G128), [M] float
+ * (PER_ROW) or one float (PER_TENSOR) (out).  PER_TENSOR needs a workspace of
+ * fge_workspace_bytes(FGE_OP_QUANT_PER_TENSOR, M, K, ...); G128 and PER_ROW take none (may
+ * be NULL).
  * M may be 0. */
 fge_status fge_fp8_quant_act(const void* x_bf16, int64_t M, int64_t K, fge_scale_mode mode,
                              uint8_t* xq, float* xs, void* workspace, size_t workspace_bytes,
@@ -191,6 +196,23 @@ fge_status fge_gemm_w8a8(const uint8_t* aq, const float* sa, int64_t M, int64_t 
 fge_status fge_linear_w8a8(const void* x_bf16, int64_t M, int64_t K, const uint8_t* wq,
                            const float* w_scale, int64_t N, void* y_bf16, void* workspace,
                            size_t workspace_bytes, fge_stream_t stream);
+
+/* gemm_w8a8_rows -- the one-group W8A8 GEMM with one activation scale per row instead of one
+ * per tensor (row-wise scales, "feat(qwen4_exp) ..." section "Limits"):
+ *   y[m, n] = (sa[m] * sw) * sum_k aq[m, k] * wq[n, k].
+ * aq: [M, K] e4m3; sa: [M] device floats; wq: [N, K] e4m3; sw: device float scalar;
+ * y: [M, N] in out_dtype.  Workspace: FGE_OP_GROUPED_GEMM. */
+fge_status fge_gemm_w8a8_rows(const uint8_t* aq, const float* sa, int64_t M, int64_t K,
+                              const uint8_t* wq, const float* sw, int64_t N, fge_dtype out_dtype,
+                              void* y, void* workspace, size_t workspace_bytes,
+                              fge_stream_t stream);
+
+/* linear_w8a8_rows -- the dense projection with row-wise activation scales in one call:
+ * per-row amax and e4m3 cast (FGE_SCALE_PER_ROW), then fge_gemm_w8a8_rows.  Arguments as
+ * fge_linear_w8a8.  Workspace: FGE_OP_LINEAR_W8A8_ROWS (quantized rows and their scales). */
+fge_status fge_linear_w8a8_rows(const void* x_bf16, int64_t M, int64_t K, const uint8_t* wq,
+                                const float* w_scale, int64_t N, void* y_bf16, void* workspace,
+                                size_t workspace_bytes, fge_stream_t stream);
 
 /* moe_layer_per_token_dispatch -- the baseline the grouped GEMM replaces ("FP8
  * grouped-expert prefill ..." section 1: one dispatch per routed token per layer): one CTA

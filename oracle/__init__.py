@@ -30,6 +30,7 @@ from .fp8 import (  # noqa: F401
     bf16_bits_to_f32,
     quant_act_g128,
     quant_act_per_tensor,
+    quant_act_per_row,
 )
 from .moe import (  # noqa: F401
     topk_gate,
@@ -42,5 +43,7 @@ from .moe import (  # noqa: F401
     linear_w8a8,
     dequant_int4_bank,
     moe_layer_int4_baseline,
+    linear_w8a8_rows_gemm,
+    linear_w8a8_rows,
 )
 from .stack import rmsnorm, router_logits, identity_attention, stacked_prefill  # noqa: F401

@@ -168,3 +168,20 @@ def quant_act_per_tensor(x_f32):
     s = _scale_from_amax(amax)
     q = e4m3_encode(x / s)
     return q, np.float32(s)
+
+
+def quant_act_per_row(x_f32):
+    """Dynamic activation quantization with one scale per row (token).
+
+    "feat(qwen4_exp): load-time per-tensor FP8 dense projections", section "Limits": the
+    row-wise alternative to one per-tensor scale, so that an outlier channel in one row no
+    longer sets the scale of every row.  Same scale rule and rounding as
+    ``quant_act_per_tensor``, with the amax taken over each row's K values.
+    Returns (codes uint8 [M, K], scales float32 [M]).
+    """
+    x = np.asarray(x_f32, dtype=np.float32)
+    m, k = x.shape
+    amax = np.max(np.abs(x), axis=1) if k else np.zeros(m, dtype=np.float32)
+    s = _scale_from_amax(amax)
+    q = e4m3_encode(x / s[:, None])
+    return q, s

@@ -12,6 +12,7 @@ from .fp8 import (
     e4m3_decode,
     int4_unpack,
     quant_act_g128,
+    quant_act_per_row,
     quant_act_per_tensor,
 )
 
@@ -235,3 +236,21 @@ def moe_layer_int4_baseline(logits, x_f32, k, w_gate_up, s_gate_up, w_down, s_do
         y = (g / (1.0 + np.exp(-g)) * u) @ wdn.T
         out[tok] += gates[tok, slot].astype(np.float64)[:, None] * y
     return _round_out(out, out_dtype), ids
+
+
+def linear_w8a8_rows_gemm(aq, sa_rows, wq, sw):
+    """Dense W8A8 GEMM with one activation scale per row: Y[m, n] = (sa[m] * sw) *
+    sum_k dec(Aq[m, k]) * dec(Wq[n, k]), in float64 ("feat(qwen4_exp) ...", section
+    "Limits": row-wise activation scales instead of the per-tensor one)."""
+    a = e4m3_decode(aq)
+    w = e4m3_decode(wq)
+    scale = np.asarray(sa_rows, dtype=np.float32).astype(np.float64) * float(np.float32(sw))
+    return scale[:, None] * (a @ w.T)
+
+
+def linear_w8a8_rows(x_f32, wq, sw, out_dtype="bf16"):
+    """Dense projection with row-wise activation scales: per-row quantization, then
+    ``linear_w8a8_rows_gemm``, rounded to ``out_dtype``.  Returns (y, xq, sa [M])."""
+    xq, sa = quant_act_per_row(x_f32)
+    y = linear_w8a8_rows_gemm(xq, sa, wq, sw)
+    return _round_out(y, out_dtype), xq, sa

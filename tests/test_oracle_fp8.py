@@ -200,3 +200,36 @@ def test_quant_error_bound():
     top = np.argmax(g, axis=2)
     qg = q.reshape(64, 4, 128)
     assert np.all(np.take_along_axis(qg, top[..., None], 2) & 0x7F == 0x7E)
+
+
+# --- per-row (row-wise) activation quant ---------------------------------------------------
+
+def test_per_row_equals_per_tensor_on_each_row():
+    # a row is a tensor of its own: the per-row mode must give, row by row, what the
+    # independent per-tensor function gives for that row alone
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((6, 384)) * np.exp(rng.uniform(-5, 5, (6, 1)))).astype(np.float32)
+    q, s = oracle.quant_act_per_row(x)
+    assert q.shape == x.shape and s.shape == (6,)
+    for i in range(6):
+        qt, st = oracle.quant_act_per_tensor(x[i:i + 1])
+        assert np.array_equal(q[i:i + 1], qt) and s[i] == st
+
+
+def test_per_row_equals_group_mode_when_k_is_128():
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((9, 128)).astype(np.float32)
+    qr, sr = oracle.quant_act_per_row(x)
+    qg, sg = oracle.quant_act_g128(x)
+    assert np.array_equal(qr, qg) and np.array_equal(sr, sg[:, 0])
+
+
+def test_per_row_zero_row_and_amax_code():
+    x = np.zeros((3, 256), dtype=np.float32)
+    x[1, 7] = -3.0                       # amax 3 -> s = 3/448; x/s = -448 -> code 0xFE
+    x[2] = np.linspace(-1.0, 2.0, 256, dtype=np.float32)  # amax 2 at the last element -> 0x7E
+    q, s = oracle.quant_act_per_row(x)
+    assert np.all(q[0] == 0) and s[0] == np.float32(1.0)
+    assert s[1] == np.float32(3.0) / np.float32(448.0) and q[1, 7] == 0xFE
+    assert np.count_nonzero(q[1]) == 1
+    assert q[2, 255] == 0x7E

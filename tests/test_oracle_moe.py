@@ -296,3 +296,46 @@ def test_int4_baseline_single_expert_closed_form():
     ref = hh @ (q_dn[0] * float(np.float32(0.02))).T
     assert np.all(ids == 0)
     assert np.allclose(out, ref.astype(np.float32), rtol=1e-6)
+
+
+# --- W8A8 with row-wise activation scales ----------------------------------------------------
+
+def test_w8a8_rows_equal_scales_is_per_tensor():
+    rng = np.random.default_rng(31)
+    aq = oracle.e4m3_encode(rng.standard_normal((9, 256)).astype(np.float32) * 40)
+    wq = oracle.e4m3_encode(rng.standard_normal((5, 256)).astype(np.float32) * 40)
+    sa, sw = np.float32(0.0173), np.float32(0.00091)
+    got = oracle.linear_w8a8_rows_gemm(aq, np.full(9, sa, dtype=np.float32), wq, sw)
+    ref = oracle.linear_w8a8_gemm(aq, sa, wq, sw)
+    assert np.allclose(got, ref, rtol=1e-15, atol=0)
+
+
+def test_w8a8_rows_exact_power_of_two_case():
+    # small integers are exact e4m3 codes and power-of-two scales keep every product exact,
+    # so the result is the integer dot product times 2^e (Python ints)
+    rng = np.random.default_rng(32)
+    a = rng.integers(-12, 13, size=(4, 128))
+    w = rng.integers(-12, 13, size=(3, 128))
+    sa = np.array([2.0 ** -3, 2.0 ** 2, 1.0, 2.0 ** -9], dtype=np.float32)
+    got = oracle.linear_w8a8_rows_gemm(oracle.e4m3_encode(a.astype(np.float32)), sa,
+                                       oracle.e4m3_encode(w.astype(np.float32)), np.float32(2.0 ** -5))
+    for m in range(4):
+        for n in range(3):
+            dot = sum(int(a[m, k]) * int(w[n, k]) for k in range(128))
+            assert got[m, n] == dot * float(sa[m]) * 2.0 ** -5
+
+
+def test_w8a8_rows_matches_naive_loop():
+    rng = np.random.default_rng(33)
+    x = rng.standard_normal((3, 256)).astype(np.float32)
+    x[1] *= 50.0
+    wq = oracle.e4m3_encode(rng.standard_normal((4, 256)).astype(np.float32) * 20)
+    y, xq, sa = oracle.linear_w8a8_rows(x, wq, np.float32(0.01), out_dtype="f32")
+    table = oracle.e4m3_decode_table()
+    for m in range(3):
+        for n in range(4):
+            acc = 0.0
+            for k in range(256):
+                acc += float(table[xq[m, k]]) * float(table[wq[n, k]])
+            ref = np.float32(acc * float(sa[m]) * float(np.float32(0.01)))
+            assert y[m, n] == ref

@@ -140,6 +140,26 @@ def dense_activations(m, k, seed=0):
     return to_bf16(rng.standard_normal((m, k), dtype=np.float32))
 
 
+def dense_activations_outliers(m, k, seed=0, frac=0.01, factor=20.0):
+    """bf16 activations ~N(0, 1), [M, K], with floor(frac * K) seeded channels (columns)
+    multiplied by `factor` (the outlier-channel recipe of the large skewed MoE workload)."""
+    rng = np.random.default_rng(_seq(seed, "dense_x_outliers", m, k))
+    x = rng.standard_normal((m, k), dtype=np.float32)
+    cols = rng.choice(k, size=int(frac * k), replace=False)
+    x[:, cols] *= np.float32(factor)
+    return to_bf16(x)
+
+
+def dense_activations_outlier_rows(m, k, seed=0, frac=0.01, factor=20.0):
+    """bf16 activations ~N(0, 1), [M, K], with max(1, floor(frac * M)) seeded rows (tokens)
+    multiplied by `factor`."""
+    rng = np.random.default_rng(_seq(seed, "dense_x_outlier_rows", m, k))
+    x = rng.standard_normal((m, k), dtype=np.float32)
+    rows = rng.choice(m, size=max(1, int(frac * m)), replace=False)
+    x[rows] *= np.float32(factor)
+    return to_bf16(x)
+
+
 def dense_inputs(M, seed=0, N=None, K=None):
     n = N or DENSE_SHAPE["N"]
     kk = K or DENSE_SHAPE["K"]
