@@ -44,6 +44,8 @@ SIGNATURES = {
     "fge_w4_prepack": [_P, _P, _I, _I64, _I64, _I, _I, _P, _P, _P],
     "fge_grouped_gemm_w4a8": [_P, _P, _P, _I64, _P, _P, _I, _I64, _I64, _I, _I, _I, _P, _P, _P,
                               _SZ, _P],
+    "fge_grouped_gemm_w4a8_gather": [_P, _P, _I64, _P, _P, _I64, _P, _P, _I, _I64, _I64, _I,
+                                     _I, _I, _P, _P, _P, _SZ, _P],
     "fge_swiglu_quant": [_P, _I64, _I64, _P, _P, _P],
     "fge_moe_combine": [_P, _I, _P, _P, _I64, _I, _I64, _I, _P, _P],
     "fge_gemm_w8a8": [_P, _P, _I64, _I64, _P, _P, _I64, _I, _P, _P, _SZ, _P],
@@ -176,7 +178,9 @@ def moe_topk_gate(logits, k):
     return ids, gates
 
 
-def moe_permute(ids, num_experts, xq, xs):
+def moe_permute(ids, num_experts, xq, xs, index_only=False):
+    """Expert-contiguous routed rows.  index_only: offsets, row_token and token_row only (no
+    row copy; xq/xs give the sizes), for grouped_gemm_w4a8_gather."""
     _need(ids, torch.int32, "ids")
     _need(xq, torch.uint8, "xq")
     _need(xs, torch.float32, "xs")
@@ -189,14 +193,16 @@ def moe_permute(ids, num_experts, xq, xs):
         offsets=torch.empty(num_experts + 1, dtype=torch.int32, device=dev),
         row_token=torch.empty(r, dtype=torch.int32, device=dev),
         token_row=torch.empty((t, k), dtype=torch.int32, device=dev),
-        aq=torch.empty((r, h), dtype=torch.uint8, device=dev),
-        as_=torch.empty((r, h // 128), dtype=torch.float32, device=dev),
     )
+    if not index_only:
+        out["aq"] = torch.empty((r, h), dtype=torch.uint8, device=dev)
+        out["as_"] = torch.empty((r, h // 128), dtype=torch.float32, device=dev)
     ws = new_workspace(workspace_bytes(OP_PERMUTE, t, h, 0, num_experts, k), dev)
     _check(lib().fge_moe_permute(_ptr(ids), t, k, num_experts, _ptr(xq), _ptr(xs), h,
                                  _ptr(out["offsets"]), _ptr(out["row_token"]),
-                                 _ptr(out["token_row"]), _ptr(out["aq"]), _ptr(out["as_"]),
-                                 _ptr(ws), ws.numel(), _stream(ids)), "fge_moe_permute")
+                                 _ptr(out["token_row"]), _ptr(out.get("aq")),
+                                 _ptr(out.get("as_")), _ptr(ws), ws.numel(), _stream(ids)),
+           "fge_moe_permute")
     return out
 
 
@@ -241,6 +247,38 @@ def grouped_gemm_w4a8(aq, as_, offsets, w_dev, s_dev, fmt=W4_SUBNORMAL, epilogue
                                        _ptr(s_dev), e, n, k, fmt, epi, od, _ptr(out),
                                        _ptr(scales), _ptr(ws), ws.numel(), _stream(aq)),
            "fge_grouped_gemm_w4a8")
+    return (out, scales) if epilogue == "swiglu" else out
+
+
+def grouped_gemm_w4a8_gather(xq, xs, row_token, offsets, w_dev, s_dev, fmt=W4_SUBNORMAL,
+                             epilogue="store", out_dtype=torch.float32, workspace=None):
+    """grouped_gemm_w4a8 with the A rows gathered from token-ordered xq [T, K] / xs [T, K/128]
+    by row_token [R] (TMA row gathers in the GEMM; no permuted copy)."""
+    _need(xq, torch.uint8, "xq")
+    _need(xs, torch.float32, "xs")
+    _need(row_token, torch.int32, "row_token")
+    _need(offsets, torch.int32, "offsets")
+    _ensure_init(xq.device)
+    t, k = xq.shape
+    r = row_token.shape[0]
+    e, n, _ = w_dev.shape
+    dev = xq.device
+    ws = workspace if workspace is not None else new_workspace(
+        workspace_bytes(OP_GROUPED_GEMM), dev)
+    if epilogue == "swiglu":
+        out = torch.zeros((r, n // 2), dtype=torch.uint8, device=dev)
+        scales = torch.zeros((r, n // 256), dtype=torch.float32, device=dev)
+        epi, od = EPI_SWIGLU_REQUANT, DTYPE_BF16
+    else:
+        out = torch.zeros((r, n), dtype=out_dtype, device=dev)
+        scales = None
+        epi = EPI_STORE
+        od = DTYPE_F32 if out_dtype == torch.float32 else DTYPE_BF16
+    _check(lib().fge_grouped_gemm_w4a8_gather(_ptr(xq), _ptr(xs), t, _ptr(row_token),
+                                              _ptr(offsets), r, _ptr(w_dev), _ptr(s_dev), e, n,
+                                              k, fmt, epi, od, _ptr(out), _ptr(scales), _ptr(ws),
+                                              ws.numel(), _stream(xq)),
+           "fge_grouped_gemm_w4a8_gather")
     return (out, scales) if epilogue == "swiglu" else out
 
 

@@ -186,11 +186,14 @@ fge_status fge_moe_permute(const int32_t* ids, int64_t T, int k, int E, const ui
                            int32_t* token_row, uint8_t* aq, float* as, void* ws,
                            size_t ws_bytes, fge_stream_t stream) {
   FGE_CHECK(cur_device_ok());
-  FGE_REQUIRE(ids && xq && xs && offsets && row_token && token_row && aq && as && ws,
+  // aq and as both null: index-only (offsets, row_token, token_row), no row copy
+  FGE_REQUIRE(ids && offsets && row_token && token_row && ws && ((aq == nullptr) == (as == nullptr)),
               FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(aq == nullptr || (xq && xs), FGE_ERR_INVALID_ARG);
   FGE_REQUIRE(T >= 0 && E >= 1 && E <= 1024 && k >= 1 && k <= E && k <= 32, FGE_ERR_BAD_SHAPE);
   FGE_REQUIRE(H > 0 && H % 128 == 0 && T * k < (1LL << 31), FGE_ERR_BAD_SHAPE);
-  FGE_REQUIRE(al16(xq) && al16(aq) && al16(ws), FGE_ERR_MISALIGNED);
+  FGE_REQUIRE(aq == nullptr || (al16(xq) && al16(aq)), FGE_ERR_MISALIGNED);
+  FGE_REQUIRE(al16(ws), FGE_ERR_MISALIGNED);
   FGE_REQUIRE(ws_bytes >= fge_workspace_bytes(FGE_OP_PERMUTE, T, H, 0, E, k),
               FGE_ERR_WORKSPACE_TOO_SMALL);
   return from_cuda(launch_permute(ids, T, k, E, xq, xs, H, offsets, row_token, token_row, aq, as,
@@ -215,7 +218,8 @@ static fge_status grouped_common(const uint8_t* aq, const float* as, const int32
                                  int64_t K, int format, int per_tensor, const float* sa_t,
                                  int epilogue, void* out, float* out_scales, void* ws,
                                  size_t ws_bytes, fge_stream_t stream,
-                                 const float* sa_rows = nullptr) {
+                                 const float* sa_rows = nullptr,
+                                 const int32_t* row_token = nullptr, int64_t rows_a = 0) {
   FGE_REQUIRE(R >= 0 && R < (1LL << 31) && N > 0 && N % 128 == 0 && N < (1LL << 24) && K > 0 &&
                   K % 128 == 0 && K < (1LL << 24),
               FGE_ERR_BAD_SHAPE);
@@ -230,6 +234,8 @@ static fge_status grouped_common(const uint8_t* aq, const float* as, const int32
   a.as = as;
   a.sa_tensor = sa_t;
   a.sa_rows = sa_rows;
+  a.row_token = row_token;
+  a.rows_a = rows_a;
   a.offsets = offsets;
   a.w = w;
   a.sw = sw;
@@ -270,6 +276,31 @@ fge_status fge_grouped_gemm_w4a8(const uint8_t* aq, const float* as, const int32
   }
   return grouped_common(aq, as, offsets, R, w_dev, w_scale_dev, E, N, K, format, 0, nullptr, epi,
                         out, out_scales, ws, ws_bytes, stream);
+}
+
+fge_status fge_grouped_gemm_w4a8_gather(const uint8_t* xq, const float* xs, int64_t T,
+                                        const int32_t* row_token, const int32_t* offsets,
+                                        int64_t R, const uint8_t* w_dev,
+                                        const float* w_scale_dev, int E, int64_t N, int64_t K,
+                                        fge_w4_format format, fge_epilogue epilogue,
+                                        fge_dtype out_dtype, void* out, float* out_scales,
+                                        void* ws, size_t ws_bytes, fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(xs && offsets && row_token, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(T > 0 && T < (1LL << 31), FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(format == FGE_W4_LUT || format == FGE_W4_SUBNORMAL, FGE_ERR_INVALID_ARG);
+  int epi;
+  if (epilogue == FGE_EPI_SWIGLU_REQUANT) {
+    FGE_REQUIRE(out_scales, FGE_ERR_INVALID_ARG);
+    FGE_REQUIRE(N % 256 == 0, FGE_ERR_BAD_SHAPE);
+    epi = 2;
+  } else {
+    FGE_REQUIRE(epilogue == FGE_EPI_STORE, FGE_ERR_INVALID_ARG);
+    FGE_REQUIRE(out_dtype == FGE_DTYPE_BF16 || out_dtype == FGE_DTYPE_F32, FGE_ERR_INVALID_ARG);
+    epi = out_dtype == FGE_DTYPE_F32 ? 0 : 1;
+  }
+  return grouped_common(xq, xs, offsets, R, w_dev, w_scale_dev, E, N, K, format, 0, nullptr, epi,
+                        out, out_scales, ws, ws_bytes, stream, nullptr, row_token, T);
 }
 
 fge_status fge_swiglu_quant(const float* c, int64_t R, int64_t I, uint8_t* hq, float* hs,
@@ -370,6 +401,9 @@ fge_status fge_moe_layer_forward(const float* logits, const void* x, int64_t T, 
   const int out_f32 = out_dtype == FGE_DTYPE_F32;
   FGE_CHECK(from_cuda(launch_topk_gate(logits, T, E, k, w.ids, w.gates, stream)));
   FGE_CHECK(from_cuda(launch_quant_g128(static_cast<const uint16_t*>(x), T, H, w.xq, w.xs, stream)));
+  // The permuted copy of the activation rows plus a tiled A load beats gathering the rows
+  // in the GEMM (fge_grouped_gemm_w4a8_gather): 32 four-row TMA gathers per K group cost
+  // more than the copy kernel saves.
   FGE_CHECK(from_cuda(launch_permute(w.ids, T, k, E, w.xq, w.xs, H, w.offsets, w.row_token,
                                      w.token_row, w.aq, w.as, w.perm, stream)));
   FGE_CHECK(grouped_common(w.aq, w.as, w.offsets, R, w_gu, s_gu, E, 2 * I, H, format, 0, nullptr,

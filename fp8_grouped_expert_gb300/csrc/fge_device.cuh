@@ -93,6 +93,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
+// Row gather: 4 rows (y0..y3) of a 2-D tensor, each the map's one-row box at column x,
+// land as 4 consecutive box rows at smem_dst (the map's swizzle applies as for a 4-row box).
+__device__ __forceinline__ void tma_gather4_2d(uint32_t smem_dst, const CUtensorMap* map,
+                                               uint32_t bar, int32_t x, int4 y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y.x), "r"(y.y), "r"(y.z),
+      "r"(y.w)
+      : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

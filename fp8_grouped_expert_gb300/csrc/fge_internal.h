@@ -59,6 +59,9 @@ struct GroupedGemmArgs {
   const float* sa_tensor;   // device scalar (per-tensor mode)
   const float* sa_rows;     // [R] per-row activation scales (per-tensor mode), or null
   const int32_t* offsets;   // [E+1]
+  const int32_t* row_token; // gather mode: routed row r reads A row row_token[r] of aq
+                            // ([rows_a, K], token order) and its scales; else null
+  int64_t rows_a;           // gather mode: rows of aq / as
   const uint8_t* w;         // int4 bank [E, N, K/2] (prepacked) or e4m3 [N, K]
   const float* sw;          // [E, K/128, N] prepacked group scales, or device scalar
   int E;

@@ -32,6 +32,7 @@ struct GemmParams {
   const float* sa_rows;    // per-row activation scales [rows] (one-group path), or null
   const float* sw_tensor;  // per-tensor weight scale (device scalar)
   const int32_t* offsets;  // [E+1]
+  const int32_t* row_token;  // gather mode: A row of routed row r is row_token[r], else null
   void* out;
   float* out_scales;
   int32_t* status;
@@ -81,7 +82,8 @@ struct Cfg {
   static constexpr int kOffOffs = align16(kOffMisc + 16);
   static constexpr int kOffMtp = kOffOffs + (kMaxExperts + 1) * 4;
   static constexpr int kOffRed = align16(kOffMtp + (kMaxExperts + 1) * 4);
-  static constexpr int kSmemBytes = kOffRed + 2 * 2 * 128 * 4 + 1024;  // + alignment slack
+  static constexpr int kOffRT = align16(kOffRed + 2 * 2 * 128 * 4);  // gather: tile row ids
+  static constexpr int kSmemBytes = kOffRT + 128 * 4 + 1024;  // + alignment slack
   static_assert(kNS >= 2, "pipeline needs at least two stages");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
@@ -339,53 +341,83 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
     }
   } else if (warp < 8) {
     if constexpr (C::kGroupScale) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsCtrl));
-    if (warp == kProducerWarp && lane == 0) {
+    if (warp == kProducerWarp) {
       // ---------------------------------------------------------------- TMA producer
-      tma_prefetch_desc(&tmA);
-      tma_prefetch_desc(&tmB);
+      // Lane 0 waits for free stages and issues the B tile, the weight scales and a plain A
+      // tile.  In gather mode the warp first stages the tile's 128 source row ids (rows past
+      // the expert's last repeat its last row; their results are never stored) and each of
+      // the 32 lanes then issues one four-row gather of the A tile per K group.
+      int32_t* s_rt = reinterpret_cast<int32_t*>(smem + C::kOffRT);
+      const bool gather = p.row_token != nullptr;
+      if (lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+      }
       uint32_t it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
         const TileInfo ti = decode_tile(t, nt_count, BN, s_off, s_mtp, E);
+        if (gather) {
+          for (int i = lane; i < 128; i += 32)
+            s_rt[i] = __ldg(p.row_token + ti.row0 + (i < ti.rows ? i : ti.rows - 1));
+          __syncwarp();
+        }
         for (int g = 0; g < G; ++g, ++it) {
           const uint32_t s = it % C::kNS;
-          if (!mbar_wait(bar_empty + 8 * s, ((it / C::kNS) & 1) ^ 1, s_abort, p.status)) {
-            ok = false;
-            break;
-          }
-          if constexpr (C::kGroupScale) {
-            // the tile's weight scales of this K group: BN contiguous floats
-            const uint32_t w = it % C::kNSW;
-            if (!mbar_wait(bar_swempty + 8 * w, ((it / C::kNSW) & 1) ^ 1, s_abort, p.status)) {
+          if (lane == 0) {
+            if (!mbar_wait(bar_empty + 8 * s, ((it / C::kNS) & 1) ^ 1, s_abort, p.status)) {
               ok = false;
-              break;
+            } else {
+              if constexpr (C::kGroupScale) {
+                // the tile's weight scales of this K group: BN contiguous floats
+                const uint32_t w = it % C::kNSW;
+                if (!mbar_wait(bar_swempty + 8 * w, ((it / C::kNSW) & 1) ^ 1, s_abort,
+                               p.status)) {
+                  ok = false;
+                } else {
+                  mbar_arrive_expect_tx(bar_swfull + 8 * w, C::kSWBytes);
+                  bulk_load(smem_u32(smem + C::kOffSW + w * C::kSWBytes),
+                            p.sw + (static_cast<size_t>(ti.e) * G + g) * p.N + ti.n0,
+                            C::kSWBytes, bar_swfull + 8 * w);
+                }
+              }
+              if (ok) {
+                mbar_arrive_expect_tx(bar_full + 8 * s, C::kStageBytes);
+                if (!gather)
+                  tma_load_2d(smem_u32(smem + C::kOffA + s * C::kABytes), &tmA, bar_full + 8 * s,
+                              g * 128, ti.row0);
+                if constexpr (C::kInt4) {
+                  tma_load_2d(smem_u32(smem + C::kOffB + s * C::kBLoadBytes), &tmB,
+                              bar_full + 8 * s, g * 64, ti.e * p.N + ti.n0);
+                } else {
+                  tma_load_2d(smem_u32(smem + C::kOffB + s * C::kBLoadBytes), &tmB,
+                              bar_full + 8 * s, g * 128, ti.n0);
+                }
+              }
             }
-            mbar_arrive_expect_tx(bar_swfull + 8 * w, C::kSWBytes);
-            bulk_load(smem_u32(smem + C::kOffSW + w * C::kSWBytes),
-                      p.sw + (static_cast<size_t>(ti.e) * G + g) * p.N + ti.n0, C::kSWBytes,
-                      bar_swfull + 8 * w);
           }
-          mbar_arrive_expect_tx(bar_full + 8 * s, C::kStageBytes);
-          tma_load_2d(smem_u32(smem + C::kOffA + s * C::kABytes), &tmA, bar_full + 8 * s,
-                      g * 128, ti.row0);
-          if constexpr (C::kInt4) {
-            tma_load_2d(smem_u32(smem + C::kOffB + s * C::kBLoadBytes), &tmB, bar_full + 8 * s,
-                        g * 64, ti.e * p.N + ti.n0);
-          } else {
-            tma_load_2d(smem_u32(smem + C::kOffB + s * C::kBLoadBytes), &tmB, bar_full + 8 * s,
-                        g * 128, ti.n0);
-          }
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;  // before ++it: the drain below counts issued stages only
+          // gather mode: each lane copies 4 of the 128 rows (its stage slot is free: lane 0
+          // waited for it above)
+          if (gather)
+            tma_gather4_2d(smem_u32(smem + C::kOffA + s * C::kABytes) + lane * 512, &tmA,
+                           bar_full + 8 * s, g * 128,
+                           *reinterpret_cast<const int4*>(s_rt + 4 * lane));
         }
+        __syncwarp();  // every lane is done with s_rt before the next tile rewrites it
       }
-      // drain: every issued stage must have landed before the CTA can exit
-      const uint32_t issued = it;
-      const uint32_t first = issued > static_cast<uint32_t>(C::kNS) ? issued - C::kNS : 0;
-      for (uint32_t i = first; i < issued; ++i)
-        mbar_wait_drain(bar_full + 8 * (i % C::kNS), (i / C::kNS) & 1);
-      if constexpr (C::kGroupScale) {
-        const uint32_t first_w = issued > static_cast<uint32_t>(C::kNSW) ? issued - C::kNSW : 0;
-        for (uint32_t i = first_w; i < issued; ++i)
-          mbar_wait_drain(bar_swfull + 8 * (i % C::kNSW), (i / C::kNSW) & 1);
+      if (lane == 0) {
+        // drain: every issued stage must have landed before the CTA can exit
+        const uint32_t issued = it;
+        const uint32_t first = issued > static_cast<uint32_t>(C::kNS) ? issued - C::kNS : 0;
+        for (uint32_t i = first; i < issued; ++i)
+          mbar_wait_drain(bar_full + 8 * (i % C::kNS), (i / C::kNS) & 1);
+        if constexpr (C::kGroupScale) {
+          const uint32_t first_w = issued > static_cast<uint32_t>(C::kNSW) ? issued - C::kNSW : 0;
+          for (uint32_t i = first_w; i < issued; ++i)
+            mbar_wait_drain(bar_swfull + 8 * (i % C::kNSW), (i / C::kNSW) & 1);
+        }
       }
     } else if (warp == kMmaWarp && lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
@@ -486,7 +518,10 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc2[i] = 0;
         // activation scales run two groups ahead of their use (global-load latency)
-        const float* as_row = p.as + static_cast<size_t>(valid ? row : 0) * G;
+        // gather mode: the scales of routed row r are those of its source row row_token[r]
+        const int src_row = p.row_token ? __ldg(p.row_token + (valid ? row : ti.row0))
+                                        : (valid ? row : 0);
+        const float* as_row = p.as + static_cast<size_t>(src_row) * G;
         float sa0 = valid ? __ldg(as_row) : 0.0f;
         float sa1 = (valid && G > 1) ? __ldg(as_row + 1) : 0.0f;
         for (int g = 0; g < G; ++g) {
@@ -720,7 +755,10 @@ static cudaError_t run(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st)
     }
   }
   CUtensorMap tmA, tmB;
-  if (!make_map_u8(&tmA, a.aq, a.K, a.R, 128, 128, true)) {
+  // gather mode: A is the token-ordered [rows_a, K] tensor read one row per box (4 per copy)
+  const bool okA = a.row_token ? make_map_u8(&tmA, a.aq, a.K, a.rows_a, 128, 1, true)
+                               : make_map_u8(&tmA, a.aq, a.K, a.R, 128, 128, true);
+  if (!okA) {
     *st = FGE_ERR_CUDA;
     return cudaSuccess;
   }
@@ -740,6 +778,7 @@ static cudaError_t run(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st)
   p.sa_rows = a.sa_rows;
   p.sw_tensor = a.per_tensor ? a.sw : nullptr;
   p.offsets = a.offsets;
+  p.row_token = a.row_token;
   p.out = a.out;
   p.out_scales = a.out_scales;
   p.status = a.status;

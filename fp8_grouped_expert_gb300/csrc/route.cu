@@ -233,6 +233,7 @@ cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, const ui
                                                                             row_token, token_row);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (aq == nullptr) return cudaSuccess;  // index-only: the GEMM gathers rows by row_token
   const int grid = static_cast<int>(std::min<int64_t>((T + 7) / 8, num_sms() * 8));
   permute_copy_kernel<<<grid, 256, 0, s>>>(xq, xs, T, k, H, token_row, aq, as);
   return cudaGetLastError();

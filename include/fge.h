@@ -132,7 +132,9 @@ fge_status fge_moe_topk_gate(const float* logits, int64_t T, int E, int k, int32
  * token, slot), then a copy of each token's e4m3 row and group scales to its k rows.
  * ids: [T, k] int32 in [0, E) (distinct within a row).  xq: [T, H] codes; xs: [T, H/128].
  * offsets: [E+1] (out); row_token: [T*k] (out); token_row: [T, k] (out);
- * aq: [T*k, H] (out); as: [T*k, H/128] (out).  Workspace: FGE_OP_PERMUTE. */
+ * aq: [T*k, H] (out); as: [T*k, H/128] (out).  With aq and as both NULL the call is
+ * index-only (offsets, row_token and token_row; xq and xs may then be NULL too), for
+ * fge_grouped_gemm_w4a8_gather.  Workspace: FGE_OP_PERMUTE. */
 fge_status fge_moe_permute(const int32_t* ids, int64_t T, int k, int E, const uint8_t* xq,
                            const float* xs, int64_t H, int32_t* offsets, int32_t* row_token,
                            int32_t* token_row, uint8_t* aq, float* as, void* workspace,
@@ -165,6 +167,21 @@ fge_status fge_grouped_gemm_w4a8(const uint8_t* aq, const float* as, const int32
                                  fge_epilogue epilogue, fge_dtype out_dtype, void* out,
                                  float* out_scales, void* workspace, size_t workspace_bytes,
                                  fge_stream_t stream);
+
+/* grouped_gemm_w4a8_gather -- the same GEMM with the permutation folded into the A load: the
+ * A rows are gathered from the token-ordered activations by TMA row gathers (4 rows a copy)
+ * instead of being read from a permuted copy, so the permute's row copy disappears.
+ * Routed row r uses row row_token[r] of xq [T, K] and of xs [T, K/128] (row_token: [R] from
+ * fge_moe_permute, values in [0, T)).  Other arguments and the output as
+ * fge_grouped_gemm_w4a8 (out rows stay in routed order). */
+fge_status fge_grouped_gemm_w4a8_gather(const uint8_t* xq, const float* xs, int64_t T,
+                                        const int32_t* row_token, const int32_t* offsets,
+                                        int64_t R, const uint8_t* w_dev,
+                                        const float* w_scale_dev, int E, int64_t N, int64_t K,
+                                        fge_w4_format format, fge_epilogue epilogue,
+                                        fge_dtype out_dtype, void* out, float* out_scales,
+                                        void* workspace, size_t workspace_bytes,
+                                        fge_stream_t stream);
 
 /* swiglu_quant -- unfused SwiGLU + requant (parity/ablation of the fused epilogue):
  * h = silu(c[:, i]) * c[:, I + i], silu(g) = g / (1 + exp(-g)), then e4m3 per (row, 128

@@ -140,3 +140,40 @@ def test_gemm_w8a8_exact(fge):
                       out_dtype=torch.float32)
     ref = oracle.linear_w8a8_gemm(aq, sa, wq, sw)
     assert np.array_equal(host(y).astype(np.float64), ref)
+
+
+# ------------------------------------------------------------------------ gathered A rows
+@pytest.mark.parametrize("epi", ["store", "swiglu"])
+@pytest.mark.parametrize("t,e,k,h,n", [(64, 8, 2, 256, 512), (300, 16, 4, 1024, 768),
+                                       (1000, 64, 8, 2048, 1536)])
+def test_gather_equals_permuted_copy(fge, epi, t, e, k, h, n):
+    """The GEMM that gathers its A rows by row_token from the token-ordered activations gives
+    exactly what the GEMM on the permuted copy gives (same operands, same arithmetic), with
+    skewed routing (some experts empty, ragged tails)."""
+    rng = np.random.default_rng(t + h)
+    lg = (rng.standard_normal((t, e)) - 1.1 * np.log(np.arange(1, e + 1))).astype(np.float32)
+    x = rng.standard_normal((t, h)).astype(np.float32)
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)
+    xq, xs = fge.fp8_quant_act(bf16_dev(bits), "g128")
+    ids, _ = fge.moe_topk_gate(to_dev(lg), k)
+    full = fge.moe_permute(ids, e, xq, xs)
+    idx = fge.moe_permute(ids, e, xq, xs, index_only=True)
+    for key in ("offsets", "row_token", "token_row"):
+        assert torch.equal(full[key], idx[key])
+    assert set(idx) == {"offsets", "row_token", "token_row"}
+    wp = pack_int4(rng.integers(-8, 8, size=(e, n, h)))
+    ws = rng.uniform(0.002, 0.02, size=(e, n, h // 128)).astype(np.float32)
+    wd, sd = _prepack(fge, wp, ws, "subnormal", interleave=(epi == "swiglu"))
+    a = fge.grouped_gemm_w4a8(full["aq"], full["as_"], full["offsets"], wd, sd, epilogue=epi)
+    b = fge.grouped_gemm_w4a8_gather(xq, xs, idx["row_token"], idx["offsets"], wd, sd,
+                                     epilogue=epi)
+    if epi == "swiglu":
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    else:
+        assert torch.equal(a, b)
+    # and against the oracle on the same quantized operands
+    if epi == "store" and t <= 300:
+        p = {kk: host(full[kk]) for kk in ("aq", "as_", "offsets")}
+        ref = oracle.grouped_gemm_w4a8(p["aq"], p["as_"], p["offsets"], wp, ws)
+        absref = abs_grouped(p["aq"], p["as_"], p["offsets"], wp, ws)
+        check_gemm(host(b), ref, absref, False)
