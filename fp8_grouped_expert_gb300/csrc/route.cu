@@ -110,10 +110,16 @@ __global__ void permute_scan_kernel(int32_t* __restrict__ chunk_counts, int64_t 
   const int e = threadIdx.x;
   int run = 0;
   if (e < E) {
-    for (int64_t c = 0; c < chunks; ++c) {
-      const int cnt = chunk_counts[c * E + e];
-      chunk_counts[c * E + e] = run;
-      run += cnt;
+    // 8 independent loads in flight per step instead of one dependent load per chunk
+    for (int64_t c0 = 0; c0 < chunks; c0 += 8) {
+      int cnt[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) cnt[j] = c0 + j < chunks ? chunk_counts[(c0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (c0 + j < chunks) chunk_counts[(c0 + j) * E + e] = run;
+        run += cnt[j];
+      }
     }
   }
   // block-wide exclusive scan of the per-expert totals
@@ -143,35 +149,69 @@ __global__ void permute_scan_kernel(int32_t* __restrict__ chunk_counts, int64_t 
   if (e == E - 1) offsets[E] = excl + run;
   __syncthreads();
   if (e < E) {
+#pragma unroll 8
     for (int64_t c = 0; c < chunks; ++c) chunk_counts[c * E + e] += totals[e];
   }
 }
 
-// (3) stable rank: one warp walks its chunk in (token, slot) order.  Lanes hold
-// consecutive entries; a token's k experts are distinct, so lanes sharing an expert
-// belong to different tokens and their lane order is the token order.
+// (3) stable rank.  A block of kRankWarps warps takes one chunk; warp w owns a contiguous
+// slice of its tokens.  Pass 1: each warp counts its slice per expert.  Then every warp's
+// base per expert is the chunk's base plus the counts of the slices before it.  Pass 2:
+// each warp walks its slice in (token, slot) order.  Lanes hold consecutive entries; a
+// token's k experts are distinct, so lanes sharing an expert belong to different tokens and
+// their lane order is the token order.  The result equals a serial walk of the chunk.
+constexpr int kRankWarps = 4;
+
 __global__ void permute_rank_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int E,
                                     const int32_t* __restrict__ chunk_base,
                                     int32_t* __restrict__ row_token,
                                     int32_t* __restrict__ token_row) {
-  extern __shared__ int ctr[];
-  const int lane = threadIdx.x;  // one warp per block
+  extern __shared__ int sm[];
+  int* cnt = sm;                          // [kRankWarps][E]: slice counts, then slice bases
+  int* sid = sm + kRankWarps * E;         // the chunk's ids
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t chunk = blockIdx.x;
-  for (int e = lane; e < E; e += 32) ctr[e] = chunk_base[chunk * E + e];
-  __syncwarp();
   const int64_t t0 = chunk * kChunkTokens;
-  const int64_t n = (T - t0 < kChunkTokens ? T - t0 : static_cast<int64_t>(kChunkTokens)) * k;
+  const int64_t nt = T - t0 < kChunkTokens ? T - t0 : static_cast<int64_t>(kChunkTokens);
+  const int64_t n = nt * k;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) sid[i] = ids[t0 * k + i];
+  for (int i = threadIdx.x; i < kRankWarps * E; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  // this warp's slice: tokens [w * tps, (w + 1) * tps) of the chunk
+  const int64_t tps = (kChunkTokens + kRankWarps - 1) / kRankWarps;
+  const int64_t lo = (w * tps < nt ? w * tps : nt) * k;
+  const int64_t hi = ((w + 1) * tps < nt ? (w + 1) * tps : nt) * k;
   const int per = (32 / k) * k;  // lanes used per step: whole tokens only
   const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int64_t base = 0; base < n; base += per) {
+  int* my = cnt + w * E;
+  for (int64_t base = lo; base < hi; base += per) {       // pass 1: counts
     const int64_t i = base + lane;
-    const bool active = lane < per && i < n;
-    const int e = active ? ids[t0 * k + i] : -1 - lane;
+    const bool active = lane < per && i < hi;
+    const int e = active ? sid[i] : -1 - lane;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    if (active && (peers >> lane) == 1u) my[e] += __popc(peers);  // highest lane of the group
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {     // slice bases
+    int run = chunk_base[chunk * E + e];
+#pragma unroll
+    for (int ww = 0; ww < kRankWarps; ++ww) {
+      const int c = cnt[ww * E + e];
+      cnt[ww * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int64_t base = lo; base < hi; base += per) {       // pass 2: ranks
+    const int64_t i = base + lane;
+    const bool active = lane < per && i < hi;
+    const int e = active ? sid[i] : -1 - lane;
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
     int r = 0;
-    if (active) r = ctr[e] + __popc(peers & lt_mask);
+    if (active) r = my[e] + __popc(peers & lt_mask);
     __syncwarp();
-    if (active && (peers >> lane) == 1u) ctr[e] += __popc(peers);  // highest lane of the group
+    if (active && (peers >> lane) == 1u) my[e] += __popc(peers);
     __syncwarp();
     if (active) {
       row_token[r] = static_cast<int32_t>(t0 + i / k);
@@ -229,8 +269,9 @@ cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, const ui
   permute_scan_kernel<<<1, 1024, 0, s>>>(cc, chunks, E, offsets);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || chunks == 0) return e;
-  permute_rank_kernel<<<static_cast<int>(chunks), 32, E * sizeof(int), s>>>(ids, T, k, E, cc,
-                                                                            row_token, token_row);
+  permute_rank_kernel<<<static_cast<int>(chunks), 32 * kRankWarps,
+                        (kRankWarps * E + kChunkTokens * k) * sizeof(int), s>>>(
+      ids, T, k, E, cc, row_token, token_row);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (aq == nullptr) return cudaSuccess;  // index-only: the GEMM gathers rows by row_token

@@ -64,7 +64,7 @@ def test_topk_gate(fge, t, e, k):
 
 
 @pytest.mark.parametrize("t,e,k,h", [(64, 8, 2, 256), (4096, 64, 8, 2048), (333, 128, 8, 512),
-                                     (200, 16, 1, 128)])
+                                     (200, 16, 1, 128), (1000, 256, 3, 256), (129, 32, 5, 128)])
 def test_permute_bit_exact(fge, t, e, k, h):
     rng = np.random.default_rng(t * k)
     bias = -1.1 * np.log(np.arange(1, e + 1))                  # skewed: some experts empty
