@@ -285,42 +285,56 @@ template <bool YF32, bool OF32>
 __global__ void combine_kernel(const void* __restrict__ y, const int32_t* __restrict__ token_row,
                                const float* __restrict__ gates, int64_t T, int k, int64_t H,
                                void* __restrict__ out) {
+  // one warp per token and per 2048-column block; lane l owns columns l*8 + 256*c (c < 8).
+  // Each slot's row block (4 KB in bf16) is read as 8 independent 16-byte loads per lane
+  // and summed in slot order.
   const int lane = threadIdx.x & 31;
   const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t t = wid; t < T; t += nw) {
+  const int64_t nb = (H + 2047) / 2048;
+  for (int64_t item = wid; item < T * nb; item += nw) {
+    const int64_t t = item / nb;
+    const int64_t c0 = (item - t * nb) * 2048;
     const int my_row = lane < k ? __ldg(token_row + t * k + lane) : 0;
     const float my_gate = lane < k ? __ldg(gates + t * k + lane) : 0.0f;
-    for (int64_t c0 = 0; c0 < H; c0 += 256) {  // all lanes iterate; shuffles stay full
-      const int64_t c = c0 + lane * 8;
-      const bool in = c < H;
-      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int j = 0; j < k; ++j) {
-        const int64_t r = __shfl_sync(0xffffffffu, my_row, j);
-        const float g = __shfl_sync(0xffffffffu, my_gate, j);
-        float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (!in) {
-        } else if constexpr (YF32) {
-          const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(y) + r * H + c);
+    float acc[8][8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[c][i] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const int64_t r = __shfl_sync(0xffffffffu, my_row, j);
+      const float g = __shfl_sync(0xffffffffu, my_gate, j);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int64_t col = c0 + 256 * c + lane * 8;
+        if (col >= H) continue;
+        float v[8];
+        if constexpr (YF32) {
+          const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(y) + r * H + col);
           const float4 a = __ldcs(p), b = __ldcs(p + 1);
           v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
         } else {
-          const uint4 a = __ldcs(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(y) + r * H + c));
+          const uint4 a = __ldcs(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(y) + r * H + col));
           v[0] = bf16_lo(a.x); v[1] = bf16_hi(a.x); v[2] = bf16_lo(a.y); v[3] = bf16_hi(a.y);
           v[4] = bf16_lo(a.z); v[5] = bf16_hi(a.z); v[6] = bf16_lo(a.w); v[7] = bf16_hi(a.w);
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, v[i], acc[i]);
+        for (int i = 0; i < 8; ++i) acc[c][i] = fmaf(g, v[i], acc[c][i]);
       }
-      if (!in) {
-      } else if constexpr (OF32) {
-        float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + t * H + c);
-        o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int64_t col = c0 + 256 * c + lane * 8;
+      if (col >= H) continue;
+      if constexpr (OF32) {
+        float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + t * H + col);
+        o[0] = make_float4(acc[c][0], acc[c][1], acc[c][2], acc[c][3]);
+        o[1] = make_float4(acc[c][4], acc[c][5], acc[c][6], acc[c][7]);
       } else {
-        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + t * H + c) =
-            make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                       pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + t * H + col) =
+            make_uint4(pack_bf16x2(acc[c][0], acc[c][1]), pack_bf16x2(acc[c][2], acc[c][3]),
+                       pack_bf16x2(acc[c][4], acc[c][5]), pack_bf16x2(acc[c][6], acc[c][7]));
       }
     }
   }
@@ -330,7 +344,8 @@ cudaError_t launch_combine(const void* y, int y_f32, const int32_t* token_row,
                            const float* gates, int64_t T, int k, int64_t H, int out_f32,
                            void* out, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const int grid = static_cast<int>(std::min<int64_t>((T + 7) / 8, num_sms() * 8));
+  const int64_t items = T * ((H + 2047) / 2048);
+  const int grid = static_cast<int>(std::min<int64_t>((items + 7) / 8, num_sms() * 8));
   if (y_f32 && out_f32) combine_kernel<true, true><<<grid, 256, 0, s>>>(y, token_row, gates, T, k, H, out);
   else if (y_f32) combine_kernel<true, false><<<grid, 256, 0, s>>>(y, token_row, gates, T, k, H, out);
   else if (out_f32) combine_kernel<false, true><<<grid, 256, 0, s>>>(y, token_row, gates, T, k, H, out);
