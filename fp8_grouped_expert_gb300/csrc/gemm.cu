@@ -509,6 +509,8 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
     uint32_t ait = 0;
     int tile_parity = 0;
     bool ok = true;
+    float pf0 = 0.0f, pf1 = 0.0f;  // group mode: next tile's first two activation scales
+    bool pf_ok = false;
     for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, tile_parity ^= 1) {
       const TileInfo ti = decode_tile(t, nt_count, BN, s_off, s_mtp, E);
       const bool valid = r_in < ti.rows;
@@ -522,8 +524,19 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
         const int src_row = p.row_token ? __ldg(p.row_token + (valid ? row : ti.row0))
                                         : (valid ? row : 0);
         const float* as_row = p.as + static_cast<size_t>(src_row) * G;
-        float sa0 = valid ? __ldg(as_row) : 0.0f;
-        float sa1 = (valid && G > 1) ? __ldg(as_row + 1) : 0.0f;
+        // the first two scales of a tile were requested at the start of the previous tile
+        float sa0 = pf_ok ? pf0 : (valid ? __ldg(as_row) : 0.0f);
+        float sa1 = pf_ok ? pf1 : ((valid && G > 1) ? __ldg(as_row + 1) : 0.0f);
+        pf_ok = false;
+        if (t + static_cast<int>(gridDim.x) < total_tiles) {
+          const TileInfo tn = decode_tile(t + gridDim.x, nt_count, BN, s_off, s_mtp, E);
+          const bool vn = r_in < tn.rows;
+          const int rn = p.row_token ? __ldg(p.row_token + (vn ? tn.row0 + r_in : tn.row0))
+                                     : (vn ? tn.row0 + r_in : 0);
+          pf0 = vn ? __ldg(p.as + static_cast<size_t>(rn) * G) : 0.0f;
+          pf1 = (vn && G > 1) ? __ldg(p.as + static_cast<size_t>(rn) * G + 1) : 0.0f;
+          pf_ok = true;
+        }
         for (int g = 0; g < G; ++g) {
           const uint32_t a = ait & 1;
           const uint32_t w = ait % C::kNSW;
