@@ -83,7 +83,12 @@ struct Cfg {
   static constexpr int kOffMtp = kOffOffs + (kMaxExperts + 1) * 4;
   static constexpr int kOffRed = align16(kOffMtp + (kMaxExperts + 1) * 4);
   static constexpr int kOffRT = align16(kOffRed + 2 * 2 * 128 * 4);  // gather: tile row ids
-  static constexpr int kSmemBytes = kOffRT + 128 * 4 + 1024;  // + alignment slack
+  // bf16 store epilogue (group mode): per warpgroup one 8 KB buffer staging 128 rows x 32
+  // columns for a TMA tile store (64-byte swizzle)
+  static constexpr bool kStageOut = kGroupScale && EPI == kEpiBf16;
+  static constexpr int kOffST = (kOffRT + 128 * 4 + 1023) / 1024 * 1024;
+  static constexpr int kSTBytes = kStageOut ? 2 * 8192 : 0;
+  static constexpr int kSmemBytes = kOffST + kSTBytes + 1024;  // + alignment slack
   static_assert(kNS >= 2, "pipeline needs at least two stages");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
@@ -205,7 +210,8 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
 template <int BN, int BFMT, int EPI>
 __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
   using C = Cfg<BN, BFMT, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -623,6 +629,32 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
             }
             if (wg == 0) p.out_scales[static_cast<size_t>(row) * (inter / 128) + ti.n0 / 256] = s;
           }
+        } else if (C::kStageOut && ti.rows == 128) {
+          // full tile, bf16: each warpgroup stages its 128 columns in four 32-column chunks
+          // (row r at r * 64 bytes, 16-byte pieces swizzled by (r / 2) % 4 as the tensor map's
+          // 64-byte swizzle expects) and one thread stores each chunk with a TMA tile store
+          uint8_t* buf = smem + C::kOffST + wg * 8192;
+          const bool issuer = q == 0 && lane == 0;
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            if (issuer) bulk_wait_read0();  // the previous chunk has left the buffer
+            asm volatile("bar.sync %0, 128;" ::"r"(2 + wg) : "memory");
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int j = ch * 16 + c * 4;
+              const uint4 v = make_uint4(pack_bf16x2(lo_f32(acc2[j]), hi_f32(acc2[j])),
+                                         pack_bf16x2(lo_f32(acc2[j + 1]), hi_f32(acc2[j + 1])),
+                                         pack_bf16x2(lo_f32(acc2[j + 2]), hi_f32(acc2[j + 2])),
+                                         pack_bf16x2(lo_f32(acc2[j + 3]), hi_f32(acc2[j + 3])));
+              *reinterpret_cast<uint4*>(buf + r_in * 64 + ((c ^ ((r_in >> 1) & 3)) << 4)) = v;
+            }
+            fence_proxy_async_smem();
+            asm volatile("bar.sync %0, 128;" ::"r"(2 + wg) : "memory");
+            if (issuer) {
+              tma_store_2d(&tmY, smem_u32(buf), ti.n0 + col_a + ch * 32, ti.row0);
+              bulk_commit();
+            }
+          }
         } else if (valid) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -697,6 +729,9 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
         ++ait;
       }
     }
+    if constexpr (C::kStageOut) {
+      if (q == 0 && lane == 0) bulk_wait0();  // every staged tile store has completed
+    }
   }
 
   // ---------------------------------------------------------------------- teardown
@@ -738,6 +773,21 @@ static bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Output map of the staged bf16 store: [rows, N] bf16, boxes of 32 columns x 128 rows with the
+// 64-byte swizzle.
+static bool make_map_bf16_out(CUtensorMap* m, void* base, uint64_t n, uint64_t rows) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {n, rows};
+  cuuint64_t strides[1] = {n * 2};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -802,7 +852,12 @@ static cudaError_t run(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st)
   p.dense_rows = static_cast<int>(a.R);
   const long tiles_bound = (a.R / 128 + a.E) * (a.N / BN);
   const int grid = static_cast<int>(std::max<long>(1, std::min<long>(num_sms(), tiles_bound)));
-  kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(tmA, tmB, p);
+  CUtensorMap tmY = tmA;  // unused unless the bf16 store is staged
+  if (C::kStageOut && !make_map_bf16_out(&tmY, a.out, a.N, a.R)) {
+    *st = FGE_ERR_CUDA;
+    return cudaSuccess;
+  }
+  kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(tmA, tmB, tmY, p);
   *st = FGE_OK;
   return cudaGetLastError();
 }

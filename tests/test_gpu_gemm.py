@@ -177,3 +177,22 @@ def test_gather_equals_permuted_copy(fge, epi, t, e, k, h, n):
         ref = oracle.grouped_gemm_w4a8(p["aq"], p["as_"], p["offsets"], wp, ws)
         absref = abs_grouped(p["aq"], p["as_"], p["offsets"], wp, ws)
         check_gemm(host(b), ref, absref, False)
+
+
+@pytest.mark.parametrize("t,e,k", [(1024, 4, 1), (700, 3, 2)])
+def test_grouped_bf16_full_and_ragged_tiles(fge, t, e, k):
+    """bf16 output with many full 128-row tiles (stored through shared memory with TMA tile
+    stores) next to each expert's ragged last tile (stored directly)."""
+    rng = np.random.default_rng(t + e)
+    h, n = 512, 768
+    p = _routed_case(rng, t, e, k, h)
+    assert np.diff(p["offsets"]).max() >= 256
+    q = rng.integers(-8, 8, size=(e, n, h))
+    wp = pack_int4(q)
+    ws = rng.uniform(0.002, 0.02, size=(e, n, h // 128)).astype(np.float32)
+    wd, sd = _prepack(fge, wp, ws, "subnormal")
+    out = fge.grouped_gemm_w4a8(to_dev(p["aq"]), to_dev(p["as_"]), to_dev(p["offsets"]), wd, sd,
+                                out_dtype=torch.bfloat16)
+    ref = oracle.grouped_gemm_w4a8(p["aq"], p["as_"], p["offsets"], wp, ws)
+    absref = abs_grouped(p["aq"], p["as_"], p["offsets"], wp, ws)
+    check_gemm(host(out), ref, absref, True)
