@@ -83,9 +83,9 @@ struct Cfg {
   static constexpr int kOffMtp = kOffOffs + (kMaxExperts + 1) * 4;
   static constexpr int kOffRed = align16(kOffMtp + (kMaxExperts + 1) * 4);
   static constexpr int kOffRT = align16(kOffRed + 2 * 2 * 128 * 4);  // gather: tile row ids
-  // bf16 store epilogue (group mode): per warpgroup one 8 KB buffer staging 128 rows x 32
-  // columns for a TMA tile store (64-byte swizzle)
-  static constexpr bool kStageOut = kGroupScale && EPI == kEpiBf16;
+  // bf16 and SwiGLU store epilogues (group mode): per warpgroup one 8 KB buffer staging 128
+  // rows x 64 bytes for a TMA tile store (64-byte swizzle)
+  static constexpr bool kStageOut = kGroupScale && (EPI == kEpiBf16 || EPI == kEpiSwiglu);
   static constexpr int kOffST = (kOffRT + 128 * 4 + 1023) / 1024 * 1024;
   static constexpr int kSTBytes = kStageOut ? 2 * 8192 : 0;
   static constexpr int kSmemBytes = kOffST + kSTBytes + 1024;  // + alignment slack
@@ -610,25 +610,44 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
           const float s = scale_from_amax(amax_all);
           const float inv_s = __frcp_rn(s);  // h * (1/s): same e4m3 code as h / s except
                                              // within 2^-23 of a rounding boundary
-          if (valid) {
-            const int inter = p.N / 2;
+          const int inter = p.N / 2;
+          uint4 o[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int i = 16 * c;
+            o[c].x = cvt_e4m3x4(hv[i + 0] * inv_s, hv[i + 1] * inv_s,
+                                hv[i + 2] * inv_s, hv[i + 3] * inv_s);
+            o[c].y = cvt_e4m3x4(hv[i + 4] * inv_s, hv[i + 5] * inv_s,
+                                hv[i + 6] * inv_s, hv[i + 7] * inv_s);
+            o[c].z = cvt_e4m3x4(hv[i + 8] * inv_s, hv[i + 9] * inv_s,
+                                hv[i + 10] * inv_s, hv[i + 11] * inv_s);
+            o[c].w = cvt_e4m3x4(hv[i + 12] * inv_s, hv[i + 13] * inv_s,
+                                hv[i + 14] * inv_s, hv[i + 15] * inv_s);
+          }
+          if (C::kStageOut && ti.rows == 128) {
+            // full tile: the warpgroup's 128 rows x 64 codes go out as one TMA tile store
+            // from an 8 KB shared buffer (64-byte swizzle, as for the bf16 store)
+            uint8_t* buf = smem + C::kOffST + wg * 8192;
+            const bool issuer = q == 0 && lane == 0;
+            if (issuer) bulk_wait_read0();
+            asm volatile("bar.sync %0, 128;" ::"r"(2 + wg) : "memory");
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              *reinterpret_cast<uint4*>(buf + r_in * 64 + ((c ^ ((r_in >> 1) & 3)) << 4)) = o[c];
+            fence_proxy_async_smem();
+            asm volatile("bar.sync %0, 128;" ::"r"(2 + wg) : "memory");
+            if (issuer) {
+              tma_store_2d(&tmY, smem_u32(buf), ti.n0 / 2 + wg * 64, ti.row0);
+              bulk_commit();
+            }
+          } else if (valid) {
             uint8_t* hq = reinterpret_cast<uint8_t*>(p.out) + static_cast<size_t>(row) * inter +
                           (ti.n0 / 2) + wg * 64;
 #pragma unroll
-            for (int i = 0; i < 64; i += 16) {
-              uint4 o;
-              o.x = cvt_e4m3x4(hv[i + 0] * inv_s, hv[i + 1] * inv_s,
-                               hv[i + 2] * inv_s, hv[i + 3] * inv_s);
-              o.y = cvt_e4m3x4(hv[i + 4] * inv_s, hv[i + 5] * inv_s,
-                               hv[i + 6] * inv_s, hv[i + 7] * inv_s);
-              o.z = cvt_e4m3x4(hv[i + 8] * inv_s, hv[i + 9] * inv_s,
-                               hv[i + 10] * inv_s, hv[i + 11] * inv_s);
-              o.w = cvt_e4m3x4(hv[i + 12] * inv_s, hv[i + 13] * inv_s,
-                               hv[i + 14] * inv_s, hv[i + 15] * inv_s);
-              *reinterpret_cast<uint4*>(hq + i) = o;
-            }
-            if (wg == 0) p.out_scales[static_cast<size_t>(row) * (inter / 128) + ti.n0 / 256] = s;
+            for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(hq + 16 * c) = o[c];
           }
+          if (valid && wg == 0)
+            p.out_scales[static_cast<size_t>(row) * (inter / 128) + ti.n0 / 256] = s;
         } else if (C::kStageOut && ti.rows == 128) {
           // full tile, bf16: each warpgroup stages its 128 columns in four 32-column chunks
           // (row r at r * 64 bytes, 16-byte pieces swizzled by (r / 2) % 4 as the tensor map's
@@ -776,6 +795,21 @@ static bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64
   return r == CUDA_SUCCESS;
 }
 
+// Output map of the staged SwiGLU store: [rows, inner] bytes, boxes of 64 bytes x 128 rows
+// with the 64-byte swizzle.
+static bool make_map_u8_swz64(CUtensorMap* m, void* base, uint64_t inner, uint64_t rows) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Output map of the staged bf16 store: [rows, N] bf16, boxes of 32 columns x 128 rows with the
 // 64-byte swizzle.
 static bool make_map_bf16_out(CUtensorMap* m, void* base, uint64_t n, uint64_t rows) {
@@ -852,8 +886,15 @@ static cudaError_t run(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st)
   p.dense_rows = static_cast<int>(a.R);
   const long tiles_bound = (a.R / 128 + a.E) * (a.N / BN);
   const int grid = static_cast<int>(std::max<long>(1, std::min<long>(num_sms(), tiles_bound)));
-  CUtensorMap tmY = tmA;  // unused unless the bf16 store is staged
-  if (C::kStageOut && !make_map_bf16_out(&tmY, a.out, a.N, a.R)) {
+  CUtensorMap tmY = tmA;  // unused unless the store is staged
+  bool okY = true;
+  if constexpr (C::kStageOut) {
+    if (EPI == kEpiSwiglu)  // hq: [rows, N/2] e4m3 codes, 64-byte x 128-row boxes
+      okY = make_map_u8_swz64(&tmY, a.out, a.N / 2, a.R);
+    else
+      okY = make_map_bf16_out(&tmY, a.out, a.N, a.R);
+  }
+  if (!okY) {
     *st = FGE_ERR_CUDA;
     return cudaSuccess;
   }

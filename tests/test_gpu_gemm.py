@@ -196,3 +196,24 @@ def test_grouped_bf16_full_and_ragged_tiles(fge, t, e, k):
     ref = oracle.grouped_gemm_w4a8(p["aq"], p["as_"], p["offsets"], wp, ws)
     absref = abs_grouped(p["aq"], p["as_"], p["offsets"], wp, ws)
     check_gemm(host(out), ref, absref, True)
+
+
+def test_swiglu_full_and_ragged_tiles(fge):
+    """SwiGLU + requant epilogue with full 128-row tiles (TMA tile stores of the codes) and
+    ragged last tiles (direct stores)."""
+    rng = np.random.default_rng(77)
+    t, e, k, h, inter = 1024, 4, 1, 256, 512
+    p = _routed_case(rng, t, e, k, h)
+    assert np.diff(p["offsets"]).max() >= 256
+    wp = pack_int4(rng.integers(-8, 8, size=(e, 2 * inter, h)))
+    ws = rng.uniform(0.002, 0.02, size=(e, 2 * inter, h // 128)).astype(np.float32)
+    wd, sd = _prepack(fge, wp, ws, "subnormal", interleave=True)
+    hq, hs = fge.grouped_gemm_w4a8(to_dev(p["aq"]), to_dev(p["as_"]), to_dev(p["offsets"]), wd,
+                                   sd, epilogue="swiglu")
+    c = oracle.grouped_gemm_w4a8(p["aq"], p["as_"], p["offsets"], wp, ws)
+    rq, rs, _ = oracle.swiglu_requant(c, inter)
+    gq, gs = host(hq), host(hs)
+    np.testing.assert_allclose(gs, rs, rtol=1e-4)
+    diff = gq != rq
+    assert diff.mean() <= 0.005, diff.mean()
+    assert np.all(np.abs(gq[diff].astype(int) - rq[diff].astype(int)) == 1)
