@@ -41,6 +41,7 @@ SIGNATURES = {
     "fge_fp8_quant_act": [_P, _I64, _I64, _I, _P, _P, _P, _SZ, _P],
     "fge_moe_topk_gate": [_P, _I64, _I, _I, _P, _P, _P],
     "fge_moe_permute": [_P, _I64, _I, _I, _P, _P, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P],
+    "fge_moe_permute_quant": [_P, _I64, _I, _I, _P, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P],
     "fge_w4_prepack": [_P, _P, _I, _I64, _I64, _I, _I, _P, _P, _P],
     "fge_grouped_gemm_w4a8": [_P, _P, _P, _I64, _P, _P, _I, _I64, _I64, _I, _I, _I, _P, _P, _P,
                               _SZ, _P],
@@ -203,6 +204,31 @@ def moe_permute(ids, num_experts, xq, xs, index_only=False):
                                  _ptr(out["token_row"]), _ptr(out.get("aq")),
                                  _ptr(out.get("as_")), _ptr(ws), ws.numel(), _stream(ids)),
            "fge_moe_permute")
+    return out
+
+
+def moe_permute_quant(ids, num_experts, x):
+    """G128 quantization folded into the permutation's row copy: x bf16 [T, H] -> the same dict
+    as moe_permute (offsets, row_token, token_row, aq, as_)."""
+    _need(ids, torch.int32, "ids")
+    _need(x, torch.bfloat16, "x")
+    _ensure_init(ids.device)
+    t, k = ids.shape
+    h = x.shape[1]
+    dev = ids.device
+    r = t * k
+    out = dict(
+        offsets=torch.empty(num_experts + 1, dtype=torch.int32, device=dev),
+        row_token=torch.empty(r, dtype=torch.int32, device=dev),
+        token_row=torch.empty((t, k), dtype=torch.int32, device=dev),
+        aq=torch.empty((r, h), dtype=torch.uint8, device=dev),
+        as_=torch.empty((r, h // 128), dtype=torch.float32, device=dev),
+    )
+    ws = new_workspace(workspace_bytes(OP_PERMUTE, t, h, 0, num_experts, k), dev)
+    _check(lib().fge_moe_permute_quant(_ptr(ids), t, k, num_experts, _ptr(x), h,
+                                       _ptr(out["offsets"]), _ptr(out["row_token"]),
+                                       _ptr(out["token_row"]), _ptr(out["aq"]), _ptr(out["as_"]),
+                                       _ptr(ws), ws.numel(), _stream(ids)), "fge_moe_permute_quant")
     return out
 
 

@@ -200,6 +200,23 @@ fge_status fge_moe_permute(const int32_t* ids, int64_t T, int k, int E, const ui
                                   static_cast<uint8_t*>(ws) + kWsHeaderBytes, stream));
 }
 
+fge_status fge_moe_permute_quant(const int32_t* ids, int64_t T, int k, int E, const void* x,
+                                 int64_t H, int32_t* offsets, int32_t* row_token,
+                                 int32_t* token_row, uint8_t* aq, float* as, void* ws,
+                                 size_t ws_bytes, fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(ids && x && offsets && row_token && token_row && aq && as && ws,
+              FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(T >= 0 && E >= 1 && E <= 1024 && k >= 1 && k <= E && k <= 32, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(H > 0 && H % 128 == 0 && T * k < (1LL << 31), FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(al16(x) && al16(aq) && al16(ws), FGE_ERR_MISALIGNED);
+  FGE_REQUIRE(ws_bytes >= fge_workspace_bytes(FGE_OP_PERMUTE, T, H, 0, E, k),
+              FGE_ERR_WORKSPACE_TOO_SMALL);
+  return from_cuda(launch_permute_quant(ids, T, k, E, static_cast<const uint16_t*>(x), H, offsets,
+                                        row_token, token_row, aq, as,
+                                        static_cast<uint8_t*>(ws) + kWsHeaderBytes, stream));
+}
+
 fge_status fge_w4_prepack(const uint8_t* w, const float* w_scale, int E, int64_t N, int64_t K,
                           int gate_up_interleave, fge_w4_format format, uint8_t* w_dev,
                           float* w_scale_dev, fge_stream_t stream) {
@@ -400,12 +417,15 @@ fge_status fge_moe_layer_forward(const float* logits, const void* x, int64_t T, 
   const int64_t R = T * k;
   const int out_f32 = out_dtype == FGE_DTYPE_F32;
   FGE_CHECK(from_cuda(launch_topk_gate(logits, T, E, k, w.ids, w.gates, stream)));
-  FGE_CHECK(from_cuda(launch_quant_g128(static_cast<const uint16_t*>(x), T, H, w.xq, w.xs, stream)));
+
   // The permuted copy of the activation rows plus a tiled A load beats gathering the rows
   // in the GEMM (fge_grouped_gemm_w4a8_gather): 32 four-row TMA gathers per K group cost
   // more than the copy kernel saves.
-  FGE_CHECK(from_cuda(launch_permute(w.ids, T, k, E, w.xq, w.xs, H, w.offsets, w.row_token,
-                                     w.token_row, w.aq, w.as, w.perm, stream)));
+  // the G128 activation quantization runs inside the permutation's row copy: each token's
+  // bf16 row is read once and its codes and scales go straight to its k expert rows
+  FGE_CHECK(from_cuda(launch_permute_quant(w.ids, T, k, E, static_cast<const uint16_t*>(x), H,
+                                           w.offsets, w.row_token, w.token_row, w.aq, w.as,
+                                           w.perm, stream)));
   FGE_CHECK(grouped_common(w.aq, w.as, w.offsets, R, w_gu, s_gu, E, 2 * I, H, format, 0, nullptr,
                            2, w.hq, w.hs, ws, ws_bytes, stream));
   FGE_CHECK(grouped_common(w.hq, w.hs, w.offsets, R, w_dn, s_dn, E, H, I, format, 0, nullptr,

@@ -43,6 +43,11 @@ cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, const ui
                            const float* xs, int64_t H, int32_t* offsets, int32_t* row_token,
                            int32_t* token_row, uint8_t* aq, float* as, void* scratch,
                            cudaStream_t s);
+// Permutation with the G128 activation quantization fused into the row copy (x: bf16 [T, H]).
+cudaError_t launch_permute_quant(const int32_t* ids, int64_t T, int k, int E,
+                                 const uint16_t* x, int64_t H, int32_t* offsets,
+                                 int32_t* row_token, int32_t* token_row, uint8_t* aq, float* as,
+                                 void* scratch, cudaStream_t s);
 cudaError_t launch_combine(const void* y, int y_f32, const int32_t* token_row,
                            const float* gates, int64_t T, int k, int64_t H, int out_f32,
                            void* out, cudaStream_t s);

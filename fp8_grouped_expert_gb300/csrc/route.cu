@@ -255,6 +255,60 @@ __global__ void permute_copy_kernel(const uint8_t* __restrict__ xq, const float*
   }
 }
 
+// (4') quantize and copy in one pass: one warp per token reads its bf16 row once, quantizes
+// each 128-value group exactly as quant_g128_kernel does (16 lanes x 8 values, shuffle amax,
+// s = amax / 448, IEEE division, e4m3 round to nearest even) and writes the codes and the
+// scale to the token's k expert rows.  Two groups per warp step.
+__global__ void permute_quant_copy_kernel(const uint4* __restrict__ x, int64_t T, int k,
+                                          int64_t H, const int32_t* __restrict__ token_row,
+                                          uint8_t* __restrict__ aq, float* __restrict__ as) {
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4, hl = lane & 15;
+  const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t G = H / 128;
+  for (int64_t t = wid; t < T; t += nw) {
+    const int my_row = lane < k ? __ldg(token_row + t * k + lane) : 0;
+    for (int64_t g0 = 0; g0 < G; g0 += 2) {  // all lanes iterate; shuffles stay full
+      const int64_t g = g0 + half;
+      const bool in = g < G;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (in) v = __ldcs(x + (t * G + g) * 16 + hl);
+      float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                    bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+      for (int d = 8; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+      const float sc = scale_from_amax(amax);
+      uint2 q;
+      q.x = cvt_e4m3x4(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc), __fdiv_rn(f[2], sc), __fdiv_rn(f[3], sc));
+      q.y = cvt_e4m3x4(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc), __fdiv_rn(f[6], sc), __fdiv_rn(f[7], sc));
+      for (int j = 0; j < k; ++j) {
+        const int64_t r = __shfl_sync(0xffffffffu, my_row, j);
+        if (in) {
+          reinterpret_cast<uint2*>(aq + r * H)[g * 16 + hl] = q;
+          if (hl == 0) as[r * G + g] = sc;
+        }
+      }
+    }
+  }
+}
+
+cudaError_t launch_permute_quant(const int32_t* ids, int64_t T, int k, int E,
+                                 const uint16_t* x, int64_t H, int32_t* offsets,
+                                 int32_t* row_token, int32_t* token_row, uint8_t* aq, float* as,
+                                 void* scratch, cudaStream_t s) {
+  cudaError_t e = launch_permute(ids, T, k, E, nullptr, nullptr, H, offsets, row_token,
+                                 token_row, nullptr, nullptr, scratch, s);
+  if (e != cudaSuccess || T == 0) return e;
+  const int grid = static_cast<int>(std::min<int64_t>((T + 7) / 8, num_sms() * 8));
+  permute_quant_copy_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), T, k, H,
+                                                 token_row, aq, as);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, const uint8_t* xq,
                            const float* xs, int64_t H, int32_t* offsets, int32_t* row_token,
                            int32_t* token_row, uint8_t* aq, float* as, void* scratch,

@@ -140,6 +140,16 @@ fge_status fge_moe_permute(const int32_t* ids, int64_t T, int k, int E, const ui
                            int32_t* token_row, uint8_t* aq, float* as, void* workspace,
                            size_t workspace_bytes, fge_stream_t stream);
 
+/* moe_permute_quant -- fge_moe_permute with the G128 activation quantization of
+ * fge_fp8_quant_act folded into the row copy: each token's bf16 row is read once and its
+ * e4m3 codes and scales are written straight to its k expert rows (same codes and scales as
+ * quantizing first, bit for bit).  x_bf16: [T, H] bf16; other arguments as fge_moe_permute.
+ * Workspace: FGE_OP_PERMUTE. */
+fge_status fge_moe_permute_quant(const int32_t* ids, int64_t T, int k, int E,
+                                 const void* x_bf16, int64_t H, int32_t* offsets,
+                                 int32_t* row_token, int32_t* token_row, uint8_t* aq, float* as,
+                                 void* workspace, size_t workspace_bytes, fge_stream_t stream);
+
 /* w4_prepack -- load-time layout of a resident int4 expert bank for the grouped GEMM.
  * Input (canonical): w [E, N, K/2] bytes, two's-complement nibbles, byte b of a row holds
  * element 2b in the low nibble and 2b+1 in the high nibble; w_scale [E, N, K/128] float.

@@ -121,3 +121,20 @@ def test_tiny_inputs_layer_routing_consistency(fge):
     ids, gates = fge.moe_topk_gate(to_dev(inp.logits), inp.k)
     rid, _ = oracle.topk_gate(inp.logits, inp.k)
     assert np.array_equal(host(ids), rid)
+
+
+@pytest.mark.parametrize("t,e,k,h", [(64, 8, 2, 256), (4096, 64, 8, 2048), (333, 128, 3, 384)])
+def test_permute_quant_equals_quant_then_permute(fge, t, e, k, h):
+    """The quantization folded into the permutation gives exactly the codes, scales and
+    indices of quantizing first and permuting after."""
+    rng = np.random.default_rng(t + 3 * k)
+    lg = rng.standard_normal((t, e)).astype(np.float32)
+    x = (rng.standard_normal((t, h)) * np.exp(rng.uniform(-4, 4, (t, 1)))).astype(np.float32)
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)
+    xd = bf16_dev(bits)
+    ids, _ = fge.moe_topk_gate(to_dev(lg), k)
+    xq, xs = fge.fp8_quant_act(xd, "g128")
+    a = fge.moe_permute(ids, e, xq, xs)
+    b = fge.moe_permute_quant(ids, e, xd)
+    for key in ("offsets", "row_token", "token_row", "aq", "as_"):
+        assert torch.equal(a[key], b[key]), key
