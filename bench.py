@@ -35,6 +35,7 @@ KNOWN_GATE_UP_TRAFFIC = {
     "bbab9dbfa1323528:422dc7d17945d077": 194.44e6,
     "84cb06a30c9e661f:21919a5a3be18255": 194.99e6,
     "3588543b1f588e0c:8f75c66d2d1b5e12": 194.63e6,
+    "6c7fc4a2718cae64:72b05a4e51127510": 194.80e6,
 }
 
 
