@@ -578,13 +578,16 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
               tmem_wait_ld();
               reg_fence32(v[(c + 1) & 1]);
             }
+            if (c == 2) {
+              // the last chunk is in registers: the TMEM buffer goes back to the MMA issuer
+              // now, one chunk of promotion math before the end of the group
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_tempty + 8 * (a * C::kHalves + half_slot));
+            }
           }
-          tc_fence_before();
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(bar_tempty + 8 * (a * C::kHalves + half_slot));
-            mbar_arrive(bar_swempty + 8 * w);
-          }
+          if (lane == 0) mbar_arrive(bar_swempty + 8 * w);
           ++ait;
           sa0 = sa1;
           sa1 = sa2;
