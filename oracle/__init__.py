@@ -32,6 +32,15 @@ from .fp8 import (  # noqa: F401
     quant_act_per_tensor,
     quant_act_per_row,
 )
+from .mx import (  # noqa: F401
+    E2M1_MAX,
+    MX_BLOCK,
+    e2m1_decode,
+    e2m1_encode,
+    mx_block_exponent,
+    mx_quant_e2m1,
+    mx_dequant_e2m1,
+)
 from .moe import (  # noqa: F401
     topk_gate,
     moe_permute,
