@@ -39,6 +39,7 @@ SIGNATURES = {
     "fge_clear_device_status": [_P, _P],
     "fge_read_device_status": [_P, _P, ctypes.POINTER(ctypes.c_int32)],
     "fge_fp8_quant_act": [_P, _I64, _I64, _I, _P, _P, _P, _SZ, _P],
+    "fge_mx_quant_e2m1": [_P, _I64, _I64, _P, _P, _P],
     "fge_moe_topk_gate": [_P, _I64, _I, _I, _P, _P, _P],
     "fge_moe_permute": [_P, _I64, _I, _I, _P, _P, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P],
     "fge_moe_permute_quant": [_P, _I64, _I, _I, _P, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P],
@@ -165,6 +166,19 @@ def fp8_quant_act(x, mode="g128", workspace=None):
         code = lib().fge_fp8_quant_act(_ptr(x), m, k, SCALE_PER_TENSOR, _ptr(xq), _ptr(xs),
                                        _ptr(ws), ws.numel(), _stream(x))
     _check(code, "fge_fp8_quant_act")
+    return xq, xs
+
+
+def mx_quant_e2m1(x):
+    """x: bf16 [M, K] (K % 32 == 0) -> (xq uint8 [M, K/2] E2M1 code pairs, low nibble first;
+    xs uint8 [M, K/32] E8M0 block scale codes)."""
+    _need(x, torch.bfloat16, "x")
+    _ensure_init(x.device)
+    m, k = x.shape
+    xq = torch.empty((m, k // 2), dtype=torch.uint8, device=x.device)
+    xs = torch.empty((m, k // 32), dtype=torch.uint8, device=x.device)
+    _check(lib().fge_mx_quant_e2m1(_ptr(x), m, k, _ptr(xq), _ptr(xs), _stream(x)),
+           "fge_mx_quant_e2m1")
     return xq, xs
 
 

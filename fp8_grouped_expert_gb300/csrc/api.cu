@@ -173,6 +173,15 @@ fge_status fge_fp8_quant_act(const void* x, int64_t M, int64_t K, fge_scale_mode
                                            static_cast<WsHeader*>(ws), stream));
 }
 
+fge_status fge_mx_quant_e2m1(const void* x, int64_t M, int64_t K, uint8_t* xq, uint8_t* xs,
+                             fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(M >= 0 && K > 0 && K % 32 == 0, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(x && xq && xs, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(al16(x) && al16(xq), FGE_ERR_MISALIGNED);
+  return from_cuda(launch_mx_quant_e2m1(static_cast<const uint16_t*>(x), M, K, xq, xs, stream));
+}
+
 fge_status fge_moe_topk_gate(const float* logits, int64_t T, int E, int k, int32_t* ids,
                              float* gates, fge_stream_t stream) {
   FGE_CHECK(cur_device_ok());

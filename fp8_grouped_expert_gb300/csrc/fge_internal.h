@@ -34,6 +34,8 @@ cudaError_t launch_quant_g128(const uint16_t* x, int64_t M, int64_t K, uint8_t* 
                               cudaStream_t s);
 cudaError_t launch_quant_rows(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,
                               cudaStream_t s);
+cudaError_t launch_mx_quant_e2m1(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq,
+                                 uint8_t* xs, cudaStream_t s);
 cudaError_t launch_quant_per_tensor(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq,
                                     float* xs, WsHeader* hdr, cudaStream_t s);
 cudaError_t launch_topk_gate(const float* logits, int64_t T, int E, int k, int32_t* ids,

@@ -4,6 +4,8 @@
 // HBM-bound: 16-byte vector loads and stores, warp-shuffle amax, grids sized to the SMs.
 #include <algorithm>
 
+#include <cuda_fp4.h>
+
 #include "fge_device.cuh"
 
 namespace fge {
@@ -117,6 +119,57 @@ __global__ void quant_row_kernel(const uint4* __restrict__ x, int64_t M, int64_t
     }
     if (lane == 0) xs[r] = s;
   }
+}
+
+// MXFP4 activations ("[RFC] Support FP4 (E2M1) activation dispatch in MegaMoE": E2M1 codes
+// halve the dispatch bytes of e4m3).  One power-of-two scale per 32 consecutive values:
+// E = max(floor(log2(amax)) - 2, -127), stored as the E8M0 code E + 127, so the block's
+// largest magnitude lands in [4, 8); each value is cast to E2M1 from x * 2^-E (exact: a
+// power-of-two multiply) with round to nearest even, saturating at 6.  Rows never split a
+// block (K % 32 == 0), so the tensor is walked as one flat array: 8 values per lane, four
+// lanes per block, one 4-byte store of codes per lane.
+__global__ void mx_e2m1_kernel(const uint4* __restrict__ x, int64_t n8, uint32_t* __restrict__ xq,
+                               uint8_t* __restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t w0 = t0 - lane; w0 < n8; w0 += stride) {  // warp-uniform trip count
+    const int64_t c = w0 + lane;
+    const bool valid = c < n8;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (valid) v = __ldcs(x + c);
+    const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                        bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    // floor(log2(amax)) is the exponent field minus 127 for a normal amax; a zero or
+    // subnormal amax lands on the clamp
+    const int ef = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+    const int e = max(ef - 129, -127);
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-E
+    uint32_t q = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      q |= (static_cast<uint32_t>(__nv_cvt_float_to_fp4(f[i] * inv, __NV_E2M1,
+                                                        cudaRoundNearest)) & 0xFu) << (4 * i);
+    if (valid) {
+      xq[c] = q;
+      if ((lane & 3) == 0) xs[c >> 2] = static_cast<uint8_t>(e + 127);
+    }
+  }
+}
+
+cudaError_t launch_mx_quant_e2m1(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq,
+                                 uint8_t* xs, cudaStream_t s) {
+  const int64_t n8 = M * (K / 8);
+  if (n8 == 0) return cudaSuccess;
+  const int grid = static_cast<int>(std::min<int64_t>((n8 + 255) / 256, num_sms() * 8));
+  mx_e2m1_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), n8,
+                                      reinterpret_cast<uint32_t*>(xq), xs);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_quant_rows(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,

@@ -117,6 +117,21 @@ fge_status fge_fp8_quant_act(const void* x_bf16, int64_t M, int64_t K, fge_scale
                              uint8_t* xq, float* xs, void* workspace, size_t workspace_bytes,
                              fge_stream_t stream);
 
+/* mx_quant_e2m1 -- FP4 (E2M1) activations with one power-of-two scale per 32 values
+ * (MXFP4).  "[RFC] Support FP4 (E2M1) activation dispatch in MegaMoE" proposes E2M1
+ * activations for the expert dispatch buffer (half the bytes of e4m3) feeding an MXF4
+ * main loop; the block size and scale format are the MX convention it names:
+ *   E = max(floor(log2(amax)) - 2, -127) over each block of 32 consecutive values of a row
+ *   (-127 for an all-zero block), stored as the E8M0 code E + 127 (scale 2^E);
+ *   q = E2M1(x * 2^-E), round to nearest even, saturating at 6; a zero keeps its sign.
+ * x_bf16: [M, K] bf16, 16-byte aligned.  xq: [M, K/2] bytes (out), 16-byte aligned: byte b
+ * of a row holds the codes of elements 2b (low nibble) and 2b + 1 (high nibble).
+ * xs: [M, K/32] E8M0 codes (out), any alignment.  K % 32 == 0; M may be 0.
+ * FGE_ERR_BAD_SHAPE, FGE_ERR_INVALID_ARG (NULL pointer) or FGE_ERR_MISALIGNED before any
+ * launch; no workspace, no host sync. */
+fge_status fge_mx_quant_e2m1(const void* x_bf16, int64_t M, int64_t K, uint8_t* xq,
+                             uint8_t* xs, fge_stream_t stream);
+
 /* moe_topk_gate -- top-k experts per token and their gates.
  * The pages route tokens to experts without fixing the rule ("FP8 grouped-expert prefill
  * ..." section 1); this is standard top-k routing: experts in descending logit order (ties
