@@ -279,6 +279,10 @@ def run_gpu(args):
     stages = stage_times(fge, torch, inp, x, logits, w_gu, s_gu, w_dn, s_dn, fmt, flush, dev,
                          args.steps)
 
+    # ---- FP4 activations (E2M1 + a power-of-two scale per 32): the dispatch-buffer half of
+    #      the E2M1 row, timed beside the e4m3 G128 quantization (not part of the step)
+    mx_ms = mx_quant_time(fge, torch, x, flush, dev, args.steps)
+
     # ---- the per-token int4 dispatch that the grouped GEMM replaces (context, untimed)
     base_ms = None
     if not args.no_baseline:
@@ -350,6 +354,18 @@ def run_gpu(args):
         "e2e": {"value": world * inp.T / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step * args.steps,
+        "e2m1_activations": {
+            "quant_ms": mx_ms,
+            "bytes_read": 2 * inp.T * inp.H,
+            "bytes_written": inp.T * inp.H // 2 + inp.T * inp.H // 32,
+            "hbm_gbs": (2 * inp.T * inp.H + inp.T * inp.H // 2 + inp.T * inp.H // 32)
+                       / (mx_ms / 1e3) / 1e9,
+            "hbm_frac": (2 * inp.T * inp.H + inp.T * inp.H // 2 + inp.T * inp.H // 32)
+                        / (mx_ms / 1e3) / 1e9 / hbm,
+            "e4m3_g128_quant_ms": stages["quant_g128"],
+            "e4m3_g128_bytes_written": inp.T * inp.H + inp.T * inp.H // 128 * 4,
+            "what": "fge_mx_quant_e2m1 on the layer's activations: E2M1 codes + E8M0 scale "
+                    "per 32 values (dispatch bytes), against the e4m3 G128 quantization"},
         "per_token_dispatch_baseline": None if base_ms is None else {
             "ms_per_step": base_ms, "grouped_speedup": base_ms / ms,
             "what": "same layer, one CTA per routed token: int4 weights dequantized in "
@@ -358,6 +374,22 @@ def run_gpu(args):
     }
     print(json.dumps(line))
     return 0
+
+
+def mx_quant_time(fge, torch, x, flush, dev, steps):
+    """FP4 (E2M1, MXFP4) quantization of the layer's activations through its C-ABI call,
+    timed like a stage (L2 flushed before each call; first call dropped)."""
+    stream = torch.cuda.current_stream(dev)
+    times = []
+    for i in range(steps + 1):
+        flush.fill_(5)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fge.mx_quant_e2m1(x)
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in times[1:]) / steps
 
 
 def stage_times(fge, torch, inp, x, logits, w_gu, s_gu, w_dn, s_dn, fmt, flush, dev, steps):
