@@ -38,6 +38,8 @@ struct GemmParams {
   int32_t* status;
   int E, N, K, G;
   int dense_rows;          // offsets == nullptr: one expert owning rows [0, dense_rows)
+  int swap_m;              // BN = 16 (decode sizes): tokens in the B tile; out is [swap_m, out_ld]
+  int out_ld;
 };
 
 constexpr int align16(int x) { return (x + 15) / 16 * 16; }
@@ -53,7 +55,8 @@ struct Cfg {
   static constexpr int kStageBytes = kABytes + kBLoadBytes;
   static constexpr int kPipeBytes = 192 * 1024;
   static constexpr int kNS = (kPipeBytes - kNU * kBUBytes) / kStageBytes;
-  static constexpr int kEpiWarps = BN / 32;  // one warpgroup per 128 columns
+  // one warpgroup per 128 columns; the 16-column decode tile still needs all 128 lanes
+  static constexpr int kEpiWarps = BN >= 128 ? BN / 32 : 4;
   static constexpr int kEpiThreads = kEpiWarps * 32;
   static constexpr int kThreads = 256 + kEpiThreads;
   static constexpr int kTmemCols = 2 * BN;
@@ -578,16 +581,13 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
               tmem_wait_ld();
               reg_fence32(v[(c + 1) & 1]);
             }
-            if (c == 2) {
-              // the last chunk is in registers: the TMEM buffer goes back to the MMA issuer
-              // now, one chunk of promotion math before the end of the group
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(bar_tempty + 8 * (a * C::kHalves + half_slot));
-            }
           }
+          tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_swempty + 8 * w);
+          if (lane == 0) {
+            mbar_arrive(bar_tempty + 8 * (a * C::kHalves + half_slot));
+            mbar_arrive(bar_swempty + 8 * w);
+          }
           ++ait;
           sa0 = sa1;
           sa1 = sa2;
@@ -697,6 +697,36 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
                     pack_bf16x2(lo_f32(acc2[(c * 32 + i) / 2 + 1]), hi_f32(acc2[(c * 32 + i) / 2 + 1])),
                     pack_bf16x2(lo_f32(acc2[(c * 32 + i) / 2 + 2]), hi_f32(acc2[(c * 32 + i) / 2 + 2])),
                     pack_bf16x2(lo_f32(acc2[(c * 32 + i) / 2 + 3]), hi_f32(acc2[(c * 32 + i) / 2 + 3])));
+            }
+          }
+        }
+      } else if constexpr (BN == 16) {
+        // decode sizes, operands swapped: the 128 lanes are output features (A rows = weight
+        // rows), the 16 columns are tokens; token j's value of feature `row` goes to
+        // out[j * out_ld + row], so each store of a warp covers 32 consecutive features
+        const uint32_t a = ait & 1;
+        if (!mbar_wait(bar_tfull + 8 * a, (ait >> 1) & 1, s_abort, p.status)) break;
+        tc_fence_after();
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(tmem_base + lane_addr + a * BN, v);
+        tmem_wait_ld();
+        reg_fence16(v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_tempty + 8 * a);
+        ++ait;
+        if (valid) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (j < p.swap_m) {
+              // per-row activation scales belong to the tokens: one per column here
+              const float rs = p.sa_rows ? __ldg(p.sa_rows + j) * tensor_scale : tensor_scale;
+              const float yv = rs * __uint_as_float(v[j]);
+              const size_t o = static_cast<size_t>(j) * p.out_ld + row;
+              if constexpr (EPI == kEpiF32)
+                reinterpret_cast<float*>(p.out)[o] = yv;
+              else
+                reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(yv);
             }
           }
         }
@@ -871,7 +901,7 @@ static cudaError_t run(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st)
     *st = FGE_ERR_CUDA;
     return cudaSuccess;
   }
-  GemmParams p;
+  GemmParams p{};
   p.as = a.as;
   p.sw = a.per_tensor ? nullptr : a.sw;
   p.sa_tensor = a.sa_tensor;
@@ -906,8 +936,53 @@ static cudaError_t run(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st)
   return cudaGetLastError();
 }
 
+// Decode sizes (at most 16 activation rows, one expert, per-tensor or per-row scales): the
+// operands trade places so that the 128-row side of the MMA walks the weights.  A = the
+// weight matrix [N, K] in 128-row tiles, B = the activations as one 16-row tile (rows past
+// M read as zeros), N = 16 per MMA; one CTA per 128 output features streams its weight rows
+// once, and the epilogue writes the result transposed back to [M, N].
+template <int EPI>
+static cudaError_t run_swapped(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st) {
+  using C = Cfg<16, kBfmtE4m3, EPI>;
+  auto kern = grouped_gemm_kernel<16, kBfmtE4m3, EPI>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  CUtensorMap tmA, tmB;
+  if (!make_map_u8(&tmA, a.w, a.K, a.N, 128, 128, true) ||
+      !make_map_u8(&tmB, a.aq, a.K, a.R, 128, 16, true)) {
+    *st = FGE_ERR_CUDA;
+    return cudaSuccess;
+  }
+  GemmParams p{};
+  p.sa_tensor = a.sa_tensor;
+  p.sa_rows = a.sa_rows;
+  p.sw_tensor = a.sw;
+  p.offsets = nullptr;
+  p.row_token = nullptr;
+  p.out = a.out;
+  p.status = a.status;
+  p.E = 1;
+  p.N = 16;
+  p.K = static_cast<int>(a.K);
+  p.G = static_cast<int>(a.K / 128);
+  p.dense_rows = static_cast<int>(a.N);
+  p.swap_m = static_cast<int>(a.R);
+  p.out_ld = static_cast<int>(a.N);
+  const int grid = static_cast<int>(std::max<long>(1, std::min<long>(num_sms(), (a.N + 127) / 128)));
+  kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(tmA, tmB, tmA, p);
+  *st = FGE_OK;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st) {
   const bool bn256 = (a.N % 256) == 0;
+  if (a.per_tensor && a.offsets == nullptr && a.row_token == nullptr && a.R <= 16)
+    return a.epilogue == 0 ? run_swapped<kEpiF32>(a, s, st) : run_swapped<kEpiBf16>(a, s, st);
   if (a.per_tensor) {
     if (a.epilogue == 0) return bn256 ? run<256, kBfmtE4m3, kEpiF32>(a, s, st) : run<128, kBfmtE4m3, kEpiF32>(a, s, st);
     return bn256 ? run<256, kBfmtE4m3, kEpiBf16>(a, s, st) : run<128, kBfmtE4m3, kEpiBf16>(a, s, st);

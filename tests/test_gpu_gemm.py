@@ -129,9 +129,11 @@ def test_linear_w8a8(fge, m):
     check_gemm(host(y), ref, absref, True)
 
 
-def test_gemm_w8a8_exact(fge):
-    rng = np.random.default_rng(51)
-    m, n, kdim = 200, 384, 512
+@pytest.mark.parametrize("m", [200, 1, 5, 16])
+def test_gemm_w8a8_exact(fge, m):
+    # m <= 16 runs the decode tile (weights on the 128-row side of the MMA, 16 token columns)
+    rng = np.random.default_rng(51 + m)
+    n, kdim = 384, 512
     a = rng.integers(-8, 9, size=(m, kdim)).astype(np.float32)
     w = rng.integers(-8, 9, size=(n, kdim)).astype(np.float32)
     aq, wq = oracle.e4m3_encode(a), oracle.e4m3_encode(w)
@@ -139,6 +141,22 @@ def test_gemm_w8a8_exact(fge):
     y = fge.gemm_w8a8(to_dev(aq), to_dev(np.array([sa])), to_dev(wq), to_dev(np.array([sw])),
                       out_dtype=torch.float32)
     ref = oracle.linear_w8a8_gemm(aq, sa, wq, sw)
+    assert np.array_equal(host(y).astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("m", [1, 7, 16, 17])
+def test_gemm_w8a8_rows_exact_decode_sizes(fge, m):
+    # per-row activation scales (powers of two) on the decode tile: exact in float32
+    rng = np.random.default_rng(77 + m)
+    n, kdim = 256, 384
+    a = rng.integers(-8, 9, size=(m, kdim)).astype(np.float32)
+    w = rng.integers(-8, 9, size=(n, kdim)).astype(np.float32)
+    aq, wq = oracle.e4m3_encode(a), oracle.e4m3_encode(w)
+    sa = (2.0 ** rng.integers(-6, 3, size=m)).astype(np.float32)
+    sw = np.float32(2.0 ** -5)
+    y = fge.gemm_w8a8_rows(to_dev(aq), to_dev(sa), to_dev(wq), to_dev(np.array([sw])),
+                           out_dtype=torch.float32)
+    ref = oracle.linear_w8a8_rows_gemm(aq, sa, wq, sw)
     assert np.array_equal(host(y).astype(np.float64), ref)
 
 
