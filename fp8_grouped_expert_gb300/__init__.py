@@ -427,6 +427,66 @@ def moe_layer_forward(logits, x, k, inter, w_gu_dev, s_gu_dev, w_dn_dev, s_dn_de
     return y
 
 
+class HostLayerPipeline:
+    """MoE layer calls from pinned host buffers to pinned host buffers, with the copies
+    overlapped with the layers: step i's inputs go up on one copy stream while step i-1
+    computes, and step i-1's output comes down on another while step i computes.  Two
+    device buffers per input and output alternate between steps; events order the three
+    streams.  Every step still moves its own inputs up and its own result down.
+
+    submit() enqueues one step and returns at once; finish() waits for every step."""
+
+    def __init__(self, tokens, hidden, experts, k, inter, w_gu_dev, s_gu_dev, w_dn_dev,
+                 s_dn_dev, fmt=W4_SUBNORMAL, out_dtype=torch.bfloat16, device=None):
+        dev = torch.device(device if device is not None else "cuda")
+        _ensure_init(dev)
+        self.k, self.inter, self.fmt, self.out_dtype = k, inter, fmt, out_dtype
+        self.banks = (w_gu_dev, s_gu_dev, w_dn_dev, s_dn_dev)
+        self.x = [torch.empty((tokens, hidden), dtype=torch.bfloat16, device=dev)
+                  for _ in range(2)]
+        self.logits = [torch.empty((tokens, experts), dtype=torch.float32, device=dev)
+                       for _ in range(2)]
+        self.out = [torch.empty((tokens, hidden), dtype=out_dtype, device=dev) for _ in range(2)]
+        self.ws = new_workspace(workspace_bytes(OP_MOE_LAYER, tokens, hidden, inter, experts, k),
+                                dev)
+        self.up = torch.cuda.Stream(dev)
+        self.compute = torch.cuda.Stream(dev)
+        self.down = torch.cuda.Stream(dev)
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        self.inputs_ready = [ev(), ev()]
+        self.layer_done = [ev(), ev()]
+        self.output_read = [ev(), ev()]
+        self.used = [False, False]
+        self.step = 0
+
+    def submit(self, x_pin, logits_pin, out_pin):
+        s = self.step % 2
+        if self.used[s]:  # the layer that read this slot's inputs has finished
+            self.up.wait_event(self.layer_done[s])
+        with torch.cuda.stream(self.up):
+            self.x[s].copy_(x_pin, non_blocking=True)
+            self.logits[s].copy_(logits_pin, non_blocking=True)
+            self.inputs_ready[s].record(self.up)
+        self.compute.wait_event(self.inputs_ready[s])
+        if self.used[s]:  # this slot's previous output has been copied down
+            self.compute.wait_event(self.output_read[s])
+        with torch.cuda.stream(self.compute):
+            moe_layer_forward(self.logits[s], self.x[s], self.k, self.inter, *self.banks,
+                              fmt=self.fmt, out_dtype=self.out_dtype, workspace=self.ws,
+                              out=self.out[s])
+            self.layer_done[s].record(self.compute)
+        self.down.wait_event(self.layer_done[s])
+        with torch.cuda.stream(self.down):
+            out_pin.copy_(self.out[s], non_blocking=True)
+            self.output_read[s].record(self.down)
+        self.used[s] = True
+        self.step += 1
+
+    def finish(self):
+        for st in (self.up, self.compute, self.down):
+            st.synchronize()
+
+
 def moe_layer_per_token_dispatch(logits, x, k, inter, w_gu, s_gu, w_dn, s_dn,
                                  out_dtype=torch.bfloat16, workspace=None, out=None):
     """Per-token int4 dispatch baseline (canonical, unprepacked int4 banks)."""
