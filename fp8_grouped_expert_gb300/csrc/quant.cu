@@ -10,32 +10,43 @@
 
 namespace fge {
 
-// One 128-value group per 16 lanes; each lane converts 8 bf16 (one 16-byte load).
+// One 128-value group per 16 lanes; each lane converts 8 bf16 (one 16-byte load).  A warp
+// takes kQuantUnroll pairs of groups per trip and issues all their loads first, so that each
+// lane keeps several 16-byte reads in flight (the kernel is bound by DRAM latency otherwise).
+constexpr int kQuantUnroll = 4;
 __global__ void quant_g128_kernel(const uint4* __restrict__ x, int64_t groups,
                                   uint2* __restrict__ xq, float* __restrict__ xs) {
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4, hl = lane & 15;
   const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t g0 = wid * 2; g0 < groups; g0 += nw * 2) {
-    const int64_t g = g0 + half;
-    const bool valid = g < groups;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (valid) v = __ldcs(x + g * 16 + hl);
-    float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                  bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-    float amax = 0.0f;
+  for (int64_t g0 = wid * 2; g0 < groups; g0 += nw * 2 * kQuantUnroll) {
+    uint4 v[kQuantUnroll];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const int64_t g = g0 + u * nw * 2 + half;
+      v[u] = g < groups ? __ldcs(x + g * 16 + hl) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
-    for (int d = 8; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
-    const float s = scale_from_amax(amax);
-    uint2 q;
-    q.x = cvt_e4m3x4(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
-    q.y = cvt_e4m3x4(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s), __fdiv_rn(f[7], s));
-    if (valid) {
-      xq[g * 16 + hl] = q;
-      if (hl == 0) xs[g] = s;
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const int64_t g = g0 + u * nw * 2 + half;
+      const float f[8] = {bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y),
+                          bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w)};
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+      for (int d = 8; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+      const float s = scale_from_amax(amax);
+      uint2 q;
+      q.x = cvt_e4m3x4(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s),
+                       __fdiv_rn(f[3], s));
+      q.y = cvt_e4m3x4(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s),
+                       __fdiv_rn(f[7], s));
+      if (g < groups) {
+        xq[g * 16 + hl] = q;
+        if (hl == 0) xs[g] = s;
+      }
     }
   }
 }
@@ -133,31 +144,38 @@ __global__ void mx_e2m1_kernel(const uint4* __restrict__ x, int64_t n8, uint32_t
   const int lane = threadIdx.x & 31;
   const int64_t t0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t w0 = t0 - lane; w0 < n8; w0 += stride) {  // warp-uniform trip count
-    const int64_t c = w0 + lane;
-    const bool valid = c < n8;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (valid) v = __ldcs(x + c);
-    const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                        bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-    float amax = 0.0f;
+  // warp-uniform trip count; kQuantUnroll independent 16-byte loads per lane per trip
+  for (int64_t w0 = t0 - lane; w0 < n8; w0 += stride * kQuantUnroll) {
+    uint4 v[kQuantUnroll];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    // floor(log2(amax)) is the exponent field minus 127 for a normal amax; a zero or
-    // subnormal amax lands on the clamp
-    const int ef = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
-    const int e = max(ef - 129, -127);
-    const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-E
-    uint32_t q = 0;
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const int64_t c = w0 + u * stride + lane;
+      v[u] = c < n8 ? __ldcs(x + c) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      q |= (static_cast<uint32_t>(__nv_cvt_float_to_fp4(f[i] * inv, __NV_E2M1,
-                                                        cudaRoundNearest)) & 0xFu) << (4 * i);
-    if (valid) {
-      xq[c] = q;
-      if ((lane & 3) == 0) xs[c >> 2] = static_cast<uint8_t>(e + 127);
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const int64_t c = w0 + u * stride + lane;
+      const float f[8] = {bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y),
+                          bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w)};
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      // floor(log2(amax)) is the exponent field minus 127 for a normal amax; a zero or
+      // subnormal amax lands on the clamp
+      const int ef = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+      const int e = max(ef - 129, -127);
+      const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-E
+      uint32_t q = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        q |= (static_cast<uint32_t>(__nv_cvt_float_to_fp4(f[i] * inv, __NV_E2M1,
+                                                          cudaRoundNearest)) & 0xFu) << (4 * i);
+      if (c < n8) {
+        xq[c] = q;
+        if ((lane & 3) == 0) xs[c >> 2] = static_cast<uint8_t>(e + 127);
+      }
     }
   }
 }
@@ -166,7 +184,8 @@ cudaError_t launch_mx_quant_e2m1(const uint16_t* x, int64_t M, int64_t K, uint8_
                                  uint8_t* xs, cudaStream_t s) {
   const int64_t n8 = M * (K / 8);
   if (n8 == 0) return cudaSuccess;
-  const int grid = static_cast<int>(std::min<int64_t>((n8 + 255) / 256, num_sms() * 8));
+  const int grid = static_cast<int>(
+      std::min<int64_t>((n8 + 256 * kQuantUnroll - 1) / (256 * kQuantUnroll), num_sms() * 8));
   mx_e2m1_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), n8,
                                       reinterpret_cast<uint32_t*>(xq), xs);
   return cudaGetLastError();
@@ -185,7 +204,7 @@ cudaError_t launch_quant_g128(const uint16_t* x, int64_t M, int64_t K, uint8_t* 
                               cudaStream_t s) {
   const int64_t groups = M * (K / 128);
   if (groups == 0) return cudaSuccess;
-  const int64_t warps = (groups + 1) / 2;
+  const int64_t warps = (groups + 2 * kQuantUnroll - 1) / (2 * kQuantUnroll);
   const int grid = static_cast<int>(std::min<int64_t>((warps + 7) / 8, num_sms() * 8));
   quant_g128_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), groups,
                                          reinterpret_cast<uint2*>(xq), xs);

@@ -267,29 +267,39 @@ __global__ void permute_quant_copy_kernel(const uint4* __restrict__ x, int64_t T
   const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int64_t G = H / 128;
+  constexpr int U = 4;  // group pairs per trip: their loads are issued together
   for (int64_t t = wid; t < T; t += nw) {
     const int my_row = lane < k ? __ldg(token_row + t * k + lane) : 0;
-    for (int64_t g0 = 0; g0 < G; g0 += 2) {  // all lanes iterate; shuffles stay full
-      const int64_t g = g0 + half;
-      const bool in = g < G;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (in) v = __ldcs(x + (t * G + g) * 16 + hl);
-      float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                    bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-      float amax = 0.0f;
+    for (int64_t g0 = 0; g0 < G; g0 += 2 * U) {  // all lanes iterate; shuffles stay full
+      uint4 v[U];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+      for (int u = 0; u < U; ++u) {
+        const int64_t g = g0 + 2 * u + half;
+        v[u] = g < G ? __ldcs(x + (t * G + g) * 16 + hl) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-      for (int d = 8; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
-      const float sc = scale_from_amax(amax);
-      uint2 q;
-      q.x = cvt_e4m3x4(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc), __fdiv_rn(f[2], sc), __fdiv_rn(f[3], sc));
-      q.y = cvt_e4m3x4(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc), __fdiv_rn(f[6], sc), __fdiv_rn(f[7], sc));
-      for (int j = 0; j < k; ++j) {
-        const int64_t r = __shfl_sync(0xffffffffu, my_row, j);
-        if (in) {
-          reinterpret_cast<uint2*>(aq + r * H)[g * 16 + hl] = q;
-          if (hl == 0) as[r * G + g] = sc;
+      for (int u = 0; u < U; ++u) {
+        const int64_t g = g0 + 2 * u + half;
+        const bool in = g < G;
+        const float f[8] = {bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y),
+                            bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w)};
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+        for (int d = 8; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+        const float sc = scale_from_amax(amax);
+        uint2 q;
+        q.x = cvt_e4m3x4(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc), __fdiv_rn(f[2], sc),
+                         __fdiv_rn(f[3], sc));
+        q.y = cvt_e4m3x4(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc), __fdiv_rn(f[6], sc),
+                         __fdiv_rn(f[7], sc));
+        for (int j = 0; j < k; ++j) {
+          const int64_t r = __shfl_sync(0xffffffffu, my_row, j);
+          if (in) {
+            reinterpret_cast<uint2*>(aq + r * H)[g * 16 + hl] = q;
+            if (hl == 0) as[r * G + g] = sc;
+          }
         }
       }
     }
