@@ -37,6 +37,7 @@ KNOWN_GATE_UP_TRAFFIC = {
     "3588543b1f588e0c:8f75c66d2d1b5e12": 194.63e6,
     "6c7fc4a2718cae64:72b05a4e51127510": 194.80e6,
     "4f87322000f2dbb1:72b05a4e51127510": 195.78e6,
+    "43dbc4055150c350:72b05a4e51127510": 194.80e6,
 }
 
 
