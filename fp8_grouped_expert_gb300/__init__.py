@@ -434,10 +434,13 @@ class HostLayerPipeline:
     device buffers per input and output alternate between steps; events order the three
     streams.  Every step still moves its own inputs up and its own result down.
 
-    submit() enqueues one step and returns at once; finish() waits for every step."""
+    submit() enqueues one step and returns at once; finish() waits for every step.  With
+    graphs=True (the default) the layer call of each slot is captured once as a CUDA graph
+    and replayed, so its 9 kernels launch without host gaps."""
 
     def __init__(self, tokens, hidden, experts, k, inter, w_gu_dev, s_gu_dev, w_dn_dev,
-                 s_dn_dev, fmt=W4_SUBNORMAL, out_dtype=torch.bfloat16, device=None):
+                 s_dn_dev, fmt=W4_SUBNORMAL, out_dtype=torch.bfloat16, device=None,
+                 graphs=True):
         dev = torch.device(device if device is not None else "cuda")
         _ensure_init(dev)
         self.k, self.inter, self.fmt, self.out_dtype = k, inter, fmt, out_dtype
@@ -458,6 +461,24 @@ class HostLayerPipeline:
         self.output_read = [ev(), ev()]
         self.used = [False, False]
         self.step = 0
+        self.graphs = None
+        if graphs:
+            for t in self.x + self.logits:
+                t.zero_()
+            self._layer(0)  # first call outside capture: one-time kernel attributes
+            torch.cuda.synchronize(dev)
+            self.graphs = []
+            for slot in range(2):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    self._layer(slot)
+                self.graphs.append(g)
+            torch.cuda.synchronize(dev)
+
+    def _layer(self, slot):
+        moe_layer_forward(self.logits[slot], self.x[slot], self.k, self.inter, *self.banks,
+                          fmt=self.fmt, out_dtype=self.out_dtype, workspace=self.ws,
+                          out=self.out[slot])
 
     def submit(self, x_pin, logits_pin, out_pin):
         s = self.step % 2
@@ -471,9 +492,10 @@ class HostLayerPipeline:
         if self.used[s]:  # this slot's previous output has been copied down
             self.compute.wait_event(self.output_read[s])
         with torch.cuda.stream(self.compute):
-            moe_layer_forward(self.logits[s], self.x[s], self.k, self.inter, *self.banks,
-                              fmt=self.fmt, out_dtype=self.out_dtype, workspace=self.ws,
-                              out=self.out[s])
+            if self.graphs is not None:
+                self.graphs[s].replay()
+            else:
+                self._layer(s)
             self.layer_done[s].record(self.compute)
         self.down.wait_event(self.layer_done[s])
         with torch.cuda.stream(self.down):

@@ -62,7 +62,7 @@ def test_full_size_layer_sampled(fge, name, sample):
 def test_host_pipeline_matches_layer_calls(fge):
     """HostLayerPipeline: three steps with different inputs, from pinned host buffers to
     pinned host buffers with the copies overlapped, equal the plain layer calls bit for bit
-    (same kernels; the slots alternate between steps)."""
+    (same kernels; the slots alternate between steps), with and without CUDA graphs."""
     inp = moe_inputs("tiny", seed=5)
     w_gu, s_gu = fge.w4_prepack(to_dev(inp.w_gu), to_dev(inp.s_gu), gate_up_interleave=True)
     w_dn, s_dn = fge.w4_prepack(to_dev(inp.w_dn), to_dev(inp.s_dn))
@@ -76,9 +76,13 @@ def test_host_pipeline_matches_layer_calls(fge):
         lgs.append(lg.cpu().pin_memory())
         outs.append(torch.empty((inp.T, inp.H), dtype=torch.bfloat16).pin_memory())
     torch.cuda.synchronize()
-    pipe = fge.HostLayerPipeline(inp.T, inp.H, inp.E, inp.k, inp.I, w_gu, s_gu, w_dn, s_dn)
-    for i in range(3):
-        pipe.submit(xs[i], lgs[i], outs[i])
-    pipe.finish()
-    for i in range(3):
-        np.testing.assert_array_equal(outs[i].float().numpy(), refs[i])
+    for graphs in (False, True):
+        pipe = fge.HostLayerPipeline(inp.T, inp.H, inp.E, inp.k, inp.I, w_gu, s_gu, w_dn, s_dn,
+                                     graphs=graphs)
+        for o in outs:
+            o.zero_()
+        for i in range(3):
+            pipe.submit(xs[i], lgs[i], outs[i])
+        pipe.finish()
+        for i in range(3):
+            np.testing.assert_array_equal(outs[i].float().numpy(), refs[i])
