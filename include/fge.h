@@ -225,6 +225,10 @@ fge_status fge_moe_combine(const void* y, fge_dtype y_dtype, const int32_t* toke
  * ("feat(qwen4_exp) ..." section "What this adds"; "Module fp8_ffi": activation scale
  * folded with the weight scale into one device scalar):  y = (sa * sw) * aq @ wq^T.
  * aq: [M, K] e4m3; sa, sw: device float scalars; wq: [N, K] e4m3; y: [M, N] in out_dtype.
+ * At decode sizes (M <= 16; also in fge_gemm_w8a8_rows, fge_linear_w8a8* and the
+ * allocation-free call) the kernel swaps its operands: the weights fill the 128-row side of
+ * the MMA and the activations one 16-row tile, and y is written transposed back to [M, N];
+ * the arithmetic and the result are the same.
  * Workspace: FGE_OP_GROUPED_GEMM. */
 fge_status fge_gemm_w8a8(const uint8_t* aq, const float* sa, int64_t M, int64_t K,
                          const uint8_t* wq, const float* sw, int64_t N, fge_dtype out_dtype,
