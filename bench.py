@@ -299,11 +299,29 @@ def run_gpu(args):
     # ---- the per-token int4 dispatch that the grouped GEMM replaces (context, untimed)
     base_ms = None
     if not args.no_baseline:
-        fge.moe_layer_per_token_dispatch(logits, x, inp.k, inp.I, *canon)
+        # launched the same way as the timed steps (a replayed CUDA graph unless --no-graph)
+        dout = torch.empty((inp.T, inp.H), dtype=torch.bfloat16, device=dev)
+        dws = fge.new_workspace(fge.workspace_bytes(fge.OP_DISPATCH_BASELINE, inp.T, inp.H,
+                                                    inp.I, inp.E, inp.k), dev)
+
+        def dispatch():
+            fge.moe_layer_per_token_dispatch(logits, x, inp.k, inp.I, *canon, workspace=dws,
+                                             out=dout)
+
+        dispatch()
+        torch.cuda.synchronize()
+        run_dispatch = dispatch
+        if not args.no_graph:
+            dgraph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(dgraph):
+                dispatch()
+            run_dispatch = dgraph.replay
+            run_dispatch()
+            torch.cuda.synchronize()
         b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         b0.record(stream)
         for _ in range(2):
-            fge.moe_layer_per_token_dispatch(logits, x, inp.k, inp.I, *canon)
+            run_dispatch()
         b1.record(stream)
         torch.cuda.synchronize()
         base_ms = b0.elapsed_time(b1) / 2
