@@ -138,26 +138,26 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------- CPU oracle
+# The timed oracle is the single-threaded C++ one (oracle/oracle_ref.cpp): one host core.
+ORACLE_CORES = 1
+
+
 def oracle_tokens_per_s(inp, sample_tokens, seconds, seed=0):
-    """Time the CPU oracle on repeated samples of `sample_tokens` tokens for ~`seconds`."""
-    import oracle
+    """Time the single-threaded C++ CPU oracle on repeated samples of `sample_tokens` tokens
+    (each a whole layer call: gate, quant, permute, both GEMMs, SwiGLU, combine) for
+    ~`seconds`."""
+    from oracle import native
+    native.build()
     rng = np.random.default_rng(seed)
     done, t0 = 0, time.perf_counter()
     while True:
         rows = np.sort(rng.choice(inp.T, size=sample_tokens, replace=False))
-        oracle.moe_layer_forward(inp.logits[rows], inp.x[rows], inp.k, inp.w_gu, inp.s_gu,
+        native.moe_layer_forward(inp.logits[rows], inp.x[rows], inp.k, inp.w_gu, inp.s_gu,
                                  inp.w_dn, inp.s_dn, inp.I, out_dtype=inp.out)
         done += sample_tokens
         el = time.perf_counter() - t0
         if el >= seconds:
             return done / el, done, el
-
-
-def _blas_threads():
-    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
-        if os.environ.get(var):
-            return int(os.environ[var])
-    return os.cpu_count()
 
 
 def run_reference(args):
@@ -176,14 +176,14 @@ def run_reference(args):
         times.append(time.perf_counter() - t0)
     ms = 1e3 * sum(times) / len(times)
     value = sample / (ms / 1e3)
-    cores = _blas_threads()
+    cores = ORACLE_CORES
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": _config(inp, note="each step: the float64 CPU oracle on %d sampled tokens"
-                          % sample),
+        "config": _config(inp, note="each step: the single-threaded float64 C++ CPU oracle on "
+                                    "%d sampled tokens" % sample),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": "%d random tokens of the T=%d layer per step"
                                    % (sample, inp.T)},
@@ -362,7 +362,7 @@ def run_gpu(args):
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         rate, done, el = oracle_tokens_per_s(inp, 64, args.cpu_seconds)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+        cpu = {"value": rate, "unit": "tokens/s", "cores": ORACLE_CORES, "kind": "oracle",
                "sample": "%d tokens (random 64-token samples of the T=%d layer) in %.1f s"
                          % (done, inp.T, el)}
     line = {

@@ -11,7 +11,14 @@ vs INT4 comparison).  Each function cites the passage it follows and lists the r
 takes where the pages are silent.  numpy matmul is the only library primitive used for a
 contraction; every quantization, rounding and ordering rule is written out here.
 
-It shares no code with the CUDA path (``fp8_grouped_expert_gb300``): the two meet only in
+Two restatements live here, written separately and sharing no code: this numpy package
+(float64, numpy matmul as the one library primitive for a contraction) and a plain,
+single-threaded C++ one (``oracle_ref.cpp``, bound by ``oracle.native`` through ctypes and
+compiled with g++ by ``oracle.native.build()``) whose layer call is also the timed CPU
+baseline.  Where a rule can be written two ways they take different routes, and the tests
+hold them to each other as well as to the pins below.
+
+Neither shares code with the CUDA path (``fp8_grouped_expert_gb300``): oracle and library meet only in
 the seeded input generators of ``workloads``, which hold none of the method's arithmetic.
 
 Pins (tests marked ``not gpu``) tie each function to facts the pages and the mathematics

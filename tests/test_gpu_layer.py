@@ -10,6 +10,7 @@ import pytest
 import torch
 
 import oracle
+from oracle import native
 from util import bf16_dev, cosine, host, to_dev
 from workloads import moe_inputs
 
@@ -42,6 +43,10 @@ def test_tiny_layer(fge, fmt_name):
     assert cosine(got, ref) >= 0.9999
     rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
     assert rel < 5e-3, rel
+    # the single-threaded C++ oracle restates the same layer independently
+    ref_c = native.moe_layer_forward(inp.logits, inp.x, inp.k, inp.w_gu, inp.s_gu, inp.w_dn,
+                                     inp.s_dn, inp.I, out_dtype=inp.out)
+    assert cosine(got, ref_c) >= 0.9999
 
 
 @pytest.mark.parametrize("name,sample", [("mid", 384), ("large", 160)])
