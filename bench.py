@@ -441,15 +441,24 @@ def stage_times(fge, torch, inp, x, logits, w_gu, s_gu, w_dn, s_dn, fmt, flush, 
         acc.setdefault(name, []).append((a, b))
         return res
 
+    # the GEMMs write into buffers allocated here, so that each GEMM stage times the kernel
+    # alone (no zero fill of its output inside the timed region)
+    r = inp.T * inp.k
+    ws = fge.new_workspace(fge.workspace_bytes(fge.OP_GROUPED_GEMM), dev)
+    hq = torch.empty((r, inp.I), dtype=torch.uint8, device=dev)
+    hs = torch.empty((r, inp.I // 128), dtype=torch.float32, device=dev)
+    y = torch.empty((r, inp.H), dtype=torch.bfloat16, device=dev)
     out = None
     for _ in range(steps + 1):
         ids, gates = timed("topk_gate", lambda: fge.moe_topk_gate(logits, inp.k))
         xq, xs = timed("quant_g128", lambda: fge.fp8_quant_act(x, "g128"))
         p = timed("permute", lambda: fge.moe_permute(ids, inp.E, xq, xs))
-        hq, hs = timed("gate_up_gemm", lambda: fge.grouped_gemm_w4a8(
-            p["aq"], p["as_"], p["offsets"], w_gu, s_gu, fmt=fmt, epilogue="swiglu"))
-        y = timed("down_gemm", lambda: fge.grouped_gemm_w4a8(
-            hq, hs, p["offsets"], w_dn, s_dn, fmt=fmt, out_dtype=torch.bfloat16))
+        timed("gate_up_gemm", lambda: fge.grouped_gemm_w4a8(
+            p["aq"], p["as_"], p["offsets"], w_gu, s_gu, fmt=fmt, epilogue="swiglu",
+            workspace=ws, out=hq, scales=hs))
+        timed("down_gemm", lambda: fge.grouped_gemm_w4a8(
+            hq, hs, p["offsets"], w_dn, s_dn, fmt=fmt, out_dtype=torch.bfloat16, workspace=ws,
+            out=y))
         out = timed("combine", lambda: fge.moe_combine(y, p["token_row"], gates))
     torch.cuda.synchronize()
     # the first pass includes allocator warm-up; drop it

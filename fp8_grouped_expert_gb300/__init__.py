@@ -263,8 +263,11 @@ def w4_prepack(w_packed, w_scale, gate_up_interleave=False, fmt=W4_SUBNORMAL):
 
 
 def grouped_gemm_w4a8(aq, as_, offsets, w_dev, s_dev, fmt=W4_SUBNORMAL, epilogue="store",
-                      out_dtype=torch.float32, workspace=None):
-    """Grouped W4A8 GEMM; epilogue 'store' -> out [R, N]; 'swiglu' -> (hq [R, N/2], hs)."""
+                      out_dtype=torch.float32, workspace=None, out=None, scales=None):
+    """Grouped W4A8 GEMM; epilogue 'store' -> out [R, N]; 'swiglu' -> (hq [R, N/2], hs).
+
+    out (and, for 'swiglu', scales) may be passed preallocated; rows past offsets[E] are
+    then left as they were.  Otherwise they are allocated zero-filled."""
     _need(aq, torch.uint8, "aq")
     _need(as_, torch.float32, "as_")
     _need(offsets, torch.int32, "offsets")
@@ -275,11 +278,21 @@ def grouped_gemm_w4a8(aq, as_, offsets, w_dev, s_dev, fmt=W4_SUBNORMAL, epilogue
     ws = workspace if workspace is not None else new_workspace(
         workspace_bytes(OP_GROUPED_GEMM), dev)
     if epilogue == "swiglu":
-        out = torch.zeros((r, n // 2), dtype=torch.uint8, device=dev)
-        scales = torch.zeros((r, n // 256), dtype=torch.float32, device=dev)
+        if out is None:
+            out = torch.zeros((r, n // 2), dtype=torch.uint8, device=dev)
+        if scales is None:
+            scales = torch.zeros((r, n // 256), dtype=torch.float32, device=dev)
+        _need(out, torch.uint8, "out")
+        _need(scales, torch.float32, "scales")
+        if tuple(out.shape) != (r, n // 2) or tuple(scales.shape) != (r, n // 256):
+            raise FgeError("out/scales must be [R, N/2] / [R, N/256]")
         epi, od = EPI_SWIGLU_REQUANT, DTYPE_BF16
     else:
-        out = torch.zeros((r, n), dtype=out_dtype, device=dev)
+        if out is None:
+            out = torch.zeros((r, n), dtype=out_dtype, device=dev)
+        _need(out, out_dtype, "out")
+        if tuple(out.shape) != (r, n):
+            raise FgeError("out must be [R, N]")
         scales = None
         epi = EPI_STORE
         od = DTYPE_F32 if out_dtype == torch.float32 else DTYPE_BF16
