@@ -86,8 +86,8 @@ struct Cfg {
   static constexpr int kOffMtp = kOffOffs + (kMaxExperts + 1) * 4;
   static constexpr int kOffRed = align16(kOffMtp + (kMaxExperts + 1) * 4);
   static constexpr int kOffRT = align16(kOffRed + 2 * 2 * 128 * 4);  // gather: tile row ids
-  // bf16 and SwiGLU store epilogues (group mode): per warpgroup one 8 KB buffer staging 128
-  // rows x 64 bytes for a TMA tile store (64-byte swizzle)
+  // bf16 and SwiGLU store epilogues (group mode): per warpgroup one 8 KB buffer, a 2 KB
+  // slice per warp staging that warp's 32 rows for its own TMA tile stores
   static constexpr bool kStageOut = kGroupScale && (EPI == kEpiBf16 || EPI == kEpiSwiglu);
   static constexpr int kOffST = (kOffRT + 128 * 4 + 1023) / 1024 * 1024;
   static constexpr int kSTBytes = kStageOut ? 2 * 8192 : 0;
@@ -628,19 +628,18 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
                                 hv[i + 14] * inv_s, hv[i + 15] * inv_s);
           }
           if (C::kStageOut && ti.rows == 128) {
-            // full tile: the warpgroup's 128 rows x 64 codes go out as one TMA tile store
-            // from an 8 KB shared buffer (64-byte swizzle, as for the bf16 store)
-            uint8_t* buf = smem + C::kOffST + wg * 8192;
-            const bool issuer = q == 0 && lane == 0;
-            if (issuer) bulk_wait_read0();
-            asm volatile("bar.sync %0, 128;" ::"r"(2 + wg) : "memory");
+            // full tile: each warp's 32 rows x 64 codes go out as one TMA tile store from
+            // the warp's own 2 KB slice (64-byte swizzle), with no barrier across warps
+            uint8_t* buf = smem + C::kOffST + wg * 8192 + q * 2048;
+            if (lane == 0) bulk_wait_read0();  // this warp's previous store has left the slice
+            __syncwarp();
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-              *reinterpret_cast<uint4*>(buf + r_in * 64 + ((c ^ ((r_in >> 1) & 3)) << 4)) = o[c];
+              *reinterpret_cast<uint4*>(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = o[c];
             fence_proxy_async_smem();
-            asm volatile("bar.sync %0, 128;" ::"r"(2 + wg) : "memory");
-            if (issuer) {
-              tma_store_2d(&tmY, smem_u32(buf), ti.n0 / 2 + wg * 64, ti.row0);
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmY, smem_u32(buf), ti.n0 / 2 + wg * 64, ti.row0 + q * 32);
               bulk_commit();
             }
           } else if (valid) {
@@ -652,28 +651,33 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
           if (valid && wg == 0)
             p.out_scales[static_cast<size_t>(row) * (inter / 128) + ti.n0 / 256] = s;
         } else if (C::kStageOut && ti.rows == 128) {
-          // full tile, bf16: each warpgroup stages its 128 columns in four 32-column chunks
-          // (row r at r * 64 bytes, 16-byte pieces swizzled by (r / 2) % 4 as the tensor map's
-          // 64-byte swizzle expects) and one thread stores each chunk with a TMA tile store
-          uint8_t* buf = smem + C::kOffST + wg * 8192;
-          const bool issuer = q == 0 && lane == 0;
+          // full tile, bf16: each warp stores its 32 rows in eight 16-column chunks from its
+          // own 2 KB slice, two 1 KB halves used in turn (row r at r * 32 bytes, 16-byte
+          // pieces swizzled by (r / 4) % 2 as the tensor map's 32-byte swizzle expects), so
+          // a chunk is staged while the previous one is still being read; no barrier across
+          // warps
+          uint8_t* slice = smem + C::kOffST + wg * 8192 + q * 2048;
+          const int swz = (lane >> 2) & 1;
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            if (issuer) bulk_wait_read0();  // the previous chunk has left the buffer
-            asm volatile("bar.sync %0, 128;" ::"r"(2 + wg) : "memory");
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int j = ch * 16 + c * 4;
-              const uint4 v = make_uint4(pack_bf16x2(lo_f32(acc2[j]), hi_f32(acc2[j])),
-                                         pack_bf16x2(lo_f32(acc2[j + 1]), hi_f32(acc2[j + 1])),
-                                         pack_bf16x2(lo_f32(acc2[j + 2]), hi_f32(acc2[j + 2])),
-                                         pack_bf16x2(lo_f32(acc2[j + 3]), hi_f32(acc2[j + 3])));
-              *reinterpret_cast<uint4*>(buf + r_in * 64 + ((c ^ ((r_in >> 1) & 3)) << 4)) = v;
-            }
+          for (int ch = 0; ch < 8; ++ch) {
+            uint8_t* buf = slice + (ch & 1) * 1024;
+            if (lane == 0) bulk_wait_read1();  // the store two chunks back has left this half
+            __syncwarp();
+            const int j = ch * 8;  // acc2[j..j+7]: columns 16 ch .. 16 ch + 15
+            const uint4 v0 = make_uint4(pack_bf16x2(lo_f32(acc2[j]), hi_f32(acc2[j])),
+                                        pack_bf16x2(lo_f32(acc2[j + 1]), hi_f32(acc2[j + 1])),
+                                        pack_bf16x2(lo_f32(acc2[j + 2]), hi_f32(acc2[j + 2])),
+                                        pack_bf16x2(lo_f32(acc2[j + 3]), hi_f32(acc2[j + 3])));
+            const uint4 v1 = make_uint4(pack_bf16x2(lo_f32(acc2[j + 4]), hi_f32(acc2[j + 4])),
+                                        pack_bf16x2(lo_f32(acc2[j + 5]), hi_f32(acc2[j + 5])),
+                                        pack_bf16x2(lo_f32(acc2[j + 6]), hi_f32(acc2[j + 6])),
+                                        pack_bf16x2(lo_f32(acc2[j + 7]), hi_f32(acc2[j + 7])));
+            *reinterpret_cast<uint4*>(buf + lane * 32 + (swz << 4)) = v0;
+            *reinterpret_cast<uint4*>(buf + lane * 32 + ((swz ^ 1) << 4)) = v1;
             fence_proxy_async_smem();
-            asm volatile("bar.sync %0, 128;" ::"r"(2 + wg) : "memory");
-            if (issuer) {
-              tma_store_2d(&tmY, smem_u32(buf), ti.n0 + col_a + ch * 32, ti.row0);
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmY, smem_u32(buf), ti.n0 + col_a + ch * 16, ti.row0 + q * 32);
               bulk_commit();
             }
           }
@@ -782,7 +786,7 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
       }
     }
     if constexpr (C::kStageOut) {
-      if (q == 0 && lane == 0) bulk_wait0();  // every staged tile store has completed
+      if (lane == 0) bulk_wait0();  // every tile store this warp issued has completed
     }
   }
 
@@ -828,14 +832,14 @@ static bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64
   return r == CUDA_SUCCESS;
 }
 
-// Output map of the staged SwiGLU store: [rows, inner] bytes, boxes of 64 bytes x 128 rows
-// with the 64-byte swizzle.
+// Output map of the staged SwiGLU store: [rows, inner] bytes, boxes of 64 bytes x 32 rows
+// (one warp's rows) with the 64-byte swizzle.
 static bool make_map_u8_swz64(CUtensorMap* m, void* base, uint64_t inner, uint64_t rows) {
   auto fn = get_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {inner};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, 32};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
@@ -843,17 +847,17 @@ static bool make_map_u8_swz64(CUtensorMap* m, void* base, uint64_t inner, uint64
   return r == CUDA_SUCCESS;
 }
 
-// Output map of the staged bf16 store: [rows, N] bf16, boxes of 32 columns x 128 rows with the
-// 64-byte swizzle.
+// Output map of the staged bf16 store: [rows, N] bf16, boxes of 16 columns x 32 rows (one
+// warp's chunk) with the 32-byte swizzle.
 static bool make_map_bf16_out(CUtensorMap* m, void* base, uint64_t n, uint64_t rows) {
   auto fn = get_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {n, rows};
   cuuint64_t strides[1] = {n * 2};
-  cuuint32_t box[2] = {32, 128};
+  cuuint32_t box[2] = {16, 32};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -922,7 +926,7 @@ static cudaError_t run(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st)
   CUtensorMap tmY = tmA;  // unused unless the store is staged
   bool okY = true;
   if constexpr (C::kStageOut) {
-    if (EPI == kEpiSwiglu)  // hq: [rows, N/2] e4m3 codes, 64-byte x 128-row boxes
+    if (EPI == kEpiSwiglu)  // hq: [rows, N/2] e4m3 codes, 64-byte x 32-row boxes (one warp)
       okY = make_map_u8_swz64(&tmY, a.out, a.N / 2, a.R);
     else
       okY = make_map_bf16_out(&tmY, a.out, a.N, a.R);
