@@ -68,6 +68,13 @@ def lib():
             "fo_linear_w8a8_gemm": (None, [u8p, f32p, f32, u8p, f32, i64, i64, i64, f64p]),
             "fo_moe_layer_forward": (i32, [f32p, f32p, i64, i64, i32, i32, i64, u8p, f32p, u8p,
                                            f32p, i32, f32p]),
+            "fo_mx_quant_e2m1": (None, [f32p, i64, i64, u8p, u8p]),
+            "fo_rmsnorm": (None, [f32p, i64, i64, f32p]),
+            "fo_router_logits": (None, [f32p, f32p, i64, i64, i32, f32p]),
+            "fo_identity_attention": (None, [f32p, i64, i32, i32, f32p]),
+            "fo_linear_w8a8": (None, [f32p, i64, i64, u8p, f32, i64, i32, f32p]),
+            "fo_moe_layer_int4_baseline": (None, [f32p, f32p, i64, i64, i32, i32, i64, u8p,
+                                                  f32p, u8p, f32p, i32, f32p]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(_lib, name)
@@ -223,3 +230,86 @@ def moe_layer_forward(logits, x_f32, k, w_gate_up, s_gate_up, w_down, s_down, in
                                _p(wdn, u), _p(sdn, f), 1 if out_dtype == "f32" else 0,
                                _p(out, f))
     return out
+
+
+def mx_quant_e2m1(x):
+    """MXFP4: (codes uint8 [M, K/2], element 2b in the low nibble; scales uint8 [M, K/32])."""
+    x = _c(x, np.float32)
+    m, k = x.shape
+    packed = np.zeros((m, k // 2), np.uint8)
+    scales = np.empty((m, k // 32), np.uint8)
+    lib().fo_mx_quant_e2m1(_p(x, ctypes.c_float), m, k, _p(packed, ctypes.c_uint8),
+                           _p(scales, ctypes.c_uint8))
+    return packed, scales
+
+
+def rmsnorm(h):
+    h = _c(h, np.float32)
+    out = np.empty_like(h)
+    lib().fo_rmsnorm(_p(h, ctypes.c_float), h.shape[0], h.shape[1], _p(out, ctypes.c_float))
+    return out
+
+
+def router_logits(xn, w_router):
+    xn = _c(xn, np.float32)
+    w = _c(w_router, np.float32)
+    out = np.empty((xn.shape[0], w.shape[0]), np.float32)
+    lib().fo_router_logits(_p(xn, ctypes.c_float), _p(w, ctypes.c_float), xn.shape[0],
+                           xn.shape[1], w.shape[0], _p(out, ctypes.c_float))
+    return out
+
+
+def identity_attention(v, n_heads, n_kv_heads):
+    v = _c(v, np.float32)
+    out = np.empty((v.shape[0], n_heads * 128), np.float32)
+    lib().fo_identity_attention(_p(v, ctypes.c_float), v.shape[0], n_heads, n_kv_heads,
+                                _p(out, ctypes.c_float))
+    return out
+
+
+def linear_w8a8(x_f32, wq, sw, rows=False):
+    """Dense projection (per-tensor or row-wise activation scales), bf16 values as float32."""
+    x = _c(x_f32, np.float32)
+    wq = _c(wq, np.uint8)
+    out = np.empty((x.shape[0], wq.shape[0]), np.float32)
+    lib().fo_linear_w8a8(_p(x, ctypes.c_float), x.shape[0], x.shape[1], _p(wq, ctypes.c_uint8),
+                         float(np.float32(sw)), wq.shape[0], 1 if rows else 0,
+                         _p(out, ctypes.c_float))
+    return out
+
+
+def moe_layer_int4_baseline(logits, x_f32, k, w_gate_up, s_gate_up, w_down, s_down, inter,
+                            out_dtype="bf16"):
+    """Per-token int4 expert dispatch in float64, token by token; float32 [T, H]."""
+    lg = _c(logits, np.float32)
+    x = _c(x_f32, np.float32)
+    wgu, sgu = _c(w_gate_up, np.uint8), _c(s_gate_up, np.float32)
+    wdn, sdn = _c(w_down, np.uint8), _c(s_down, np.float32)
+    t, h = x.shape
+    out = np.empty((t, h), np.float32)
+    f, u = ctypes.c_float, ctypes.c_uint8
+    lib().fo_moe_layer_int4_baseline(_p(lg, f), _p(x, f), t, h, wgu.shape[0], k, inter,
+                                     _p(wgu, u), _p(sgu, f), _p(wdn, u), _p(sdn, f),
+                                     1 if out_dtype == "f32" else 0, _p(out, f))
+    return out
+
+
+def stacked_prefill(h0, layers, k, inter, n_heads, n_kv_heads):
+    """The stacked prefill layers, each step a C++ call (same layer order and readings as the
+    numpy ``stacked_prefill``): xn = RMSNorm(h); v = W8A8(xn); attn = identity(v);
+    h += W8A8(attn); xn2 = RMSNorm(h); logits = router(xn2); h += MoE(xn2), h in float32.
+    Returns (h float32 [T, H], list of per-layer routing ids)."""
+    h = np.asarray(h0, dtype=np.float32).copy()
+    routes = []
+    for lw in layers:
+        xn = rmsnorm(h)
+        v = linear_w8a8(xn, lw["wv"], lw["sv"])
+        o = linear_w8a8(identity_attention(v, n_heads, n_kv_heads), lw["wo"], lw["so"])
+        h = (h.astype(np.float64) + o.astype(np.float64)).astype(np.float32)
+        xn2 = rmsnorm(h)
+        logits = router_logits(xn2, lw["w_router"])
+        routes.append(topk_gate(logits, k)[0])
+        y = moe_layer_forward(logits, xn2, k, lw["w_gu"], lw["s_gu"], lw["w_dn"], lw["s_dn"],
+                              inter, out_dtype="bf16")
+        h = (h.astype(np.float64) + y.astype(np.float64)).astype(np.float32)
+    return h, routes

@@ -429,4 +429,136 @@ int fo_moe_layer_forward(const float* logits, const float* x, int64_t T, int64_t
   return 0;
 }
 
+// ---------------------------------------------------------------------- MXFP4 (E2M1)
+// "[RFC] Support FP4 (E2M1) activation dispatch in MegaMoE": E2M1 activations for the
+// dispatch buffer, consumed by an MXF4 main loop.  Readings (the page gives neither block nor
+// scale format): the MX convention of blocks of 32 values along K with one power-of-two
+// scale stored as E8M0 (code E + 127); E = floor(log2(amax)) - 2 (2 is the largest E2M1
+// exponent), clamped at -127, which is also the code of an all-zero block; elements are the
+// nearest E2M1 value of x / 2^E (ties to the even mantissa bit), saturating at 6, sign kept.
+// Here the element code is found by a nearest-value search over the eight magnitudes.
+void fo_mx_quant_e2m1(const float* x, int64_t M, int64_t K, uint8_t* packed, uint8_t* scales) {
+  static const double mags[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+  const int64_t nb = K / 32;
+  for (int64_t r = 0; r < M; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* blk = x + r * K + b * 32;
+      double amax = 0.0;
+      for (int i = 0; i < 32; ++i) amax = std::fabs(static_cast<double>(blk[i])) > amax ? std::fabs(static_cast<double>(blk[i])) : amax;
+      int E = -127;
+      if (amax > 0.0) {
+        int ex;
+        std::frexp(amax, &ex);                 // amax = f * 2^ex, f in [0.5, 1)
+        E = ex - 1 - 2;
+        if (E < -127) E = -127;
+      }
+      scales[r * nb + b] = static_cast<uint8_t>(E + 127);
+      for (int i = 0; i < 32; ++i) {
+        const double v = std::ldexp(static_cast<double>(blk[i]), -E);
+        const double a = std::fabs(v);
+        int best = 7;
+        if (a < 6.0) {
+          best = 0;
+          for (int c = 1; c < 8; ++c) {
+            const double dc = std::fabs(a - mags[c]), db = std::fabs(a - mags[best]);
+            if (dc < db || (dc == db && (c & 1) == 0)) best = c;
+          }
+        }
+        const uint8_t code = static_cast<uint8_t>((std::signbit(v) ? 0x8 : 0x0) | best);
+        const int64_t k = b * 32 + i;
+        uint8_t& byte = packed[r * (K / 2) + (k >> 1)];
+        if (k & 1) byte = static_cast<uint8_t>((byte & 0x0F) | (code << 4));
+        else byte = static_cast<uint8_t>((byte & 0xF0) | code);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------ stacked-layer helpers
+// The stacked prefill workload's glue, not a page step.  Readings: a pre-norm block whose
+// RMSNorm has unit gain and eps 1e-6, computed in float64 and rounded to bfloat16; router
+// logits as float64 dot products rounded to float32; the attention core replaced by the
+// identity on v with grouped-query sharing (query head h reads kv head h / (heads / kv_heads),
+// head size 128).
+void fo_rmsnorm(const float* h, int64_t T, int64_t H, float* out) {
+  for (int64_t t = 0; t < T; ++t) {
+    double ss = 0.0;
+    for (int64_t c = 0; c < H; ++c) ss += static_cast<double>(h[t * H + c]) * h[t * H + c];
+    const double inv = 1.0 / std::sqrt(ss / static_cast<double>(H) + 1e-6);
+    for (int64_t c = 0; c < H; ++c)
+      out[t * H + c] = bf16_to_float(bf16_bits(static_cast<double>(h[t * H + c]) * inv));
+  }
+}
+
+void fo_router_logits(const float* xn, const float* w, int64_t T, int64_t H, int E, float* out) {
+  for (int64_t t = 0; t < T; ++t)
+    for (int e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int64_t c = 0; c < H; ++c) acc += static_cast<double>(xn[t * H + c]) * w[e * H + c];
+      out[t * E + e] = static_cast<float>(acc);
+    }
+}
+
+void fo_identity_attention(const float* v, int64_t T, int n_heads, int n_kv_heads, float* out) {
+  const int rep = n_heads / n_kv_heads;
+  for (int64_t t = 0; t < T; ++t)
+    for (int h = 0; h < n_heads; ++h)
+      for (int d = 0; d < 128; ++d)
+        out[(t * n_heads + h) * 128 + d] = v[(t * n_kv_heads + h / rep) * 128 + d];
+}
+
+// Dense projection: dynamic activation quantization (per tensor, or one scale per row when
+// rows != 0), the W8A8 GEMM, and the result rounded to bfloat16 ("feat(qwen4_exp) ...",
+// sections "What this adds" and "Limits").  x [M, K]; wq [N, K]; out [M, N] float values.
+void fo_linear_w8a8(const float* x, int64_t M, int64_t K, const uint8_t* wq, float sw,
+                    int64_t N, int rows, float* out) {
+  std::vector<uint8_t> q(M * K);
+  std::vector<float> s(rows ? M : 1);
+  if (rows) fo_quant_per_row(x, M, K, q.data(), s.data());
+  else fo_quant_per_tensor(x, M, K, q.data(), s.data());
+  std::vector<double> y(M * N);
+  fo_linear_w8a8_gemm(q.data(), rows ? s.data() : nullptr, s[0], wq, sw, M, N, K, y.data());
+  for (int64_t i = 0; i < M * N; ++i) out[i] = bf16_to_float(bf16_bits(y[i]));
+}
+
+// The per-token int4 expert dispatch that the grouped GEMM replaces ("FP8 grouped-expert
+// prefill ...", section 1: one dispatch per routed token per layer).  Reading: activations
+// stay unquantized; for each routed (token, slot) the expert FFN y = Wd (silu(Wg x) * (Wu x))
+// runs with the int4 weights dequantized as q * scale, in float64, token by token; the
+// output is the gate-weighted sum in slot order, rounded to the output type.
+void fo_moe_layer_int4_baseline(const float* logits, const float* x, int64_t T, int64_t H, int E,
+                                int k, int64_t I, const uint8_t* w_gu, const float* s_gu,
+                                const uint8_t* w_dn, const float* s_dn, int out_f32, float* out) {
+  std::vector<int32_t> ids(T * k);
+  std::vector<float> gates(T * k);
+  fo_topk_gate(logits, T, E, k, ids.data(), gates.data());
+  const int64_t Gh = H / kGroup, Gi = I / kGroup;
+  std::vector<double> c(2 * I), hmid(I), acc(H);
+  for (int64_t t = 0; t < T; ++t) {
+    for (int64_t o = 0; o < H; ++o) acc[o] = 0.0;
+    for (int j = 0; j < k; ++j) {
+      const int e = ids[t * k + j];
+      for (int64_t n = 0; n < 2 * I; ++n) {
+        const uint8_t* wrow = w_gu + (static_cast<int64_t>(e) * 2 * I + n) * (H / 2);
+        const float* srow = s_gu + (static_cast<int64_t>(e) * 2 * I + n) * Gh;
+        double d = 0.0;
+        for (int64_t kk = 0; kk < H; ++kk)
+          d += static_cast<double>(x[t * H + kk]) * (int4_at(wrow, kk) * static_cast<double>(srow[kk / kGroup]));
+        c[n] = d;
+      }
+      for (int64_t i = 0; i < I; ++i) hmid[i] = c[i] / (1.0 + std::exp(-c[i])) * c[I + i];
+      for (int64_t o = 0; o < H; ++o) {
+        const uint8_t* wrow = w_dn + (static_cast<int64_t>(e) * H + o) * (I / 2);
+        const float* srow = s_dn + (static_cast<int64_t>(e) * H + o) * Gi;
+        double d = 0.0;
+        for (int64_t i = 0; i < I; ++i)
+          d += hmid[i] * (int4_at(wrow, i) * static_cast<double>(srow[i / kGroup]));
+        acc[o] += static_cast<double>(gates[t * k + j]) * d;
+      }
+    }
+    for (int64_t o = 0; o < H; ++o)
+      out[t * H + o] = out_f32 ? static_cast<float>(acc[o]) : bf16_to_float(bf16_bits(acc[o]));
+  }
+}
+
 }  // extern "C"

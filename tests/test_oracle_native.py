@@ -225,3 +225,74 @@ def test_tiny_layer_equals_numpy(out_dtype):
     rel = np.linalg.norm(got - want) / np.linalg.norm(want)
     assert rel < 1e-5, rel
     assert np.mean(got != want) < 0.02
+
+
+def test_mx_quant_equals_numpy_over_every_bf16_value():
+    bits = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+    v = bits[np.isfinite(bits)]
+    v = np.concatenate([v, np.zeros((-v.size) % 1024, np.float32)]).reshape(-1, 1024)
+    rng = np.random.default_rng(13)
+    v = v[:, rng.permutation(1024)]             # mix magnitudes inside each 32-value block
+    pc, sc = cpp.mx_quant_e2m1(v)
+    pn, sn = oracle.mx_quant_e2m1(v.astype(np.float64))
+    assert np.array_equal(pc, pn) and np.array_equal(sc, sn)
+    zero = np.zeros((1, 64), np.float32)
+    assert np.array_equal(cpp.mx_quant_e2m1(zero)[1], np.zeros((1, 2), np.uint8))
+
+
+def test_stack_helpers_equal_numpy():
+    rng = np.random.default_rng(14)
+    h = (rng.standard_normal((9, 256)) * 3).astype(np.float32)
+    assert np.array_equal(cpp.rmsnorm(h), oracle.rmsnorm(h))
+    xn = oracle.rmsnorm(h)
+    w = (rng.standard_normal((16, 256)) * 0.02).astype(np.float32)
+    got, want = cpp.router_logits(xn, w), oracle.router_logits(xn, w)
+    # float64 sums in two orders, then one float32 rounding: at most one float32 step apart
+    assert np.all(np.abs(got - want) <= np.spacing(np.abs(want)))
+    v = rng.standard_normal((5, 4 * 128)).astype(np.float32)
+    assert np.array_equal(cpp.identity_attention(v, 16, 4), oracle.identity_attention(v, 16, 4))
+
+
+@pytest.mark.parametrize("rows", [False, True])
+def test_dense_projection_equals_numpy(rows):
+    rng = np.random.default_rng(15)
+    wq, sw = oracle.quant_act_per_tensor((rng.standard_normal((40, 256)) * 0.02).astype(np.float32))
+    x = rng.standard_normal((7, 256)).astype(np.float32)
+    x[3] *= 20
+    want = (oracle.linear_w8a8_rows if rows else oracle.linear_w8a8)(x, wq, sw)[0]
+    assert np.array_equal(cpp.linear_w8a8(x, wq, sw, rows=rows), want)
+
+
+def test_int4_baseline_equals_numpy():
+    inp = moe_inputs("tiny", seed=16)
+    rows = np.arange(12)
+    got = cpp.moe_layer_int4_baseline(inp.logits[rows], inp.x[rows], inp.k, inp.w_gu, inp.s_gu,
+                                      inp.w_dn, inp.s_dn, inp.I, out_dtype="f32")
+    want, _ = oracle.moe_layer_int4_baseline(inp.logits[rows], inp.x[rows], inp.k, inp.w_gu,
+                                             inp.s_gu, inp.w_dn, inp.s_dn, inp.I, out_dtype="f32")
+    assert np.allclose(got, want, rtol=1e-6, atol=1e-6 * np.abs(want).max())
+
+
+def test_stacked_prefill_equals_numpy():
+    rng = np.random.default_rng(17)
+    T, H, E, I, k, nh, nkv = 24, 256, 8, 256, 2, 2, 1
+    layers = []
+    for _ in range(3):
+        wv, sv = oracle.quant_act_per_tensor((rng.standard_normal((nkv * 128, H)) * 0.02).astype(np.float32))
+        wo, so = oracle.quant_act_per_tensor((rng.standard_normal((H, nh * 128)) * 0.02).astype(np.float32))
+        layers.append(dict(
+            wv=wv, sv=sv, wo=wo, so=so,
+            w_router=(rng.standard_normal((E, H)) * 0.02).astype(np.float32),
+            w_gu=pack_int4(rng.integers(-8, 8, (E, 2 * I, H))),
+            s_gu=rng.uniform(0.0005, 0.002, (E, 2 * I, H // 128)).astype(np.float32),
+            w_dn=pack_int4(rng.integers(-8, 8, (E, H, I))),
+            s_dn=rng.uniform(0.0005, 0.002, (E, H, I // 128)).astype(np.float32)))
+    h0 = rng.standard_normal((T, H)).astype(np.float32)
+    hc, rc = cpp.stacked_prefill(h0, layers, k, I, nh, nkv)
+    hn, rn = oracle.stacked_prefill(h0, layers, k, I, nh, nkv)
+    # the router sums and the SwiGLU exp may differ in a last bit between the two, which
+    # can move a requant code; everything else is the same arithmetic
+    cos = float((hc.ravel().astype(np.float64) @ hn.ravel()) /
+                np.sqrt((hc.astype(np.float64) ** 2).sum() * (hn.astype(np.float64) ** 2).sum()))
+    assert cos >= 0.99999, cos
+    assert all(np.array_equal(a, b) for a, b in zip(rc, rn))
