@@ -197,12 +197,13 @@ def test_gather_equals_permuted_copy(fge, epi, t, e, k, h, n):
         check_gemm(host(b), ref, absref, False)
 
 
-@pytest.mark.parametrize("t,e,k", [(1024, 4, 1), (700, 3, 2)])
-def test_grouped_bf16_full_and_ragged_tiles(fge, t, e, k):
-    """bf16 output with many full 128-row tiles (stored through shared memory with TMA tile
-    stores) next to each expert's ragged last tile (stored directly)."""
-    rng = np.random.default_rng(t + e)
-    h, n = 512, 768
+@pytest.mark.parametrize("t,e,k,n", [(1024, 4, 1, 768), (700, 3, 2, 768), (700, 3, 2, 640)])
+def test_grouped_bf16_full_and_ragged_tiles(fge, t, e, k, n):
+    """bf16 output with many full 128-row tiles (each warp stages its rows in shared memory
+    and writes them with TMA tile stores) next to each expert's ragged last tile (stored
+    directly).  N = 640 takes the 128-column tile (N not a multiple of 256)."""
+    rng = np.random.default_rng(t + e + n)
+    h = 512
     p = _routed_case(rng, t, e, k, h)
     assert np.diff(p["offsets"]).max() >= 256
     q = rng.integers(-8, 8, size=(e, n, h))
