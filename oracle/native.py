@@ -28,7 +28,7 @@ def build():
     os.makedirs(BUILD, exist_ok=True)
     if os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):
         return LIB
-    tmp = LIB + ".tmp"
+    tmp = "%s.%d.tmp" % (LIB, os.getpid())  # concurrent builds each write their own file
     r = subprocess.run([os.environ.get("CXX", "g++")] + CXXFLAGS + [SRC, "-o", tmp],
                        capture_output=True, text=True)
     if r.returncode != 0:
