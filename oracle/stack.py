@@ -1,10 +1,12 @@
 """Oracle: stacked prefill layers (RMSNorm, dense W8A8 q/k/v/o, identity attention, router,
 MoE FFN, float32 residual).
 
-Test infrastructure only (see the package docstring).  "Parity unpinned" beyond the final
-cosine: the stack is compared by cosine similarity of the final hidden state and by the
-count of routing choices that differ, as the source page compares its FP8 prefill by logit
-cosine ("FP8 grouped-expert prefill with on-chip int4-to-e4m3 dequant", sections 1 and 3).
+Test infrastructure only (see the package docstring).  The composition is pinned by two
+properties (zero weights give the identity; token permutations commute with the stack) and
+each piece by its own pins; the GPU stack is compared with it by cosine similarity of the
+final hidden state and by the count of routing choices that differ, as the source page
+compares its FP8 prefill by logit cosine ("FP8 grouped-expert prefill with on-chip
+int4-to-e4m3 dequant", sections 1 and 3).
 """
 
 import numpy as np
