@@ -23,8 +23,10 @@ the seeded input generators of ``workloads``, which hold none of the method's ar
 
 Pins (tests marked ``not gpu``) tie each function to facts the pages and the mathematics
 fix: the e4m3 code table, int4 exactness in e4m3, exact power-of-two GEMMs, closed forms,
-brute force on tiny inputs, and the permutation invariants.  Functions whose result is only
-checked by a similarity measure say "parity unpinned" in their docstring.
+brute force on tiny inputs, and the permutation invariants; the stacked prefill's
+composition by its zero-weight identity and token-permutation equivariance.  A function
+whose result were only checked by a similarity measure would say "parity unpinned" in its
+docstring; none is left.
 """
 
 from .fp8 import (  # noqa: F401
