@@ -95,3 +95,107 @@ def test_planted_replaced_residual_is_caught(monkeypatch):
     monkeypatch.setattr(oracle, "stacked_prefill", bad_stack)
     with pytest.raises(AssertionError):
         _identity_pin()
+
+
+# ---------------------------------------------------------------------------------------
+# Layer order.  The pins above cannot tell the two norms of a layer apart (with zero
+# projections the residual does not move, so both norms see the same rows).  These build a
+# layer whose attention half has a closed form: rows h = c_t * sign with c_t a power of two
+# normalise to exactly the signs in bf16; v and o projections that copy channels (e4m3
+# weight 1.0, per-tensor scale 1/448 on both operands) reproduce their input exactly; the
+# grouped-query repeat then gives attn[t, j] = sign[t, j mod 128].  So after the attention
+# residual h1 = h + sign[:, j mod 128] exactly, and h1 is not a multiple of h: a router or
+# MoE that reads the first norm's output instead of the second's gives a different layer.
+
+def _order_layer(rng, H=256, E=8, I=256, zero_moe=False):
+    wv = np.zeros((128, H), np.float32)
+    wv[np.arange(128), np.arange(128)] = 1.0        # v copies channels 0..127
+    wo = np.eye(H, dtype=np.float32)                 # o copies its input
+    wvq, sv = oracle.quant_act_per_tensor(wv)
+    woq, so = oracle.quant_act_per_tensor(wo)
+    q_gu = np.zeros((E, 2 * I, H), np.int8) if zero_moe else rng.integers(-8, 8, (E, 2 * I, H))
+    q_dn = np.zeros((E, H, I), np.int8) if zero_moe else rng.integers(-8, 8, (E, H, I))
+    return dict(wv=wvq, sv=sv, wo=woq, so=so,
+                w_router=(rng.standard_normal((E, H)) * 0.5).astype(np.float32),
+                w_gu=pack_int4(q_gu),
+                s_gu=rng.uniform(5e-4, 2e-3, (E, 2 * I, H // 128)).astype(np.float32),
+                w_dn=pack_int4(q_dn),
+                s_dn=rng.uniform(5e-4, 2e-3, (E, H, I // 128)).astype(np.float32))
+
+
+def _order_rows(rng, T=32, H=256):
+    sign = np.where(rng.random((T, H)) < 0.5, -1.0, 1.0).astype(np.float32)
+    c = (2.0 ** rng.integers(-1, 3, (T, 1))).astype(np.float32)
+    return (c * sign).astype(np.float32), sign
+
+
+def _attention_half_pin():
+    rng = np.random.default_rng(41)
+    h, sign = _order_rows(rng)
+    h1 = h + sign[:, np.arange(256) % 128]               # closed form of the attention half
+    out, _ = oracle.stacked_prefill(h, [_order_layer(rng, zero_moe=True)], 2, 256, 2, 1)
+    assert np.array_equal(out, h1)                       # zero experts add exactly zero
+
+
+def _moe_half_pin():
+    rng = np.random.default_rng(42)
+    h, sign = _order_rows(rng)
+    lw = _order_layer(rng)
+    h1 = h + sign[:, np.arange(256) % 128]
+    xn2 = oracle.rmsnorm(h1)                             # the second norm reads h1
+    y, _ = oracle.moe_layer_forward(oracle.router_logits(xn2, lw["w_router"]), xn2, 2,
+                                    lw["w_gu"], lw["s_gu"], lw["w_dn"], lw["s_dn"], 256,
+                                    out_dtype="bf16")
+    want = (h1.astype(np.float64) + y.astype(np.float64)).astype(np.float32)
+    out, _ = oracle.stacked_prefill(h, [lw], 2, 256, 2, 1)
+    assert not np.array_equal(want, h1)                  # the experts did contribute
+    assert np.array_equal(out, want)
+
+
+def test_attention_half_closed_form():
+    _attention_half_pin()
+
+
+def test_moe_reads_the_second_norm():
+    _moe_half_pin()
+
+
+def _planted_stack(router_from_first_norm=False, moe_from_first_norm=False,
+                   attention_on_raw=False):
+    def stack(h0, layers, k, inter, n_heads, n_kv_heads):
+        h = np.asarray(h0, dtype=np.float32).copy()
+        for lw in layers:
+            xn = ostack.rmsnorm(h)
+            v, _, _ = ostack.linear_w8a8(h if attention_on_raw else xn, lw["wv"], lw["sv"])
+            o, _, _ = ostack.linear_w8a8(ostack.identity_attention(v, n_heads, n_kv_heads),
+                                         lw["wo"], lw["so"])
+            h = (h.astype(np.float64) + o.astype(np.float64)).astype(np.float32)
+            xn2 = ostack.rmsnorm(h)
+            lg = ostack.router_logits(xn if router_from_first_norm else xn2, lw["w_router"])
+            y, _ = ostack.moe_layer_forward(lg, xn if moe_from_first_norm else xn2, k,
+                                            lw["w_gu"], lw["s_gu"], lw["w_dn"], lw["s_dn"],
+                                            inter, out_dtype="bf16")
+            h = (h.astype(np.float64) + y.astype(np.float64)).astype(np.float32)
+        return h, []
+    return stack
+
+
+@pytest.mark.parametrize("mistake", ["router_from_first_norm", "moe_from_first_norm"])
+def test_planted_first_norm_reader_is_caught(monkeypatch, mistake):
+    monkeypatch.setattr(oracle, "stacked_prefill", _planted_stack(**{mistake: True}))
+    with pytest.raises(AssertionError):
+        _moe_half_pin()
+
+
+def test_planted_attention_on_unnormed_rows_is_caught(monkeypatch):
+    monkeypatch.setattr(oracle, "stacked_prefill", _planted_stack(attention_on_raw=True))
+    with pytest.raises(AssertionError):
+        _attention_half_pin()
+
+
+def test_unplanted_stack_passes_the_order_pins(monkeypatch):
+    # the restated stack used for the planted versions is itself correct: with no mistake
+    # planted it passes both pins (so the failures above come from the planted mistakes)
+    monkeypatch.setattr(oracle, "stacked_prefill", _planted_stack())
+    _attention_half_pin()
+    _moe_half_pin()
