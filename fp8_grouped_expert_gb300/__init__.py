@@ -57,6 +57,7 @@ SIGNATURES = {
     "fge_moe_layer_per_token_dispatch": [_P, _P, _I64, _I64, _I, _I, _I64, _P, _P, _P, _P, _I,
                                          _P, _P, _SZ, _P],
     "fge_linear_w8a8_noalloc": [_P, _I64, _I64, _P, _P, _I64, _P, _P],
+    "fge_linear_w8a8_noalloc_status": [_P, ctypes.POINTER(ctypes.c_int32)],
     "fge_moe_layer_forward": [_P, _P, _I64, _I64, _I, _I, _I64, _P, _P, _P, _P, _I, _I, _P, _P,
                               _SZ, _P],
     "fge_selftest_wait_timeout": [_P, _I64, _P],

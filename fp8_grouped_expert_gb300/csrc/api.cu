@@ -84,8 +84,40 @@ LayerWs carve_layer(void* base, int64_t T, int64_t H, int64_t I, int E, int k) {
 
 int num_sms() {
   int dev = 0;
-  cudaGetDevice(&dev);
-  return (dev >= 0 && dev < kMaxDevices && g_sms[dev] > 0) ? g_sms[dev] : 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_sms[dev] > 0) return g_sms[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 1;
+  g_sms[dev] = n;
+  return n;
+}
+
+namespace {
+struct KernelSetup {
+  int dev;
+  const void* kernel;
+  bool ok;
+};
+constexpr int kMaxKernelSetups = 512;
+std::mutex g_kernel_mu;
+KernelSetup g_kernel_setup[kMaxKernelSetups];
+int g_kernel_setups = 0;
+}  // namespace
+
+bool device_kernel_ready(int dev, const void* kernel, int smem_bytes, int min_regs) {
+  std::lock_guard<std::mutex> lock(g_kernel_mu);
+  for (int i = 0; i < g_kernel_setups; ++i)
+    if (g_kernel_setup[i].dev == dev && g_kernel_setup[i].kernel == kernel)
+      return g_kernel_setup[i].ok;
+  bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_bytes) == cudaSuccess;
+  cudaFuncAttributes attr;
+  if (ok) ok = cudaFuncGetAttributes(&attr, kernel) == cudaSuccess && attr.numRegs >= min_regs;
+  if (g_kernel_setups < kMaxKernelSetups)
+    g_kernel_setup[g_kernel_setups++] = KernelSetup{dev, kernel, ok};
+  return ok;
 }
 
 }  // namespace fge

@@ -97,13 +97,12 @@ cudaError_t launch_per_token_dispatch(const uint16_t* x, const int32_t* ids, int
   const int64_t pairs = T * k;
   if (pairs == 0) return cudaSuccess;
   const size_t smem = static_cast<size_t>(H + 2 * I) * sizeof(float);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(per_token_dispatch_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return ce;
+  if (!device_kernel_ready(dev, reinterpret_cast<const void*>(per_token_dispatch_kernel),
+                           96 * 1024, 0))
+    return cudaErrorInvalidConfiguration;
   per_token_dispatch_kernel<<<static_cast<unsigned>(pairs), kDispatchThreads, smem, s>>>(
       x, ids, T, k, static_cast<int>(H), static_cast<int>(I), w_gu, s_gu, w_dn, s_dn, y);
   cudaError_t e = cudaGetLastError();

@@ -95,6 +95,14 @@ cudaError_t launch_per_token_dispatch(const uint16_t* x, const int32_t* ids, int
                                       const float* s_gu, const uint8_t* w_dn, const float* s_dn,
                                       float* y, int32_t* token_row, cudaStream_t s);
 
+// SM count of the current device (cached per device; queried on first use, which allocates
+// nothing, so calls that need no fge_init still size their grids from the real count).
 int num_sms();
+
+// Per-device set-up of one kernel, done once per (device, kernel) with that device current
+// and guarded by a mutex: sets the dynamic shared-memory limit to smem_bytes and checks that
+// the kernel was compiled with at least min_regs registers per thread (kernels that split
+// their registers with setmaxnreg need the whole launch allotment).  False if either fails.
+bool device_kernel_ready(int dev, const void* kernel, int smem_bytes, int min_regs);
 
 }  // namespace fge

@@ -14,6 +14,7 @@
 // stage carries one group and each group is 4 MMAs of K = 32 into a fresh TMEM buffer.
 // Two TMEM buffers (2 x BN columns) let the MMA run one group ahead of the promotion.
 #include <algorithm>
+#include <mutex>
 #include <cudaTypedefs.h>
 
 #include "fge_device.cuh"
@@ -803,17 +804,18 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
 // -------------------------------------------------------------------------------------
 // host side
 // -------------------------------------------------------------------------------------
+// The driver's tensor-map encoder, looked up once per process (thread-safe).
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static std::once_flag once;
+  std::call_once(once, [] {
     cudaDriverEntryPointQueryResult q;
     void* p = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
   return fn;
 }
 
@@ -866,27 +868,18 @@ template <int BN, int BFMT, int EPI>
 static cudaError_t run(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st) {
   using C = Cfg<BN, BFMT, EPI>;
   auto kern = grouped_gemm_kernel<BN, BFMT, EPI>;
-  static bool configured = false;
-  static int regs = 0;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    cudaFuncAttributes attr;
-    e = cudaFuncGetAttributes(&attr, kern);
-    if (e != cudaSuccess) return e;
-    regs = attr.numRegs;
-    configured = true;
-  }
-  if (C::kGroupScale) {
-    // the register split must fit in what the CTA is launched with, or the growing
-    // warpgroups would wait forever
-    const long need = 128L * C::kRegsUnpack + 128L * C::kRegsCtrl +
-                      static_cast<long>(C::kEpiThreads) * C::kRegsHigh;
-    if (static_cast<long>(regs) * C::kThreads < need || regs < C::kRegsUnpack) {
-      *st = FGE_ERR_UNSUPPORTED_DEVICE;
-      return cudaSuccess;
-    }
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return ce;
+  // group mode: the register split must fit in what the CTA is launched with, or the growing
+  // warpgroups would wait forever; the per-device set-up refuses a kernel with fewer
+  const long need = C::kGroupScale ? 128L * C::kRegsUnpack + 128L * C::kRegsCtrl +
+                                         static_cast<long>(C::kEpiThreads) * C::kRegsHigh
+                                   : 0L;
+  const int min_regs = static_cast<int>((need + C::kThreads - 1) / C::kThreads);
+  if (!device_kernel_ready(dev, reinterpret_cast<const void*>(kern), C::kSmemBytes, min_regs)) {
+    *st = FGE_ERR_UNSUPPORTED_DEVICE;
+    return cudaSuccess;
   }
   CUtensorMap tmA, tmB;
   // gather mode: A is the token-ordered [rows_a, K] tensor read one row per box (4 per copy)
@@ -949,12 +942,12 @@ template <int EPI>
 static cudaError_t run_swapped(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st) {
   using C = Cfg<16, kBfmtE4m3, EPI>;
   auto kern = grouped_gemm_kernel<16, kBfmtE4m3, EPI>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return ce;
+  if (!device_kernel_ready(dev, reinterpret_cast<const void*>(kern), C::kSmemBytes, 0)) {
+    *st = FGE_ERR_UNSUPPORTED_DEVICE;
+    return cudaSuccess;
   }
   CUtensorMap tmA, tmB;
   if (!make_map_u8(&tmA, a.w, a.K, a.N, 128, 128, true) ||

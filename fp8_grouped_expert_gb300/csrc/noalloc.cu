@@ -103,3 +103,19 @@ extern "C" fge_status fge_linear_w8a8_noalloc(const void* x, int64_t M, int64_t 
   if (launch_grouped_gemm(a, stream, &gst) != cudaSuccess) return FGE_ERR_CUDA;
   return gst;
 }
+
+// Device status word of the no-alloc call's scratch (the same header layout as a workspace):
+// non-zero when a pipeline wait of one of its kernels ran out of its time budget.  Waits for
+// `stream`, then copies the word to *out (host).  Like the rest of the scratch it is shared by
+// every call on the device and cleared at the start of each call.
+extern "C" fge_status fge_linear_w8a8_noalloc_status(fge_stream_t stream, int32_t* out) {
+  if (!out) return FGE_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  const fge_status st = scratch_for_current_device(&scratch);
+  if (st != FGE_OK) return st;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FGE_ERR_CUDA;
+  if (cudaMemcpy(out, &static_cast<WsHeader*>(scratch)->status, sizeof(int32_t),
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FGE_ERR_CUDA;
+  return FGE_OK;
+}

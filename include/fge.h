@@ -84,8 +84,10 @@ typedef enum {
 /* Library version (major*10000 + minor*100 + patch). */
 int fge_version(void);
 
-/* Checks that `device` is an sm_103 GPU and caches its SM count; sets kernel attributes.
- * Idempotent; call once per device before any other call on it. */
+/* Checks that `device` is an sm_103 GPU and caches its SM count.  Idempotent and safe to
+ * call from several host threads; call once per device before any other call on it.  Each
+ * kernel's shared-memory limit is set on its first launch on a device (per device, under a
+ * lock), so a process may drive several GPUs. */
 fge_status fge_init(int device);
 
 /* Human-readable name of a status code (static string). */
@@ -294,6 +296,13 @@ fge_status fge_moe_layer_per_token_dispatch(const float* logits, const void* x_b
 fge_status fge_linear_w8a8_noalloc(const void* x_bf16, int64_t M, int64_t K, const uint8_t* wq,
                                    const float* w_scale, int64_t N, void* y_bf16,
                                    fge_stream_t stream);
+
+/* linear_w8a8_noalloc_status -- the device status word of fge_linear_w8a8_noalloc's scratch:
+ * FGE_ERR_DEVICE_TIMEOUT if a pipeline wait of its last call ran out of its time budget
+ * (the output is then incomplete), else 0.  Waits for `stream`, then copies the word to *out
+ * (host).  The word is shared by all calls on the current device, like the rest of the
+ * scratch, and each call clears it before its kernels run.  Allocates nothing. */
+fge_status fge_linear_w8a8_noalloc_status(fge_stream_t stream, int32_t* out);
 
 /* moe_layer_forward -- one MoE FFN prefill layer in one call: top-k gate -> G128 quant ->
  * permute -> gate_up grouped GEMM with fused SwiGLU + requant -> down grouped GEMM ->
