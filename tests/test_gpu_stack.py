@@ -1,12 +1,21 @@
 """GPU parity of the stacked-prefill glue (RMSNorm, fp32 router, identity attention,
-residual add) and of the stacked prefill itself against the oracle.
+residual add) and of the stacked prefill itself against the oracle, on the stacked workload
+itself (T=2048, H=2048, 64 experts, I=768, top-8, 12 layers).
 
-The stack is compared layer by layer: each GPU layer and the oracle layer run on the same
-input (the GPU's hidden state) and their outputs and updates must have cosine >= 0.9999.
-Free-running trajectories are compared too (cosine >= 0.9999 at depth 4, reported at 8 and
-12): dynamic per-tensor and per-group e4m3 quantization makes a layer discontinuous in its
-input (one ulp on a tensor's amax element moves every code of the tensor), so fp32 and
-float64 accumulations that agree per layer drift apart with depth."""
+Layer by layer: each GPU layer and the oracle layer run on the same input (the GPU's hidden
+state) and their outputs and updates must have cosine >= 0.9999.
+
+Free running: the GPU stack and the oracle stack each run all 12 layers on their own states.
+Dynamic per-tensor and per-group e4m3 quantization makes a layer discontinuous in its input
+(one ulp on a tensor's amax element moves every code of the tensor), so any two
+implementations that round differently in the last bits drift apart with depth.  How far is
+measured on the oracle alone: tests/golden/stack_self_drift.json holds the cosine of the
+oracle's free-running state from an input moved by ~1e-6 against the unperturbed run, at
+every depth.  The GPU must stay within twice that distance (1 - cos_gpu <= 2 (1 - cos_self))
+at depths 4, 8 and 12, and at or above 0.9999 at depth 4."""
+
+import json
+import os
 
 import numpy as np
 import pytest
@@ -17,6 +26,8 @@ from util import bf16_dev, bf16_ulp, cosine, host, to_dev
 from workloads import stacked_inputs, to_bf16
 
 pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def test_rmsnorm(fge):
@@ -79,9 +90,14 @@ def _model(fge, st):
                               sh["n_heads"], sh["n_kv_heads"], "cuda")
 
 
-def test_stacked_prefill_layer_by_layer_full_size(fge):
+@pytest.fixture(scope="module")
+def stack12():
+    return stacked_inputs(12, seed=1)     # the seed the oracle self-drift study uses
+
+
+def test_stacked_prefill_layer_by_layer_full_size(fge, stack12):
     # T = 2048 tokens, 12 layers; each layer checked on 48 sampled tokens
-    st = stacked_inputs(12, seed=2)
+    st = stack12
     sh = st["shape"]
     model = _model(fge, st)
     rng = np.random.default_rng(7)
@@ -97,20 +113,25 @@ def test_stacked_prefill_layer_by_layer_full_size(fge):
         h = hg
 
 
-def test_stacked_prefill_free_running_depths(fge):
-    T = 256
-    st = stacked_inputs(12, seed=1, T=T)
+def test_stacked_prefill_free_running_depths(fge, stack12):
+    st = stack12
     sh = st["shape"]
+    with open(os.path.join(ROOT, "tests", "golden", "stack_self_drift.json")) as f:
+        drift = json.load(f)
+    assert drift["workload"]["T"] == sh["T"] and drift["workload"]["seed"] == 1
+    self_cos = drift["runs"]["rel_noise"]["cosine_by_depth"]
     model = _model(fge, st)
     hg = to_dev(st["h0"])
     ho = st["h0"].copy()
-    rows = np.arange(T)
+    rows = np.arange(sh["T"])
     cos = {}
     for li, lw in enumerate(st["layers"]):
         model.forward(hg, layers=[li])
         ho, _ = _oracle_layer(ho, lw, sh, rows)
         if li + 1 in (4, 8, 12):
             cos[li + 1] = cosine(host(hg), ho)
-    print("free-running final-state cosine by depth:", cos)
+    print("free-running final-state cosine by depth:", cos,
+          "oracle self-drift:", {d: self_cos[d - 1] for d in cos})
     assert cos[4] >= 0.9999, cos
-    assert cos[8] >= 0.999 and cos[12] >= 0.995, cos
+    for d, c in cos.items():
+        assert 1 - c <= 2 * (1 - self_cos[d - 1]), (d, c, self_cos[d - 1])
