@@ -1,9 +1,18 @@
 """Benchmark of the W4A8 grouped-expert MoE prefill layer on GB300.
 
 One step = one MoE FFN prefill layer through the C ABI (fge_moe_layer_forward: top-k gate,
-per-(token, 128) e4m3 quant, permute, gate_up grouped GEMM with fused SwiGLU requant, down
-grouped GEMM, combine) on the mid workload: T=4096 tokens, H=2048, 64 experts, I=768,
-top-8, int4 expert banks with 128-group fp32 scales, bf16 activations ~N(0,1).
+permute with the per-(token, 128) e4m3 quantization folded into its row copy, gate_up
+grouped GEMM with fused SwiGLU requant, down grouped GEMM, combine).  The headline workload
+is the largest single-GPU one, the large skewed layer: T=16384 tokens, H=4096, 128 experts,
+I=1536, top-8, Zipf(1.1)-biased routing (the hottest expert gets > 10x the mean rows, some
+get none), int4 expert banks with 128-group fp32 scales, bf16 activations ~N(0,1) with 1%
+of channels x20.
+
+Beside the headline the line reports every other workload: the tiny and mid layers, the
+dense per-tensor W8A8 projection at M = 16, 256, 2048, 8192 (N=6656, K=2560) and the stacked
+prefill at depth 4, 8 and 12 (T=2048): each with tokens/s, TFLOPS and the fraction of its
+roofline, max(flops / fp8 peak, bytes / HBM bandwidth) / time.  The HBM-bound kernels of
+the headline layer (top-k, quantization, permute, combine) get their achieved GB/s.
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead on a bounded
 sample of the same workload.  Under torchrun (N > 1) every rank runs its own replica of the
@@ -24,20 +33,15 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = "mid"
+WORKLOAD = "large"
 METRIC = "MoE prefill tokens/s; grouped-GEMM TFLOPS as % of GB300 FP8 peak, 1 GPU"
 L2_FLUSH_BYTES = 256 << 20
 
-# DRAM bytes (read + write) of one gate_up grouped-GEMM launch on this workload, from an
-# ncu capture, keyed by the sha256 prefixes of the kernel sources it was taken on.  A
-# kernel changed since the capture reports traffic = null.
+# DRAM bytes (read + write) of one gate_up grouped-GEMM launch, from an ncu capture, keyed
+# by the workload and the sha256 prefixes of the kernel sources it was taken on.  A kernel
+# changed since its capture reports traffic = null.
 KNOWN_GATE_UP_TRAFFIC = {
-    "bbab9dbfa1323528:422dc7d17945d077": 194.44e6,
-    "84cb06a30c9e661f:21919a5a3be18255": 194.99e6,
-    "3588543b1f588e0c:8f75c66d2d1b5e12": 194.63e6,
-    "6c7fc4a2718cae64:72b05a4e51127510": 194.80e6,
-    "4f87322000f2dbb1:72b05a4e51127510": 195.78e6,
-    "43dbc4055150c350:72b05a4e51127510": 194.80e6,
+    ("mid", "43dbc4055150c350:72b05a4e51127510"): 194.80e6,
 }
 
 
@@ -166,7 +170,7 @@ def run_reference(args):
         return 0
     from workloads import moe_inputs
     inp = moe_inputs(args.workload, seed=0)
-    sample = 64 if args.workload == "mid" else 16
+    sample = 64 if inp.T <= 4096 else 16
     for _ in range(args.warmup):
         oracle_tokens_per_s(inp, sample, 0.0)
     times = []
@@ -184,9 +188,10 @@ def run_reference(args):
         "data": "synthetic",
         "config": _config(inp, note="each step: the single-threaded float64 C++ CPU oracle on "
                                     "%d sampled tokens" % sample),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": "%d random tokens of the T=%d layer per step"
-                                   % (sample, inp.T)},
+        "cpu_baseline": dict({"value": value, "unit": "tokens/s", "cores": cores,
+                              "kind": "oracle",
+                              "sample": "%d random tokens of the T=%d layer per step"
+                                        % (sample, inp.T)}, **cpu_info()),
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -355,16 +360,40 @@ def run_gpu(args):
     gu_flops = 2.0 * r * (2 * inp.I) * inp.H
     gu_ms = stages["gate_up_gemm"]
     achieved = gu_flops / (gu_ms / 1e3) / 1e12
-    layer_flops = gu_flops + 2.0 * r * inp.H * inp.I
+    ids_dev, _ = fge.moe_topk_gate(logits, inp.k)
+    counts = torch.bincount(ids_dev.flatten().long(), minlength=inp.E).cpu().numpy()
+    layer_flops, layer_bytes = layer_work(inp, counts)
+    layer_frac, layer_bound = roofline_frac(layer_flops, layer_bytes, ms, fp8_peak, hbm)
+
+    # the HBM-bound stages of this layer against the measured copy bandwidth
+    sb = stage_bytes(inp)
+    memory_kernels = {name: {"ms": stages[name], "bytes": nbytes,
+                             "hbm_gbs": nbytes / (stages[name] / 1e3) / 1e9,
+                             "hbm_frac": nbytes / (stages[name] / 1e3) / 1e9 / hbm}
+                      for name, nbytes in sb.items()}
+
+    # every other workload, each on its own line of the object (rank 0 only)
+    configs = None
+    if rank == 0 and not args.no_extras:
+        reps = max(5, min(args.steps, 20))
+        configs = {}
+        for name in ("tiny", "mid", "large"):
+            if name != args.workload:
+                configs[name] = layer_config(fge, torch, name, dev, flush, reps, fp8_peak, hbm)
+        configs["dense_w8a8"] = dense_sweep(fge, torch, dev, flush, reps, fp8_peak, hbm)
+        configs["stacked_prefill"] = stacked_depths(fge, torch, dev, flush, max(5, reps // 2),
+                                                    fp8_peak, hbm)
 
     if rank != 0:
         return 0
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        rate, done, el = oracle_tokens_per_s(inp, 64, args.cpu_seconds)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": ORACLE_CORES, "kind": "oracle",
-               "sample": "%d tokens (random 64-token samples of the T=%d layer) in %.1f s"
-                         % (done, inp.T, el)}
+        sample = 64 if inp.T <= 4096 else 16
+        rate, done, el = oracle_tokens_per_s(inp, sample, args.cpu_seconds)
+        cpu = dict({"value": rate, "unit": "tokens/s", "cores": ORACLE_CORES, "kind": "oracle",
+                    "sample": "%d tokens (random %d-token samples of the T=%d layer, each a "
+                              "whole layer call of the single-threaded float64 C++ oracle) "
+                              "in %.1f s" % (done, sample, inp.T, el)}, **cpu_info())
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -373,14 +402,21 @@ def run_gpu(args):
         "config": dict(_config(inp), launch="direct stream launches" if args.no_graph
                        else "CUDA graph of the layer call, replayed per step"),
         "layer_tflops": layer_flops / (ms / 1e3) / 1e12,
+        "layer_roofline": {"bound": layer_bound, "frac": layer_frac, "flops": layer_flops,
+                           "bytes": layer_bytes,
+                           "what": "max(flops / fp8 peak, irreducible bytes / HBM) / layer "
+                                   "time; bytes = activations in + logits + output + the "
+                                   "banks and scales of the experts that got rows"},
         "stages_ms": stages,
         "roofline": {"bound": "tensor", "kernel": "grouped_gemm gate_up (fused SwiGLU requant)",
                      "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                      "frac": achieved / fp8_peak,
-                     "traffic": KNOWN_GATE_UP_TRAFFIC.get(_kernel_key()),
+                     "traffic": KNOWN_GATE_UP_TRAFFIC.get((inp.name, _kernel_key())),
                      "peak_source": "%s bf16 burst %.1f TF x 2 (fp8/bf16 nominal ratio)"
                                     % (peak_kind, bf16),
                      "algorithmic_flops_per_launch": gu_flops},
+        "memory_kernels": memory_kernels,
+        "configs": configs,
         "cpu_baseline": cpu,
         "e2e": {"value": world * inp.T / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
@@ -427,7 +463,9 @@ def mx_quant_time(fge, torch, x, flush, dev, steps):
 
 def stage_times(fge, torch, inp, x, logits, w_gu, s_gu, w_dn, s_dn, fmt, flush, dev, steps):
     """Each stage of the layer through its own C-ABI call, timed with CUDA events on the
-    launching stream, L2 flushed before each stage."""
+    launching stream, L2 flushed before each stage.  'permute_quant' is the layer's own
+    routing stage (histogram, scan, rank and the row copy that quantizes); 'quant_g128' and
+    'permute' are the same work as two separate calls."""
     stream = torch.cuda.current_stream(dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     acc = {}
@@ -448,21 +486,231 @@ def stage_times(fge, torch, inp, x, logits, w_gu, s_gu, w_dn, s_dn, fmt, flush, 
     hq = torch.empty((r, inp.I), dtype=torch.uint8, device=dev)
     hs = torch.empty((r, inp.I // 128), dtype=torch.float32, device=dev)
     y = torch.empty((r, inp.H), dtype=torch.bfloat16, device=dev)
-    out = None
     for _ in range(steps + 1):
         ids, gates = timed("topk_gate", lambda: fge.moe_topk_gate(logits, inp.k))
         xq, xs = timed("quant_g128", lambda: fge.fp8_quant_act(x, "g128"))
-        p = timed("permute", lambda: fge.moe_permute(ids, inp.E, xq, xs))
+        timed("permute", lambda: fge.moe_permute(ids, inp.E, xq, xs))
+        p = timed("permute_quant", lambda: fge.moe_permute_quant(ids, inp.E, x))
         timed("gate_up_gemm", lambda: fge.grouped_gemm_w4a8(
             p["aq"], p["as_"], p["offsets"], w_gu, s_gu, fmt=fmt, epilogue="swiglu",
             workspace=ws, out=hq, scales=hs))
         timed("down_gemm", lambda: fge.grouped_gemm_w4a8(
             hq, hs, p["offsets"], w_dn, s_dn, fmt=fmt, out_dtype=torch.bfloat16, workspace=ws,
             out=y))
-        out = timed("combine", lambda: fge.moe_combine(y, p["token_row"], gates))
+        timed("combine", lambda: fge.moe_combine(y, p["token_row"], gates))
     torch.cuda.synchronize()
     # the first pass includes allocator warm-up; drop it
     return {k: sum(a.elapsed_time(b) for a, b in v[1:]) / (len(v) - 1) for k, v in acc.items()}
+
+
+def stage_bytes(inp):
+    """Algorithmic HBM bytes of the memory-bound stages (each tensor read or written once):
+    what each stage must move, not what it happens to move."""
+    t, h, e, k = inp.T, inp.H, inp.E, inp.k
+    r = t * k
+    g = h // 128
+    return {
+        # logits in; ids and gates out
+        "topk_gate": t * e * 4 + r * 8,
+        # bf16 in; codes and one scale per 128 out
+        "quant_g128": t * h * 2 + t * h + t * g * 4,
+        # ids read (histogram and rank), codes and scales read once, written k times; the
+        # row and token index maps written
+        "permute": 2 * r * 4 + t * h + t * g * 4 + r * h + r * g * 4 + 2 * r * 4,
+        # the layer's routing stage: bf16 rows read once, codes and scales written k times
+        "permute_quant": 2 * r * 4 + t * h * 2 + r * h + r * g * 4 + 2 * r * 4,
+        # expert outputs (bf16) read once with their gates and row map; bf16 out
+        "combine": r * h * 2 + r * 8 + t * h * 2,
+    }
+
+
+def layer_work(inp, counts):
+    """(flops, irreducible HBM bytes) of one MoE layer call: the two grouped GEMMs' flops,
+    and the bytes no implementation can avoid -- activations in, logits in, output out,
+    and the int4 banks and scales of every expert that received a row."""
+    r = inp.T * inp.k
+    flops = 2.0 * r * (2 * inp.I) * inp.H + 2.0 * r * inp.H * inp.I
+    active = int((np.asarray(counts) > 0).sum())
+    bank = (2 * inp.I * inp.H // 2 + inp.H * inp.I // 2            # int4 bytes
+            + (2 * inp.I * (inp.H // 128) + inp.H * (inp.I // 128)) * 4)  # scales
+    nbytes = inp.T * inp.H * 2 * 2 + inp.T * inp.E * 4 + active * bank
+    return flops, nbytes
+
+
+def roofline_frac(flops, nbytes, ms, fp8_peak_tf, hbm_gbs):
+    """Fraction of the roofline: the slower of flops at the fp8 peak and bytes at the HBM
+    bandwidth, over the measured time."""
+    t_floor = max(flops / (fp8_peak_tf * 1e12), nbytes / (hbm_gbs * 1e9))
+    return t_floor / (ms / 1e3), ("tensor" if flops / (fp8_peak_tf * 1e12)
+                                  >= nbytes / (hbm_gbs * 1e9) else "hbm")
+
+
+def timed_calls(torch, fn, flush, stream, warm, reps, graph=True):
+    """Median device time (ms) of fn() over reps calls, L2 flushed before each; fn is
+    captured once as a CUDA graph and replayed unless graph=False."""
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    run = fn
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        run = g.replay
+        run()
+        torch.cuda.synchronize()
+    evs = []
+    for i in range(reps):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        run()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    ts = sorted(a.elapsed_time(b) for a, b in evs)
+    return ts[len(ts) // 2]
+
+
+def layer_config(fge, torch, name, dev, flush, reps, fp8_peak, hbm):
+    """One MoE layer workload timed like the headline (graph replay, L2 flushed)."""
+    from workloads import moe_inputs
+    inp = moe_inputs(name, seed=0)
+    x = torch.from_numpy(inp.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    logits = torch.from_numpy(inp.logits).to(dev)
+    fmt = fge.W4_SUBNORMAL
+    w_gu, s_gu = fge.w4_prepack(torch.from_numpy(inp.w_gu).to(dev),
+                                torch.from_numpy(inp.s_gu).to(dev), True, fmt)
+    w_dn, s_dn = fge.w4_prepack(torch.from_numpy(inp.w_dn).to(dev),
+                                torch.from_numpy(inp.s_dn).to(dev), False, fmt)
+    od = torch.float32 if inp.out == "f32" else torch.bfloat16
+    ws = fge.new_workspace(fge.workspace_bytes(fge.OP_MOE_LAYER, inp.T, inp.H, inp.I, inp.E,
+                                               inp.k), dev)
+    out = torch.empty((inp.T, inp.H), dtype=od, device=dev)
+    ms = timed_calls(torch, lambda: fge.moe_layer_forward(logits, x, inp.k, inp.I, w_gu, s_gu,
+                                                         w_dn, s_dn, fmt=fmt, out_dtype=od,
+                                                         workspace=ws, out=out),
+                     flush, torch.cuda.current_stream(dev), 3, reps)
+    ids, _ = fge.moe_topk_gate(logits, inp.k)
+    counts = torch.bincount(ids.flatten().long(), minlength=inp.E).cpu().numpy()
+    flops, nbytes = layer_work(inp, counts)
+    frac, bound = roofline_frac(flops, nbytes, ms, fp8_peak, hbm)
+    return {"workload": "%s MoE layer: T=%d, H=%d, E=%d, I=%d, top-%d" % (
+                name, inp.T, inp.H, inp.E, inp.I, inp.k),
+            "ms": ms, "tokens_per_s": inp.T / (ms / 1e3), "tflops": flops / (ms / 1e3) / 1e12,
+            "roofline": {"bound": bound, "frac": frac, "flops": flops, "bytes": nbytes}}
+
+
+def dense_sweep(fge, torch, dev, flush, reps, fp8_peak, hbm):
+    """Dense per-tensor W8A8 projection (N=6656, K=2560): quantization + GEMM through
+    fge_linear_w8a8 at each M; the weights come from HBM (L2 flushed before each call)."""
+    gen = torch.Generator(device=dev).manual_seed(1)
+    n, k = 6656, 2560
+    w = (torch.randn((n, k), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+    wq, sw = fge.fp8_quant_act(w, "tensor")
+    res = {}
+    for m in (16, 256, 2048, 8192):
+        x = torch.randn((m, k), generator=gen, device=dev).to(torch.bfloat16)
+        ws = fge.new_workspace(fge.workspace_bytes(fge.OP_LINEAR_W8A8, m, k), dev)
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        ms = timed_calls(torch, lambda: fge.linear_w8a8(x, wq, sw, workspace=ws, out=y), flush,
+                         torch.cuda.current_stream(dev), 3, reps)
+        flops = 2.0 * m * n * k
+        nbytes = n * k + 2 * m * k + 2 * m * n
+        frac, bound = roofline_frac(flops, nbytes, ms, fp8_peak, hbm)
+        res["M=%d" % m] = {"ms": ms, "tokens_per_s": m / (ms / 1e3),
+                           "tflops": flops / (ms / 1e3) / 1e12,
+                           "hbm_gbs": nbytes / (ms / 1e3) / 1e9,
+                           "roofline": {"bound": bound, "frac": frac, "flops": flops,
+                                        "bytes": nbytes}}
+    return res
+
+
+def stacked_layers_on_device(torch, dev, L, H=2048, E=64, I=768, q=2048, kv=512, seed=0):
+    """Weights of an L-layer stack drawn on the device from a seeded generator, the stacked
+    workload's recipe: bf16 q/k/v/o projections ~N(0, 0.02), fp32 router ~N(0, 0.02), and int4
+    expert banks from N(0, 0.02) draws with s = absmax/7 per (row, 128) and q = clamp(round(w /
+    s), -8, 7) packed two per byte (even element in the low nibble)."""
+    gen = torch.Generator(device=dev).manual_seed(seed)
+
+    def int4_bank(e, n, kk):
+        w = torch.randn((e, n, kk // 128, 128), generator=gen, device=dev) * 0.02
+        s = (w.abs().amax(dim=3) / 7.0).float()
+        s = torch.where(s == 0, torch.ones_like(s), s)
+        qv = torch.clamp(torch.round(w / s[..., None]), -8, 7).to(torch.int32).reshape(e, n, kk)
+        lo = qv[..., 0::2] & 0xF
+        hi = qv[..., 1::2] & 0xF
+        return (lo | (hi << 4)).to(torch.uint8).contiguous(), s.contiguous()
+
+    layers = []
+    for _ in range(L):
+        d = {}
+        for name, rows in (("q", q), ("k", kv), ("v", kv), ("o", H)):
+            d["w" + name] = (torch.randn((rows, H), generator=gen, device=dev) * 0.02
+                             ).to(torch.bfloat16)
+        d["w_router"] = torch.randn((E, H), generator=gen, device=dev) * 0.02
+        d["w_gu"], d["s_gu"] = int4_bank(E, 2 * I, H)
+        d["w_dn"], d["s_dn"] = int4_bank(E, H, I)
+        layers.append(d)
+    return layers
+
+
+def stacked_depths(fge, torch, dev, flush, reps, fp8_peak, hbm):
+    """The stacked prefill (T=2048, H=2048, 16 query / 4 kv heads, MoE 64 x 768 top-8) timed
+    over 4, 8 and 12 layers, each depth captured as one CUDA graph."""
+    T, H, E, I, k = 2048, 2048, 64, 768, 8
+    layers = stacked_layers_on_device(torch, dev, 12)
+    model = fge.StackedPrefill(layers, T, H, E, I, k, 16, 4, dev)
+    del layers
+    gen = torch.Generator(device=dev).manual_seed(2)
+    h0 = torch.randn((T, H), generator=gen, device=dev)
+    h = h0.clone()
+    per_layer_flops = (2.0 * T * H * (2048 + 512 + 512) + 2.0 * T * 2048 * H    # q, k, v, o
+                       + 2.0 * T * E * H                                        # router
+                       + 2.0 * T * k * (2 * I * H + H * I))                     # experts
+    per_layer_bytes = ((2048 + 512 + 512 + 2048) * H                            # e4m3 weights
+                       + E * (2 * I * H // 2 + H * I // 2
+                              + (2 * I * (H // 128) + H * (I // 128)) * 4)      # int4 banks
+                       + E * H * 4)                                             # router
+    res = {}
+    for L in (4, 8, 12):
+        def run():
+            h.copy_(h0)
+            model.forward(h, layers=range(L))
+        ms = timed_calls(torch, run, flush, torch.cuda.current_stream(dev), 2, reps)
+        flops = L * per_layer_flops
+        nbytes = L * per_layer_bytes + T * H * 4 * 2
+        frac, bound = roofline_frac(flops, nbytes, ms, fp8_peak, hbm)
+        res["L=%d" % L] = {"ms": ms, "tokens_per_s": T / (ms / 1e3),
+                           "tflops": flops / (ms / 1e3) / 1e12,
+                           "roofline": {"bound": bound, "frac": frac, "flops": flops,
+                                        "bytes": nbytes}}
+    return res
+
+
+def cpu_info():
+    """The host CPU's model name and the number of cores the OS offers."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith(("model name", "cpu part")):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    import platform
+    return {"cpu_model": model, "machine": platform.machine(), "nproc": os.cpu_count()}
 
 
 def main():
@@ -472,7 +720,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=["mid", "large", "tiny"],
-                    help="MoE layer workload (the headline line uses mid)")
+                    help="MoE layer workload of the headline (default: large)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="headline only: skip the other workloads' lines")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",

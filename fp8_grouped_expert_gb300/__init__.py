@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_PKG, "libfge.so")
 
 # enums of include/fge.h
 OK = 0
+ERR_DEVICE_TIMEOUT, ERR_NONFINITE = 7, 10
 SCALE_PER_TENSOR, SCALE_PER_TOKEN_G128, SCALE_PER_ROW = 0, 1, 2
 DTYPE_BF16, DTYPE_F32 = 0, 1
 EPI_STORE, EPI_SWIGLU_REQUANT = 0, 1
@@ -37,6 +38,8 @@ SIGNATURES = {
     "fge_status_string": [_I],
     "fge_workspace_bytes": [_I, _I64, _I64, _I64, _I, _I],
     "fge_clear_device_status": [_P, _P],
+    "fge_read_ledger": [_P],
+    "fge_reset_ledger": [],
     "fge_read_device_status": [_P, _P, ctypes.POINTER(ctypes.c_int32)],
     "fge_fp8_quant_act": [_P, _I64, _I64, _I, _P, _P, _P, _SZ, _P],
     "fge_mx_quant_e2m1": [_P, _I64, _I64, _P, _P, _P],
@@ -131,6 +134,23 @@ def workspace_bytes(op, a=0, b=0, c=0, E=0, k=0):
 
 def new_workspace(nbytes, device):
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+class Ledger(ctypes.Structure):
+    """fge_ledger (include/fge.h): host counters of this process's library calls."""
+    _fields_ = [(n, ctypes.c_uint64) for n in ("calls", "refused", "layers", "grouped_gemms",
+                                               "dense_decode_tile", "dense_row_tile")]
+
+
+def ledger():
+    """The library's call ledger as a dict."""
+    led = Ledger()
+    _check(lib().fge_read_ledger(ctypes.byref(led)), "fge_read_ledger")
+    return {name: getattr(led, name) for name, _ in Ledger._fields_}
+
+
+def reset_ledger():
+    _check(lib().fge_reset_ledger(), "fge_reset_ledger")
 
 
 def read_device_status(ws):
@@ -590,9 +610,10 @@ class StackedPrefill:
     -> fp32 residual.
 
     layers: list of dicts with bf16 projection weights (wq_bits, wk_bits, wv_bits, wo_bits as
-    uint16 numpy [rows, H]), fp32 w_router [E, H] and canonical int4 banks w_gu/s_gu,
-    w_dn/s_dn.  Projection weights are quantized per tensor to e4m3 at load by the
-    library's own quantizer; int4 banks are prepacked at load.
+    uint16 numpy [rows, H], or wq, wk, wv, wo as bf16 device tensors), fp32 w_router [E, H]
+    and canonical int4 banks w_gu/s_gu, w_dn/s_dn (numpy arrays or device tensors).
+    Projection weights are quantized per tensor to e4m3 at load by the library's own
+    quantizer; int4 banks are prepacked at load.
     """
 
     def __init__(self, layers, T, H, E, I, k, n_heads, n_kv_heads, device, fmt=W4_SUBNORMAL):
@@ -603,17 +624,24 @@ class StackedPrefill:
         self.dev = torch.device(device)
         _ensure_init(self.dev)
         self.layers = []
+        def dev_tensor(a):
+            return a.to(self.dev) if torch.is_tensor(a) else torch.from_numpy(a).to(self.dev)
+
         for lw in layers:
             d = {}
             for name in ("q", "k", "v", "o"):
-                wb = torch.from_numpy(np.ascontiguousarray(lw["w" + name + "_bits"]).view(np.int16))
-                wq, ws = fp8_quant_act(wb.view(torch.bfloat16).to(self.dev), "tensor")
+                if "w" + name in lw:
+                    wb = lw["w" + name].to(self.dev)
+                else:
+                    bits = np.ascontiguousarray(lw["w" + name + "_bits"]).view(np.int16)
+                    wb = torch.from_numpy(bits).view(torch.bfloat16).to(self.dev)
+                wq, ws = fp8_quant_act(wb, "tensor")
                 d["w" + name], d["s" + name] = wq, ws
-            d["w_router"] = torch.from_numpy(lw["w_router"]).to(self.dev)
-            d["w_gu"], d["s_gu"] = w4_prepack(torch.from_numpy(lw["w_gu"]).to(self.dev),
-                                              torch.from_numpy(lw["s_gu"]).to(self.dev), True, fmt)
-            d["w_dn"], d["s_dn"] = w4_prepack(torch.from_numpy(lw["w_dn"]).to(self.dev),
-                                              torch.from_numpy(lw["s_dn"]).to(self.dev), False, fmt)
+            d["w_router"] = dev_tensor(lw["w_router"])
+            d["w_gu"], d["s_gu"] = w4_prepack(dev_tensor(lw["w_gu"]), dev_tensor(lw["s_gu"]),
+                                              True, fmt)
+            d["w_dn"], d["s_dn"] = w4_prepack(dev_tensor(lw["w_dn"]), dev_tensor(lw["s_dn"]),
+                                              False, fmt)
             self.layers.append(d)
         dev = self.dev
         kv = n_kv_heads * 128

@@ -1,7 +1,10 @@
 // C ABI of libfge: argument validation, workspace carving and stream-ordered launches.
 // No entry point allocates device memory or synchronises the host (except
 // fge_read_device_status, which exists to read a result back).
+#include <atomic>
 #include <mutex>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "fge_internal.h"
 
@@ -13,13 +16,27 @@ int g_sms[kMaxDevices] = {0};
 bool g_init[kMaxDevices] = {false};
 std::mutex g_mu;
 
+std::atomic<uint64_t> g_ledger[kLedFields];
+
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Every compute entry point starts here: counts the call, and the call as refused when the
+// current device was not initialised.
 inline fge_status cur_device_ok() {
+  g_ledger[kLedCalls].fetch_add(1, std::memory_order_relaxed);
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FGE_ERR_CUDA;
-  return g_init[dev] ? FGE_OK : FGE_ERR_NOT_INITIALIZED;
+  fge_status st = FGE_OK;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) st = FGE_ERR_CUDA;
+  else if (!g_init[dev]) st = FGE_ERR_NOT_INITIALIZED;
+  if (st != FGE_OK) g_ledger[kLedRefused].fetch_add(1, std::memory_order_relaxed);
+  return st;
 }
+
+// Enqueue-side NVTX range (a profiler shows each layer stage by name; free without one).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 inline fge_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FGE_OK : FGE_ERR_CUDA; }
 
@@ -29,9 +46,12 @@ inline fge_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FGE_OK : 
     if (st_ != FGE_OK) return st_;      \
   } while (0)
 
-#define FGE_REQUIRE(cond, code) \
-  do {                          \
-    if (!(cond)) return (code); \
+#define FGE_REQUIRE(cond, code)                                           \
+  do {                                                                    \
+    if (!(cond)) {                                                        \
+      fge::g_ledger[fge::kLedRefused].fetch_add(1, std::memory_order_relaxed); \
+      return (code);                                                      \
+    }                                                                     \
   } while (0)
 
 // Workspace layout of a full MoE layer.
@@ -81,6 +101,8 @@ LayerWs carve_layer(void* base, int64_t T, int64_t H, int64_t I, int E, int k) {
 }
 
 }  // namespace
+
+void ledger_note(LedgerField f) { g_ledger[f].fetch_add(1, std::memory_order_relaxed); }
 
 int num_sms() {
   int dev = 0;
@@ -140,6 +162,7 @@ const char* fge_status_string(fge_status s) {
     case FGE_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
     case FGE_ERR_NOT_INITIALIZED: return "fge_init not called for this device";
     case FGE_ERR_EXCEEDS_STATIC_SCRATCH: return "size exceeds the fixed scratch of the no-alloc call";
+    case FGE_ERR_NONFINITE: return "an activation to quantize is an infinity or a NaN";
   }
   return "unknown status";
 }
@@ -173,6 +196,22 @@ size_t fge_workspace_bytes(fge_op op, int64_t a, int64_t b, int64_t c, int E, in
   return 0;
 }
 
+fge_status fge_read_ledger(fge_ledger* out) {
+  if (!out) return FGE_ERR_INVALID_ARG;
+  out->calls = g_ledger[kLedCalls].load();
+  out->refused = g_ledger[kLedRefused].load();
+  out->layers = g_ledger[kLedLayers].load();
+  out->grouped_gemms = g_ledger[kLedGroupedGemms].load();
+  out->dense_decode_tile = g_ledger[kLedDenseDecodeTile].load();
+  out->dense_row_tile = g_ledger[kLedDenseRowTile].load();
+  return FGE_OK;
+}
+
+fge_status fge_reset_ledger(void) {
+  for (int i = 0; i < kLedFields; ++i) g_ledger[i].store(0);
+  return FGE_OK;
+}
+
 fge_status fge_clear_device_status(void* ws, fge_stream_t stream) {
   FGE_REQUIRE(ws, FGE_ERR_INVALID_ARG);
   return from_cuda(cudaMemsetAsync(ws, 0, sizeof(int32_t), stream));
@@ -191,11 +230,17 @@ fge_status fge_fp8_quant_act(const void* x, int64_t M, int64_t K, fge_scale_mode
   FGE_REQUIRE(M >= 0 && K > 0 && K % 128 == 0, FGE_ERR_BAD_SHAPE);
   FGE_REQUIRE(x && xq && xs, FGE_ERR_INVALID_ARG);
   FGE_REQUIRE(al16(x) && al16(xq), FGE_ERR_MISALIGNED);
+  // G128 and per-row take no workspace; with one (>= its 256-byte header) a non-finite input
+  // is reported in its status word
+  int32_t* status = (ws && ws_bytes >= kWsHeaderBytes && al16(ws))
+                        ? &static_cast<WsHeader*>(ws)->status : nullptr;
   if (mode == FGE_SCALE_PER_TOKEN_G128) {
-    return from_cuda(launch_quant_g128(static_cast<const uint16_t*>(x), M, K, xq, xs, stream));
+    return from_cuda(launch_quant_g128(static_cast<const uint16_t*>(x), M, K, xq, xs, status,
+                                       stream));
   }
   if (mode == FGE_SCALE_PER_ROW) {
-    return from_cuda(launch_quant_rows(static_cast<const uint16_t*>(x), M, K, xq, xs, stream));
+    return from_cuda(launch_quant_rows(static_cast<const uint16_t*>(x), M, K, xq, xs, status,
+                                       stream));
   }
   FGE_REQUIRE(mode == FGE_SCALE_PER_TENSOR, FGE_ERR_INVALID_ARG);
   FGE_REQUIRE(ws, FGE_ERR_INVALID_ARG);
@@ -255,7 +300,8 @@ fge_status fge_moe_permute_quant(const int32_t* ids, int64_t T, int k, int E, co
               FGE_ERR_WORKSPACE_TOO_SMALL);
   return from_cuda(launch_permute_quant(ids, T, k, E, static_cast<const uint16_t*>(x), H, offsets,
                                         row_token, token_row, aq, as,
-                                        static_cast<uint8_t*>(ws) + kWsHeaderBytes, stream));
+                                        static_cast<uint8_t*>(ws) + kWsHeaderBytes,
+                                        &static_cast<WsHeader*>(ws)->status, stream));
 }
 
 fge_status fge_w4_prepack(const uint8_t* w, const float* w_scale, int E, int64_t N, int64_t K,
@@ -403,6 +449,7 @@ fge_status fge_linear_w8a8(const void* x, int64_t M, int64_t K, const uint8_t* w
   FGE_REQUIRE(al16(x) && al16(ws), FGE_ERR_MISALIGNED);
   FGE_REQUIRE(ws_bytes >= fge_workspace_bytes(FGE_OP_LINEAR_W8A8, M, K, 0, 0, 0),
               FGE_ERR_WORKSPACE_TOO_SMALL);
+  NvtxRange range("fge.linear_w8a8");
   WsHeader* hdr = static_cast<WsHeader*>(ws);
   uint8_t* xq = static_cast<uint8_t*>(ws) + kWsHeaderBytes;
   FGE_CHECK(from_cuda(launch_quant_per_tensor(static_cast<const uint16_t*>(x), M, K, xq,
@@ -432,7 +479,8 @@ fge_status fge_linear_w8a8_rows(const void* x, int64_t M, int64_t K, const uint8
               FGE_ERR_WORKSPACE_TOO_SMALL);
   uint8_t* xq = static_cast<uint8_t*>(ws) + kWsHeaderBytes;
   float* xs = reinterpret_cast<float*>(xq + align_up(static_cast<size_t>(M * K), 256));
-  FGE_CHECK(from_cuda(launch_quant_rows(static_cast<const uint16_t*>(x), M, K, xq, xs, stream)));
+  FGE_CHECK(from_cuda(launch_quant_rows(static_cast<const uint16_t*>(x), M, K, xq, xs,
+                                        &static_cast<WsHeader*>(ws)->status, stream)));
   return grouped_common(xq, nullptr, nullptr, M, wq, w_scale, 1, N, K, 0, 1, nullptr, 1, y,
                         nullptr, ws, ws_bytes, stream, xs);
 }
@@ -457,21 +505,38 @@ fge_status fge_moe_layer_forward(const float* logits, const void* x, int64_t T, 
   if (T == 0) return FGE_OK;
   const int64_t R = T * k;
   const int out_f32 = out_dtype == FGE_DTYPE_F32;
-  FGE_CHECK(from_cuda(launch_topk_gate(logits, T, E, k, w.ids, w.gates, stream)));
+  NvtxRange layer_range("fge.moe_layer");
+  {
+    NvtxRange r("fge.topk_gate");
+    FGE_CHECK(from_cuda(launch_topk_gate(logits, T, E, k, w.ids, w.gates, stream)));
+  }
 
   // The permuted copy of the activation rows plus a tiled A load beats gathering the rows
   // in the GEMM (fge_grouped_gemm_w4a8_gather): 32 four-row TMA gathers per K group cost
   // more than the copy kernel saves.
   // the G128 activation quantization runs inside the permutation's row copy: each token's
   // bf16 row is read once and its codes and scales go straight to its k expert rows
-  FGE_CHECK(from_cuda(launch_permute_quant(w.ids, T, k, E, static_cast<const uint16_t*>(x), H,
-                                           w.offsets, w.row_token, w.token_row, w.aq, w.as,
-                                           w.perm, stream)));
-  FGE_CHECK(grouped_common(w.aq, w.as, w.offsets, R, w_gu, s_gu, E, 2 * I, H, format, 0, nullptr,
-                           2, w.hq, w.hs, ws, ws_bytes, stream));
-  FGE_CHECK(grouped_common(w.hq, w.hs, w.offsets, R, w_dn, s_dn, E, H, I, format, 0, nullptr,
-                           out_f32 ? 0 : 1, w.y, nullptr, ws, ws_bytes, stream));
-  return from_cuda(launch_combine(w.y, out_f32, w.token_row, w.gates, T, k, H, out_f32, out, stream));
+  {
+    NvtxRange r("fge.permute_quant");
+    FGE_CHECK(from_cuda(launch_permute_quant(w.ids, T, k, E, static_cast<const uint16_t*>(x), H,
+                                             w.offsets, w.row_token, w.token_row, w.aq, w.as,
+                                             w.perm, &w.hdr->status, stream)));
+  }
+  {
+    NvtxRange r("fge.gate_up_gemm");
+    FGE_CHECK(grouped_common(w.aq, w.as, w.offsets, R, w_gu, s_gu, E, 2 * I, H, format, 0,
+                             nullptr, 2, w.hq, w.hs, ws, ws_bytes, stream));
+  }
+  {
+    NvtxRange r("fge.down_gemm");
+    FGE_CHECK(grouped_common(w.hq, w.hs, w.offsets, R, w_dn, s_dn, E, H, I, format, 0, nullptr,
+                             out_f32 ? 0 : 1, w.y, nullptr, ws, ws_bytes, stream));
+  }
+  NvtxRange r("fge.combine");
+  const fge_status st = from_cuda(launch_combine(w.y, out_f32, w.token_row, w.gates, T, k, H,
+                                                 out_f32, out, stream));
+  if (st == FGE_OK) ledger_note(kLedLayers);
+  return st;
 }
 
 fge_status fge_moe_layer_per_token_dispatch(const float* logits, const void* x, int64_t T,

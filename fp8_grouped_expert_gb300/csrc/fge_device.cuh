@@ -21,6 +21,14 @@ __device__ __forceinline__ void set_device_error(int32_t* status, int32_t code) 
   if (status) atomicCAS(status, 0, code);
 }
 
+// Non-finite input probe: folding every value x of a group into acc = fma(x, 0, acc) leaves
+// acc at 0 for finite values and makes it NaN as soon as one x is an infinity or a NaN
+// (fmaxf-based amax reductions skip NaN, so the amax alone cannot tell).
+__device__ __forceinline__ float nonfinite_fold(float acc, float x) { return fmaf(x, 0.0f, acc); }
+__device__ __forceinline__ void report_nonfinite(int32_t* status, float acc) {
+  if (status && acc != acc) set_device_error(status, FGE_ERR_NONFINITE);
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

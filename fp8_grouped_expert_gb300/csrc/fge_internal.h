@@ -30,10 +30,12 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 enum BankFormat { kBankLut = 0, kBankSubnormal = 1 };
 
 // Launchers (return a cudaError_t from the launch; argument checks happen in the API layer).
+// status (may be null): a device status word that receives FGE_ERR_NONFINITE when an input
+// value is an infinity or a NaN.
 cudaError_t launch_quant_g128(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,
-                              cudaStream_t s);
+                              int32_t* status, cudaStream_t s);
 cudaError_t launch_quant_rows(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,
-                              cudaStream_t s);
+                              int32_t* status, cudaStream_t s);
 cudaError_t launch_mx_quant_e2m1(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq,
                                  uint8_t* xs, cudaStream_t s);
 cudaError_t launch_quant_per_tensor(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq,
@@ -49,7 +51,7 @@ cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, const ui
 cudaError_t launch_permute_quant(const int32_t* ids, int64_t T, int k, int E,
                                  const uint16_t* x, int64_t H, int32_t* offsets,
                                  int32_t* row_token, int32_t* token_row, uint8_t* aq, float* as,
-                                 void* scratch, cudaStream_t s);
+                                 void* scratch, int32_t* status, cudaStream_t s);
 cudaError_t launch_combine(const void* y, int y_f32, const int32_t* token_row,
                            const float* gates, int64_t T, int k, int64_t H, int out_f32,
                            void* out, cudaStream_t s);
@@ -94,6 +96,18 @@ cudaError_t launch_per_token_dispatch(const uint16_t* x, const int32_t* ids, int
                                       int64_t H, int64_t I, const uint8_t* w_gu,
                                       const float* s_gu, const uint8_t* w_dn, const float* s_dn,
                                       float* y, int32_t* token_row, cudaStream_t s);
+
+// Host-side ledger of the library's calls (see fge_read_ledger in include/fge.h).
+enum LedgerField {
+  kLedCalls = 0,
+  kLedRefused,
+  kLedLayers,
+  kLedGroupedGemms,
+  kLedDenseDecodeTile,
+  kLedDenseRowTile,
+  kLedFields
+};
+void ledger_note(LedgerField f);
 
 // SM count of the current device (cached per device; queried on first use, which allocates
 // nothing, so calls that need no fge_init still size their grids from the real count).

@@ -978,8 +978,11 @@ static cudaError_t run_swapped(const GroupedGemmArgs& a, cudaStream_t s, fge_sta
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st) {
   const bool bn256 = (a.N % 256) == 0;
-  if (a.per_tensor && a.offsets == nullptr && a.row_token == nullptr && a.R <= 16)
+  if (a.per_tensor && a.offsets == nullptr && a.row_token == nullptr && a.R <= 16) {
+    ledger_note(kLedDenseDecodeTile);
     return a.epilogue == 0 ? run_swapped<kEpiF32>(a, s, st) : run_swapped<kEpiBf16>(a, s, st);
+  }
+  ledger_note(a.per_tensor ? kLedDenseRowTile : kLedGroupedGemms);
   if (a.per_tensor) {
     if (a.epilogue == 0) return bn256 ? run<256, kBfmtE4m3, kEpiF32>(a, s, st) : run<128, kBfmtE4m3, kEpiF32>(a, s, st);
     return bn256 ? run<256, kBfmtE4m3, kEpiBf16>(a, s, st) : run<128, kBfmtE4m3, kEpiBf16>(a, s, st);

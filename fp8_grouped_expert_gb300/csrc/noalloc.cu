@@ -45,29 +45,29 @@ fge_status scratch_for_current_device(void** out) {
 
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-}  // namespace
-}  // namespace fge
-
-using namespace fge;
-
-extern "C" fge_status fge_linear_w8a8_noalloc(const void* x, int64_t M, int64_t K,
-                                              const uint8_t* wq, const float* w_scale,
-                                              int64_t N, void* y, fge_stream_t stream) {
+// Argument checks of fge_linear_w8a8_noalloc, before anything is enqueued.
+fge_status noalloc_checks(const void* x, int64_t M, int64_t K, const uint8_t* wq,
+                          const float* w_scale, int64_t N, void* y) {
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return FGE_ERR_CUDA;
   if (major != 10 || minor != 3) return FGE_ERR_UNSUPPORTED_DEVICE;
-  if (!x || !wq || !w_scale || !y) return FGE_ERR_INVALID_ARG;
   if (M < 0 || K <= 0 || K % 128 != 0 || N <= 0 || N % 128 != 0 || N >= (1LL << 24) ||
       K >= (1LL << 24) || M >= (1LL << 31))
     return FGE_ERR_BAD_SHAPE;
+  if (M == 0) return FGE_OK;  // nothing is read or written: x and y may be NULL
+  if (!x || !wq || !w_scale || !y) return FGE_ERR_INVALID_ARG;
   if (static_cast<uint64_t>(M) * static_cast<uint64_t>(K) > kNoallocMaxActBytes)
     return FGE_ERR_EXCEEDS_STATIC_SCRATCH;
   if (!al16(x) || !al16(wq) || !al16(y)) return FGE_ERR_MISALIGNED;
-  if (M == 0) return FGE_OK;
+  return FGE_OK;
+}
 
+// The projection itself: per-tensor quantization into the scratch, then the one-expert GEMM.
+fge_status noalloc_run(const void* x, int64_t M, int64_t K, const uint8_t* wq,
+                       const float* w_scale, int64_t N, void* y, fge_stream_t stream) {
   void* scratch = nullptr;
   const fge_status st = scratch_for_current_device(&scratch);
   if (st != FGE_OK) return st;
@@ -104,10 +104,29 @@ extern "C" fge_status fge_linear_w8a8_noalloc(const void* x, int64_t M, int64_t 
   return gst;
 }
 
+}  // namespace
+}  // namespace fge
+
+using namespace fge;
+
+extern "C" fge_status fge_linear_w8a8_noalloc(const void* x, int64_t M, int64_t K,
+                                              const uint8_t* wq, const float* w_scale,
+                                              int64_t N, void* y, fge_stream_t stream) {
+  ledger_note(kLedCalls);
+  const fge_status st = noalloc_checks(x, M, K, wq, w_scale, N, y);
+  if (st != FGE_OK) {
+    ledger_note(kLedRefused);
+    return st;
+  }
+  if (M == 0) return FGE_OK;
+  return noalloc_run(x, M, K, wq, w_scale, N, y, stream);
+}
+
 // Device status word of the no-alloc call's scratch (the same header layout as a workspace):
-// non-zero when a pipeline wait of one of its kernels ran out of its time budget.  Waits for
-// `stream`, then copies the word to *out (host).  Like the rest of the scratch it is shared by
-// every call on the device and cleared at the start of each call.
+// non-zero when a pipeline wait of one of its kernels ran out of its time budget, or when an
+// activation was an infinity or a NaN.  Waits for `stream`, then copies the word to *out
+// (host).  Like the rest of the scratch it is shared by every call on the device and cleared
+// at the start of each call.
 extern "C" fge_status fge_linear_w8a8_noalloc_status(fge_stream_t stream, int32_t* out) {
   if (!out) return FGE_ERR_INVALID_ARG;
   void* scratch = nullptr;

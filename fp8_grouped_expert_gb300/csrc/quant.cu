@@ -15,7 +15,8 @@ namespace fge {
 // lane keeps several 16-byte reads in flight (the kernel is bound by DRAM latency otherwise).
 constexpr int kQuantUnroll = 4;
 __global__ void quant_g128_kernel(const uint4* __restrict__ x, int64_t groups,
-                                  uint2* __restrict__ xq, float* __restrict__ xs) {
+                                  uint2* __restrict__ xq, float* __restrict__ xs,
+                                  int32_t* status) {
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4, hl = lane & 15;
   const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
@@ -32,9 +33,13 @@ __global__ void quant_g128_kernel(const uint4* __restrict__ x, int64_t groups,
       const int64_t g = g0 + u * nw * 2 + half;
       const float f[8] = {bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y),
                           bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w)};
-      float amax = 0.0f;
+      float amax = 0.0f, bad = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+      for (int i = 0; i < 8; ++i) {
+        amax = fmaxf(amax, fabsf(f[i]));
+        bad = nonfinite_fold(bad, f[i]);
+      }
+      report_nonfinite(status, bad);
 #pragma unroll
       for (int d = 8; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
       const float s = scale_from_amax(amax);
@@ -53,8 +58,9 @@ __global__ void quant_g128_kernel(const uint4* __restrict__ x, int64_t groups,
 
 // Per-tensor pass 1: amax over the tensor, combined across blocks with atomicMax on the
 // float bits (|x| >= 0, so the unsigned order of the bits is the float order).
-__global__ void amax_kernel(const uint4* __restrict__ x, int64_t n8, uint32_t* __restrict__ amax_bits) {
-  float m = 0.0f;
+__global__ void amax_kernel(const uint4* __restrict__ x, int64_t n8, uint32_t* __restrict__ amax_bits,
+                            int32_t* status) {
+  float m = 0.0f, bad = 0.0f;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const uint4 v = __ldg(x + i);
@@ -62,7 +68,16 @@ __global__ void amax_kernel(const uint4* __restrict__ x, int64_t n8, uint32_t* _
                        fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)))));
     m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))),
                        fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)))));
+    bad = nonfinite_fold(nonfinite_fold(nonfinite_fold(nonfinite_fold(bad, bf16_lo(v.x)),
+                                                       bf16_hi(v.x)),
+                                        bf16_lo(v.y)),
+                         bf16_hi(v.y));
+    bad = nonfinite_fold(nonfinite_fold(nonfinite_fold(nonfinite_fold(bad, bf16_lo(v.z)),
+                                                       bf16_hi(v.z)),
+                                        bf16_lo(v.w)),
+                         bf16_hi(v.w));
   }
+  report_nonfinite(status, bad);
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
   __shared__ float red[32];
@@ -101,20 +116,30 @@ __global__ void cast_per_tensor_kernel(const uint4* __restrict__ x, int64_t n8,
 // One scale per row (token): one warp per row, two passes over the row (amax, then the
 // cast; the second pass reads the row back from L1/L2).
 __global__ void quant_row_kernel(const uint4* __restrict__ x, int64_t M, int64_t n8_row,
-                                 uint2* __restrict__ xq, float* __restrict__ xs) {
+                                 uint2* __restrict__ xq, float* __restrict__ xs,
+                                 int32_t* status) {
   const int lane = threadIdx.x & 31;
   const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   for (int64_t r = wid; r < M; r += nw) {
     const uint4* xr = x + r * n8_row;
-    float amax = 0.0f;
+    float amax = 0.0f, bad = 0.0f;
     for (int64_t i = lane; i < n8_row; i += 32) {
       const uint4 v = __ldg(xr + i);
       amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
                                fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)))));
       amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))),
                                fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)))));
+      bad = nonfinite_fold(nonfinite_fold(nonfinite_fold(nonfinite_fold(bad, bf16_lo(v.x)),
+                                                         bf16_hi(v.x)),
+                                          bf16_lo(v.y)),
+                           bf16_hi(v.y));
+      bad = nonfinite_fold(nonfinite_fold(nonfinite_fold(nonfinite_fold(bad, bf16_lo(v.z)),
+                                                         bf16_hi(v.z)),
+                                          bf16_lo(v.w)),
+                           bf16_hi(v.w));
     }
+    report_nonfinite(status, bad);
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
     const float s = scale_from_amax(amax);
@@ -192,22 +217,22 @@ cudaError_t launch_mx_quant_e2m1(const uint16_t* x, int64_t M, int64_t K, uint8_
 }
 
 cudaError_t launch_quant_rows(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,
-                              cudaStream_t s) {
+                              int32_t* status, cudaStream_t s) {
   if (M == 0) return cudaSuccess;
   const int grid = static_cast<int>(std::min<int64_t>((M + 7) / 8, num_sms() * 8));
   quant_row_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), M, K / 8,
-                                        reinterpret_cast<uint2*>(xq), xs);
+                                        reinterpret_cast<uint2*>(xq), xs, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_g128(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,
-                              cudaStream_t s) {
+                              int32_t* status, cudaStream_t s) {
   const int64_t groups = M * (K / 128);
   if (groups == 0) return cudaSuccess;
   const int64_t warps = (groups + 2 * kQuantUnroll - 1) / (2 * kQuantUnroll);
   const int grid = static_cast<int>(std::min<int64_t>((warps + 7) / 8, num_sms() * 8));
   quant_g128_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), groups,
-                                         reinterpret_cast<uint2*>(xq), xs);
+                                         reinterpret_cast<uint2*>(xq), xs, status);
   return cudaGetLastError();
 }
 
@@ -218,7 +243,8 @@ cudaError_t launch_quant_per_tensor(const uint16_t* x, int64_t M, int64_t K, uin
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((n8 + 255) / 256, num_sms() * 4)));
   if (n8 > 0) {
-    amax_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), n8, &hdr->amax_bits);
+    amax_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), n8, &hdr->amax_bits,
+                                     &hdr->status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -261,7 +261,8 @@ __global__ void permute_copy_kernel(const uint8_t* __restrict__ xq, const float*
 // scale to the token's k expert rows.  Two groups per warp step.
 __global__ void permute_quant_copy_kernel(const uint4* __restrict__ x, int64_t T, int k,
                                           int64_t H, const int32_t* __restrict__ token_row,
-                                          uint8_t* __restrict__ aq, float* __restrict__ as) {
+                                          uint8_t* __restrict__ aq, float* __restrict__ as,
+                                          int32_t* status) {
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4, hl = lane & 15;
   const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
@@ -283,9 +284,13 @@ __global__ void permute_quant_copy_kernel(const uint4* __restrict__ x, int64_t T
         const bool in = g < G;
         const float f[8] = {bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y),
                             bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w)};
-        float amax = 0.0f;
+        float amax = 0.0f, bad = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        for (int i = 0; i < 8; ++i) {
+          amax = fmaxf(amax, fabsf(f[i]));
+          bad = nonfinite_fold(bad, f[i]);
+        }
+        report_nonfinite(status, bad);
 #pragma unroll
         for (int d = 8; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
         const float sc = scale_from_amax(amax);
@@ -309,13 +314,13 @@ __global__ void permute_quant_copy_kernel(const uint4* __restrict__ x, int64_t T
 cudaError_t launch_permute_quant(const int32_t* ids, int64_t T, int k, int E,
                                  const uint16_t* x, int64_t H, int32_t* offsets,
                                  int32_t* row_token, int32_t* token_row, uint8_t* aq, float* as,
-                                 void* scratch, cudaStream_t s) {
+                                 void* scratch, int32_t* status, cudaStream_t s) {
   cudaError_t e = launch_permute(ids, T, k, E, nullptr, nullptr, H, offsets, row_token,
                                  token_row, nullptr, nullptr, scratch, s);
   if (e != cudaSuccess || T == 0) return e;
   const int grid = static_cast<int>(std::min<int64_t>((T + 7) / 8, num_sms() * 8));
   permute_quant_copy_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), T, k, H,
-                                                 token_row, aq, as);
+                                                 token_row, aq, as, status);
   return cudaGetLastError();
 }
 

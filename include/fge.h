@@ -21,8 +21,10 @@
  *    order, with no host synchronisation and no branch on tensor values (shapes only).
  *  - Errors: argument, shape and alignment problems return a status before anything is
  *    enqueued.  A launch failure returns FGE_ERR_CUDA.  Problems detected on the device
- *    (a pipeline wait that ran out of its time budget) are written to the status word at
- *    the start of the workspace; read it with fge_read_device_status().
+ *    (a pipeline wait that ran out of its time budget: FGE_ERR_DEVICE_TIMEOUT; an
+ *    activation to quantize that is an infinity or a NaN: FGE_ERR_NONFINITE) are written to
+ *    the status word at the start of the workspace -- the first problem wins -- and the
+ *    kernels finish without trapping; read the word with fge_read_device_status().
  *  - Sizes: K, H and I are multiples of 128 (the scale group); N is a multiple of 128.
  */
 #ifndef FGE_H_
@@ -47,7 +49,9 @@ typedef enum {
   FGE_ERR_CUDA = 6,               /* a CUDA runtime call or launch failed */
   FGE_ERR_DEVICE_TIMEOUT = 7,     /* device status only: a pipeline wait ran out */
   FGE_ERR_NOT_INITIALIZED = 8,    /* fge_init() was not called for the current device */
-  FGE_ERR_EXCEEDS_STATIC_SCRATCH = 9 /* fge_linear_w8a8_noalloc: M*K beyond its fixed scratch */
+  FGE_ERR_EXCEEDS_STATIC_SCRATCH = 9, /* fge_linear_w8a8_noalloc: M*K beyond its fixed scratch */
+  FGE_ERR_NONFINITE = 10          /* device status only: an activation the call quantized was an
+                                     infinity or a NaN (its scale and codes are meaningless) */
 } fge_status;
 
 typedef enum {
@@ -96,6 +100,26 @@ const char* fge_status_string(fge_status status);
 /* Workspace bytes an operation needs for the given sizes (0 for a bad op). */
 size_t fge_workspace_bytes(fge_op op, int64_t a, int64_t b, int64_t c, int E, int k);
 
+/* Host-side ledger of this process's calls into the library (counted from library load
+ * or the last fge_reset_ledger; thread-safe; no device access):
+ *   calls              compute entry-point calls;
+ *   refused            of those, calls refused before anything was enqueued (bad argument,
+ *                      shape, alignment, workspace size, device not initialised, ...);
+ *   layers             fge_moe_layer_forward calls that enqueued their kernels;
+ *   grouped_gemms      grouped W4A8 GEMM launches (stand-alone or inside a layer);
+ *   dense_decode_tile  dense W8A8 GEMMs run with the 16-token decode tile (M <= 16);
+ *   dense_row_tile     dense W8A8 GEMMs run with 128-row tiles. */
+typedef struct {
+  uint64_t calls;
+  uint64_t refused;
+  uint64_t layers;
+  uint64_t grouped_gemms;
+  uint64_t dense_decode_tile;
+  uint64_t dense_row_tile;
+} fge_ledger;
+fge_status fge_read_ledger(fge_ledger* out);
+fge_status fge_reset_ledger(void);
+
 /* Zero the device status word of a workspace (enqueued on `stream`). */
 fge_status fge_clear_device_status(void* workspace, fge_stream_t stream);
 
@@ -112,8 +136,9 @@ fge_status fge_read_device_status(const void* workspace, fge_stream_t stream, in
  * "feat(qwen4_exp) ..." measures against per-tensor, section "Limits").
  * x_bf16: [M, K] bf16.  xq: [M, K] e4m3 codes (out).  xs: [M, K/128] float (G128), [M] float
  * (PER_ROW) or one float (PER_TENSOR) (out).  PER_TENSOR needs a workspace of
- * fge_workspace_bytes(FGE_OP_QUANT_PER_TENSOR, M, K, ...); G128 and PER_ROW take none (may
- * be NULL).
+ * fge_workspace_bytes(FGE_OP_QUANT_PER_TENSOR, M, K, ...); G128 and PER_ROW need none (may
+ * be NULL), but given one of at least 256 bytes they report a non-finite input
+ * (FGE_ERR_NONFINITE) in its status word, as PER_TENSOR always does.
  * M may be 0. */
 fge_status fge_fp8_quant_act(const void* x_bf16, int64_t M, int64_t K, fge_scale_mode mode,
                              uint8_t* xq, float* xs, void* workspace, size_t workspace_bytes,
@@ -292,7 +317,9 @@ fge_status fge_moe_layer_per_token_dispatch(const float* logits, const void* x_b
  * must start at zero itself), so calls whose GPU work overlaps -- on different streams, or
  * from several host threads -- race on it; issue them on one stream or serialise them.
  * Arguments as fge_linear_w8a8: x_bf16 [M, K], wq [N, K] e4m3, w_scale device scalar,
- * y_bf16 [M, N]. */
+ * y_bf16 [M, N].  M may be 0: nothing is read or written then (any pointer may be NULL).
+ * A device-side problem of the last call (see fge_linear_w8a8_noalloc_status) leaves y
+ * incomplete. */
 fge_status fge_linear_w8a8_noalloc(const void* x_bf16, int64_t M, int64_t K, const uint8_t* wq,
                                    const float* w_scale, int64_t N, void* y_bf16,
                                    fge_stream_t stream);

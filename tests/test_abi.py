@@ -60,3 +60,23 @@ def test_calls_without_init_or_with_bad_args_fail_before_launch(mod):
     st = lib.fge_moe_topk_gate(None, 0, 8, 2, None, None, None)
     assert st != 0
     assert lib.fge_init(-1) == 1  # invalid argument
+
+
+def test_ledger_counts_refusals_without_a_gpu(mod):
+    lib = mod.lib()
+    mod.reset_ledger()
+    assert mod.ledger() == {k: 0 for k in ("calls", "refused", "layers", "grouped_gemms",
+                                           "dense_decode_tile", "dense_row_tile")}
+    # three compute calls on a process with no initialised device: all refused before launch
+    assert lib.fge_moe_topk_gate(None, 0, 8, 2, None, None, None) != 0
+    assert lib.fge_moe_combine(None, 0, None, None, 0, 1, 128, 0, None, None) != 0
+    assert lib.fge_rmsnorm(None, 0, 128, 1e-6, None, None) != 0
+    led = mod.ledger()
+    assert led["calls"] == 3 and led["refused"] == 3 and led["layers"] == 0
+    mod.reset_ledger()
+    assert mod.ledger()["calls"] == 0
+
+
+def test_status_strings_cover_the_device_codes(mod):
+    assert "timed out" in mod.status_string(mod.ERR_DEVICE_TIMEOUT)
+    assert "NaN" in mod.status_string(mod.ERR_NONFINITE)

@@ -52,3 +52,45 @@ def test_kernel_key_tracks_the_gemm_sources():
     parts = key.split(":")
     assert len(parts) == 2 and all(len(p) == 16 for p in parts)
     int(parts[0], 16), int(parts[1], 16)
+
+
+class _Inp:
+    def __init__(self, T, H, E, I, k):
+        self.T, self.H, self.E, self.I, self.k = T, H, E, I, k
+
+
+def test_stage_bytes_count_each_tensor_once():
+    inp = _Inp(4096, 2048, 64, 768, 8)
+    b = bench.stage_bytes(inp)
+    r = 4096 * 8
+    assert b["combine"] == r * 2048 * 2 + r * 8 + 4096 * 2048 * 2
+    assert b["quant_g128"] == 4096 * 2048 * 3 + 4096 * 16 * 4
+    assert b["topk_gate"] == 4096 * 64 * 4 + r * 8
+    # the fused routing stage reads bf16 once instead of the codes, so it moves T*H bytes more
+    # than the separate permute minus the separate quantization's own output
+    assert b["permute_quant"] - b["permute"] == 4096 * 2048 - 4096 * 16 * 4
+
+
+def test_layer_work_counts_only_experts_with_rows():
+    inp = _Inp(64, 256, 8, 512, 2)
+    f_all, b_all = bench.layer_work(inp, [16] * 8)
+    f_half, b_half = bench.layer_work(inp, [32, 0] * 4)
+    assert f_all == f_half == 2.0 * 128 * (1024 * 256 + 256 * 512)
+    bank = 1024 * 256 // 2 + 256 * 512 // 2 + (1024 * 2 + 256 * 4) * 4
+    assert b_all - b_half == 4 * bank
+
+
+def test_roofline_fraction_takes_the_slower_floor():
+    # 1 TFLOP at 1000 TF/s = 1 ms; 1 GB at 1000 GB/s = 1 ms; measured 2 ms -> 0.5
+    frac, bound = bench.roofline_frac(1e12, 1e9, 2.0, 1000.0, 1000.0)
+    assert abs(frac - 0.5) < 1e-12
+    frac, bound = bench.roofline_frac(1e12, 4e9, 8.0, 1000.0, 1000.0)
+    assert abs(frac - 0.5) < 1e-12 and bound == "hbm"
+    frac, bound = bench.roofline_frac(4e12, 1e9, 8.0, 1000.0, 1000.0)
+    assert abs(frac - 0.5) < 1e-12 and bound == "tensor"
+
+
+def test_cpu_info_reports_the_core_count():
+    import os
+    info = bench.cpu_info()
+    assert info["nproc"] == os.cpu_count() and info["machine"]

@@ -65,3 +65,68 @@ def test_host_side_refusals(fge):
     # k > E
     st = lib.fge_moe_topk_gate(_p(lg), 16, 8, 9, _p(xq), _p(xs), _s())
     assert st == BAD_SHAPE
+
+
+# ------------------------------------------------------------------ non-finite inputs
+def _layer_inputs(fge):
+    from workloads import moe_inputs
+    inp = moe_inputs("tiny", seed=3)
+    x = torch.from_numpy(inp.x_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    lg = torch.from_numpy(inp.logits).cuda()
+    w_gu, s_gu = fge.w4_prepack(torch.from_numpy(inp.w_gu).cuda(),
+                                torch.from_numpy(inp.s_gu).cuda(), True)
+    w_dn, s_dn = fge.w4_prepack(torch.from_numpy(inp.w_dn).cuda(),
+                                torch.from_numpy(inp.s_dn).cuda())
+    ws = fge.new_workspace(fge.workspace_bytes(fge.OP_MOE_LAYER, inp.T, inp.H, inp.I, inp.E,
+                                               inp.k), x.device)
+    return inp, x, lg, (w_gu, s_gu, w_dn, s_dn), ws
+
+
+@pytest.mark.parametrize("bad", [float("nan"), float("inf"), -float("inf")])
+def test_layer_reports_a_nonfinite_activation(fge, bad):
+    inp, x, lg, banks, ws = _layer_inputs(fge)
+    fge.clear_device_status(ws)
+    fge.moe_layer_forward(lg, x, inp.k, inp.I, *banks, workspace=ws, out_dtype=torch.float32)
+    assert fge.read_device_status(ws) == 0          # finite inputs: nothing reported
+    x2 = x.clone()
+    x2[5, 17] = bad
+    fge.moe_layer_forward(lg, x2, inp.k, inp.I, *banks, workspace=ws, out_dtype=torch.float32)
+    assert fge.read_device_status(ws) == fge.ERR_NONFINITE
+    fge.clear_device_status(ws)                     # and the context keeps working
+    out = fge.moe_layer_forward(lg, x, inp.k, inp.I, *banks, workspace=ws,
+                                out_dtype=torch.float32)
+    assert fge.read_device_status(ws) == 0 and torch.isfinite(out).all()
+
+
+@pytest.mark.parametrize("mode", ["tensor", "g128", "row"])
+def test_quantizers_report_a_nonfinite_activation(fge, mode):
+    x = torch.randn((64, 512), device="cuda").to(torch.bfloat16)
+    x[3, 200] = float("inf")
+    ws = fge.new_workspace(fge.workspace_bytes(fge.OP_QUANT_PER_TENSOR, 64, 512), x.device)
+    fge.clear_device_status(ws)
+    lib = fge.lib()
+    xq = torch.empty((64, 512), dtype=torch.uint8, device="cuda")
+    xs = torch.empty((64 * 4,), dtype=torch.float32, device="cuda")
+    m = {"tensor": fge.SCALE_PER_TENSOR, "g128": fge.SCALE_PER_TOKEN_G128,
+         "row": fge.SCALE_PER_ROW}[mode]
+    st = lib.fge_fp8_quant_act(ctypes.c_void_p(x.data_ptr()), 64, 512, m,
+                               ctypes.c_void_p(xq.data_ptr()), ctypes.c_void_p(xs.data_ptr()),
+                               ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                               ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    assert fge.read_device_status(ws) == fge.ERR_NONFINITE
+
+
+def test_ledger_counts_launches(fge):
+    inp, x, lg, banks, ws = _layer_inputs(fge)
+    fge.reset_ledger()
+    fge.moe_layer_forward(lg, x, inp.k, inp.I, *banks, workspace=ws, out_dtype=torch.float32)
+    wq = torch.zeros((256, 512), dtype=torch.uint8, device="cuda")
+    sw = torch.ones(1, dtype=torch.float32, device="cuda")
+    fge.linear_w8a8(torch.randn((16, 512), device="cuda").to(torch.bfloat16), wq, sw)
+    fge.linear_w8a8(torch.randn((300, 512), device="cuda").to(torch.bfloat16), wq, sw)
+    torch.cuda.synchronize()
+    led = fge.ledger()
+    assert led["layers"] == 1 and led["grouped_gemms"] == 2
+    assert led["dense_decode_tile"] == 1 and led["dense_row_tile"] == 1
+    assert led["refused"] == 0 and led["calls"] >= 3
