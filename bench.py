@@ -42,6 +42,7 @@ L2_FLUSH_BYTES = 256 << 20
 # changed since its capture reports traffic = null.
 KNOWN_GATE_UP_TRAFFIC = {
     ("mid", "43dbc4055150c350:72b05a4e51127510"): 194.80e6,
+    ("mid", "c16c58ceab18302e:38ada4bbcaee05c8"): 195.18e6,
 }
 
 

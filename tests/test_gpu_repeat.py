@@ -66,6 +66,7 @@ def test_mid_gemms_twenty_launches_identical_and_in_parity(fge):
     hq = torch.empty((r, inp.I), dtype=torch.uint8, device=dev)
     hs = torch.empty((r, inp.I // 128), dtype=torch.float32, device=dev)
     y = torch.empty((r, inp.H), dtype=torch.bfloat16, device=dev)
+    fge.clear_device_status(ws)
     first = None
     for it in range(20):
         fge.grouped_gemm_w4a8(p["aq"], p["as_"], p["offsets"], w_gu, s_gu, epilogue="swiglu",
