@@ -43,6 +43,7 @@ L2_FLUSH_BYTES = 256 << 20
 KNOWN_GATE_UP_TRAFFIC = {
     ("mid", "43dbc4055150c350:72b05a4e51127510"): 194.80e6,
     ("mid", "c16c58ceab18302e:38ada4bbcaee05c8"): 195.18e6,
+    ("large", "c16c58ceab18302e:38ada4bbcaee05c8"): 1622.82e6,
 }
 
 

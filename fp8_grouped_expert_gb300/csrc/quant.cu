@@ -10,51 +10,8 @@
 
 namespace fge {
 
-// One 128-value group per 16 lanes; each lane converts 8 bf16 (one 16-byte load).  A warp
-// takes kQuantUnroll pairs of groups per trip and issues all their loads first, so that each
-// lane keeps several 16-byte reads in flight (the kernel is bound by DRAM latency otherwise).
+// 16-byte loads each lane keeps in flight per trip in the flat-array kernels below.
 constexpr int kQuantUnroll = 4;
-__global__ void quant_g128_kernel(const uint4* __restrict__ x, int64_t groups,
-                                  uint2* __restrict__ xq, float* __restrict__ xs,
-                                  int32_t* status) {
-  const int lane = threadIdx.x & 31;
-  const int half = lane >> 4, hl = lane & 15;
-  const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
-  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t g0 = wid * 2; g0 < groups; g0 += nw * 2 * kQuantUnroll) {
-    uint4 v[kQuantUnroll];
-#pragma unroll
-    for (int u = 0; u < kQuantUnroll; ++u) {
-      const int64_t g = g0 + u * nw * 2 + half;
-      v[u] = g < groups ? __ldcs(x + g * 16 + hl) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int u = 0; u < kQuantUnroll; ++u) {
-      const int64_t g = g0 + u * nw * 2 + half;
-      const float f[8] = {bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y),
-                          bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w)};
-      float amax = 0.0f, bad = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        amax = fmaxf(amax, fabsf(f[i]));
-        bad = nonfinite_fold(bad, f[i]);
-      }
-      report_nonfinite(status, bad);
-#pragma unroll
-      for (int d = 8; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
-      const float s = scale_from_amax(amax);
-      uint2 q;
-      q.x = cvt_e4m3x4(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s),
-                       __fdiv_rn(f[3], s));
-      q.y = cvt_e4m3x4(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s),
-                       __fdiv_rn(f[7], s));
-      if (g < groups) {
-        xq[g * 16 + hl] = q;
-        if (hl == 0) xs[g] = s;
-      }
-    }
-  }
-}
 
 // Per-tensor pass 1: amax over the tensor, combined across blocks with atomicMax on the
 // float bits (|x| >= 0, so the unsigned order of the bits is the float order).
@@ -222,17 +179,6 @@ cudaError_t launch_quant_rows(const uint16_t* x, int64_t M, int64_t K, uint8_t* 
   const int grid = static_cast<int>(std::min<int64_t>((M + 7) / 8, num_sms() * 8));
   quant_row_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), M, K / 8,
                                         reinterpret_cast<uint2*>(xq), xs, status);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_quant_g128(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,
-                              int32_t* status, cudaStream_t s) {
-  const int64_t groups = M * (K / 128);
-  if (groups == 0) return cudaSuccess;
-  const int64_t warps = (groups + 2 * kQuantUnroll - 1) / (2 * kQuantUnroll);
-  const int grid = static_cast<int>(std::min<int64_t>((warps + 7) / 8, num_sms() * 8));
-  quant_g128_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), groups,
-                                         reinterpret_cast<uint2*>(xq), xs, status);
   return cudaGetLastError();
 }
 

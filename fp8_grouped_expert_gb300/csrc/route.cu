@@ -102,29 +102,53 @@ __global__ void permute_count_kernel(const int32_t* __restrict__ ids, int64_t T,
     chunk_counts[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
 }
 
-// (2) exclusive scan: offsets[e] and, in place, the first row of (chunk, expert)
+// (2) exclusive scan: offsets[e] and, in place, the first row of (chunk, expert).  The 1024
+// threads split as P = 1024 / E' threads per expert (E' = E rounded up to a power of two),
+// thread j of an expert owning a contiguous slice of the chunks, so that the chain of
+// dependent loads per thread is chunks / P long instead of chunks.
 __global__ void permute_scan_kernel(int32_t* __restrict__ chunk_counts, int64_t chunks, int E,
                                     int32_t* __restrict__ offsets) {
-  __shared__ int totals[1024];
+  __shared__ int part_sum[1024];   // slice sums, then slice bases within the expert
+  __shared__ int totals[1024];     // per expert: total, then the expert's first row
   __shared__ int warp_sums[32];
-  const int e = threadIdx.x;
+  int ep2 = 1;
+  while (ep2 < E) ep2 <<= 1;
+  const int P = static_cast<int>(blockDim.x) / ep2;  // >= 1 (E <= 1024)
+  const int t = threadIdx.x;
+  const int e = t / P, j = t - (t / P) * P;
+  const int64_t per = (chunks + P - 1) / P;
+  const int64_t c0 = j * per < chunks ? j * per : chunks;
+  const int64_t c1 = c0 + per < chunks ? c0 + per : chunks;
+  // pass 1: this slice's count
   int run = 0;
   if (e < E) {
-    // 8 independent loads in flight per step instead of one dependent load per chunk
-    for (int64_t c0 = 0; c0 < chunks; c0 += 8) {
+    for (int64_t c = c0; c < c1; c += 8) {
       int cnt[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) cnt[j] = c0 + j < chunks ? chunk_counts[(c0 + j) * E + e] : 0;
+      for (int i = 0; i < 8; ++i) cnt[i] = c + i < c1 ? chunk_counts[(c + i) * E + e] : 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (c0 + j < chunks) chunk_counts[(c0 + j) * E + e] = run;
-        run += cnt[j];
-      }
+      for (int i = 0; i < 8; ++i) run += cnt[i];
     }
   }
-  // block-wide exclusive scan of the per-expert totals
-  const int lane = e & 31, w = e >> 5;
-  int incl = run;
+  part_sum[t] = run;
+  __syncthreads();
+  // slice bases within the expert, and the expert's total
+  int base = 0, total = 0;
+  if (e < E) {
+    for (int i = 0; i < P; ++i) {
+      const int v = part_sum[e * P + i];
+      if (i < j) base += v;
+      total += v;
+    }
+  }
+  __syncthreads();
+  part_sum[t] = base;
+  if (e < E && j == 0) totals[e] = total;
+  __syncthreads();
+  // block-wide exclusive scan of the per-expert totals (thread x holds expert x)
+  const int lane = t & 31, w = t >> 5;
+  const int my_total = t < E ? totals[t] : 0;
+  int incl = my_total;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
     const int v = __shfl_up_sync(0xffffffffu, incl, d);
@@ -133,7 +157,7 @@ __global__ void permute_scan_kernel(int32_t* __restrict__ chunk_counts, int64_t 
   if (lane == 31) warp_sums[w] = incl;
   __syncthreads();
   if (w == 0) {
-    int ws = lane < (blockDim.x >> 5) ? warp_sums[lane] : 0;
+    const int ws = lane < static_cast<int>(blockDim.x >> 5) ? warp_sums[lane] : 0;
     int wi = ws;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -143,14 +167,27 @@ __global__ void permute_scan_kernel(int32_t* __restrict__ chunk_counts, int64_t 
     warp_sums[lane] = wi - ws;
   }
   __syncthreads();
-  const int excl = warp_sums[w] + incl - run;
-  totals[e] = excl;
-  if (e < E) offsets[e] = excl;
-  if (e == E - 1) offsets[E] = excl + run;
+  const int excl = warp_sums[w] + incl - my_total;
   __syncthreads();
+  if (t < E) {
+    totals[t] = excl;
+    offsets[t] = excl;
+    if (t == E - 1) offsets[E] = excl + my_total;
+  }
+  __syncthreads();
+  // pass 2: each slice writes the first row of (chunk, expert) for its chunks
   if (e < E) {
-#pragma unroll 8
-    for (int64_t c = 0; c < chunks; ++c) chunk_counts[c * E + e] += totals[e];
+    int row = totals[e] + part_sum[t];
+    for (int64_t c = c0; c < c1; c += 8) {
+      int cnt[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) cnt[i] = c + i < c1 ? chunk_counts[(c + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (c + i < c1) chunk_counts[(c + i) * E + e] = row;
+        row += cnt[i];
+      }
+    }
   }
 }
 
@@ -259,6 +296,9 @@ __global__ void permute_copy_kernel(const uint8_t* __restrict__ xq, const float*
 // each 128-value group exactly as quant_g128_kernel does (16 lanes x 8 values, shuffle amax,
 // s = amax / 448, IEEE division, e4m3 round to nearest even) and writes the codes and the
 // scale to the token's k expert rows.  Two groups per warp step.
+// kIdentity: the plain G128 quantization of x (k = 1, row t to row t, no token_row), the
+// same row-per-warp structure writing each row's codes and scales contiguously.
+template <bool kIdentity>
 __global__ void permute_quant_copy_kernel(const uint4* __restrict__ x, int64_t T, int k,
                                           int64_t H, const int32_t* __restrict__ token_row,
                                           uint8_t* __restrict__ aq, float* __restrict__ as,
@@ -270,7 +310,8 @@ __global__ void permute_quant_copy_kernel(const uint4* __restrict__ x, int64_t T
   const int64_t G = H / 128;
   constexpr int U = 4;  // group pairs per trip: their loads are issued together
   for (int64_t t = wid; t < T; t += nw) {
-    const int my_row = lane < k ? __ldg(token_row + t * k + lane) : 0;
+    const int my_row = kIdentity ? static_cast<int>(t)
+                                 : (lane < k ? __ldg(token_row + t * k + lane) : 0);
     for (int64_t g0 = 0; g0 < G; g0 += 2 * U) {  // all lanes iterate; shuffles stay full
       uint4 v[U];
 #pragma unroll
@@ -319,8 +360,8 @@ cudaError_t launch_permute_quant(const int32_t* ids, int64_t T, int k, int E,
                                  token_row, nullptr, nullptr, scratch, s);
   if (e != cudaSuccess || T == 0) return e;
   const int grid = static_cast<int>(std::min<int64_t>((T + 7) / 8, num_sms() * 8));
-  permute_quant_copy_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), T, k, H,
-                                                 token_row, aq, as, status);
+  permute_quant_copy_kernel<false><<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), T, k,
+                                                        H, token_row, aq, as, status);
   return cudaGetLastError();
 }
 
@@ -419,6 +460,17 @@ cudaError_t launch_combine(const void* y, int y_f32, const int32_t* token_row,
   else if (y_f32) combine_kernel<true, false><<<grid, 256, 0, s>>>(y, token_row, gates, T, k, H, out);
   else if (out_f32) combine_kernel<false, true><<<grid, 256, 0, s>>>(y, token_row, gates, T, k, H, out);
   else combine_kernel<false, false><<<grid, 256, 0, s>>>(y, token_row, gates, T, k, H, out);
+  return cudaGetLastError();
+}
+
+// The stand-alone G128 activation quantization: the quantizing copy in its identity form
+// (one warp per row, the row's codes and scales written contiguously).
+cudaError_t launch_quant_g128(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,
+                              int32_t* status, cudaStream_t s) {
+  if (M == 0) return cudaSuccess;
+  const int grid = static_cast<int>(std::min<int64_t>((M + 7) / 8, num_sms() * 8));
+  permute_quant_copy_kernel<true><<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), M, 1, K,
+                                                       nullptr, xq, xs, status);
   return cudaGetLastError();
 }
 

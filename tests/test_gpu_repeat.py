@@ -5,7 +5,8 @@
   the results meet the parity rules on 256 sampled rows (elementwise GEMM bound for down,
   scales within 1e-4 and at most 0.5% of codes one step apart for the SwiGLU codes).
 * The large layer's GEMMs (K=4096, N=3072 and K=1536, N=4096, 131072 routed rows over 128
-  Zipf-skewed experts) against the oracle on 256 sampled rows under the same rules.
+  Zipf-skewed experts) against the oracle on about 256 sampled rows (from the hottest expert,
+  the smallest one and at random) under the same rules.
 * The layer's quantizing permutation (fge_moe_permute_quant) against the oracle's G128
   quantization followed by its permutation, bit for bit, at the mid and large sizes."""
 
@@ -95,7 +96,8 @@ def test_large_shape_gemms_on_sampled_rows(fge):
     p_host = {k: host(p[k]) for k in ("aq", "as_", "offsets")}
     off = p_host["offsets"]
     counts = np.diff(off)
-    assert counts.max() > 10 * counts.mean() and (counts == 0).any()
+    # Zipf-skewed routing: the hottest expert far above the mean, the coldest nearly empty
+    assert counts.max() > 10 * counts.mean() and counts.min() < counts.mean() / 100
     rng = np.random.default_rng(4)
     # rows of the hottest expert, of the smallest non-empty one, and random ones
     hot = int(np.argmax(counts))
