@@ -299,6 +299,12 @@ def run_gpu(args):
     stages = stage_times(fge, torch, inp, x, logits, w_gu, s_gu, w_dn, s_dn, fmt, flush, dev,
                          args.steps)
 
+    # ---- the combine folded into the down GEMM's epilogue (bit-identical output), timed
+    #      the same way as a step, beside the plain layer
+    fused_ms = timed_calls(torch, lambda: fge.moe_layer_forward(
+        logits, x, inp.k, inp.I, w_gu, s_gu, w_dn, s_dn, fmt=fmt, workspace=ws, out=out,
+        fused_combine=True), flush, stream, 3, max(3, args.steps))
+
     # ---- FP4 activations (E2M1 + a power-of-two scale per 32): the dispatch-buffer half of
     #      the E2M1 row, timed beside the e4m3 G128 quantization (not part of the step)
     mx_ms = mx_quant_time(fge, torch, x, flush, dev, args.steps)
@@ -437,6 +443,11 @@ def run_gpu(args):
             "e4m3_g128_bytes_written": inp.T * inp.H + inp.T * inp.H // 128 * 4,
             "what": "fge_mx_quant_e2m1 on the layer's activations: E2M1 codes + E8M0 scale "
                     "per 32 values (dispatch bytes), against the e4m3 G128 quantization"},
+        "fused_combine": {
+            "ms_per_step": fused_ms, "plain_ms_per_step": ms,
+            "what": "fge_moe_layer_forward_fused_combine: the k-th slot row of each (token, "
+                    "128-column chunk) to leave the down GEMM sums the chunk in slot order "
+                    "inside the epilogue (no combine kernel; bit-identical output)"},
         "per_token_dispatch_baseline": None if base_ms is None else {
             "ms_per_step": base_ms, "grouped_speedup": base_ms / ms,
             "what": "same layer, one CTA per routed token: int4 weights dequantized in "

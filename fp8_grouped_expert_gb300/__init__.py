@@ -63,6 +63,8 @@ SIGNATURES = {
     "fge_linear_w8a8_noalloc_status": [_P, ctypes.POINTER(ctypes.c_int32)],
     "fge_moe_layer_forward": [_P, _P, _I64, _I64, _I, _I, _I64, _P, _P, _P, _P, _I, _I, _P, _P,
                               _SZ, _P],
+    "fge_moe_layer_forward_fused_combine": [_P, _P, _I64, _I64, _I, _I, _I64, _P, _P, _P, _P,
+                                            _I, _P, _P, _SZ, _P],
     "fge_selftest_wait_timeout": [_P, _I64, _P],
     "fge_rmsnorm": [_P, _I64, _I64, ctypes.c_float, _P, _P],
     "fge_router_logits": [_P, _P, _I64, _I64, _I, _P, _P],
@@ -444,15 +446,27 @@ def linear_w8a8_rows(x, wq, w_scale, workspace=None, out=None):
 
 
 def moe_layer_forward(logits, x, k, inter, w_gu_dev, s_gu_dev, w_dn_dev, s_dn_dev,
-                      fmt=W4_SUBNORMAL, out_dtype=torch.bfloat16, workspace=None, out=None):
+                      fmt=W4_SUBNORMAL, out_dtype=torch.bfloat16, workspace=None, out=None,
+                      fused_combine=False):
+    """One MoE FFN layer.  fused_combine: the combine runs in the down GEMM's epilogue
+    (fge_moe_layer_forward_fused_combine; bf16 output, bit-identical to the plain call)."""
     _need(logits, torch.float32, "logits")
     _need(x, torch.bfloat16, "x")
     _ensure_init(x.device)
     t, h = x.shape
     e = logits.shape[1]
+    if fused_combine and out_dtype != torch.bfloat16:
+        raise FgeError("fused_combine writes a bf16 output")
     ws = workspace if workspace is not None else new_workspace(
         workspace_bytes(OP_MOE_LAYER, t, h, inter, e, k), x.device)
     y = out if out is not None else torch.empty((t, h), dtype=out_dtype, device=x.device)
+    if fused_combine:
+        _need(y, torch.bfloat16, "out")
+        _check(lib().fge_moe_layer_forward_fused_combine(
+            _ptr(logits), _ptr(x), t, h, e, k, inter, _ptr(w_gu_dev), _ptr(s_gu_dev),
+            _ptr(w_dn_dev), _ptr(s_dn_dev), fmt, _ptr(y), _ptr(ws), ws.numel(), _stream(x)),
+            "fge_moe_layer_forward_fused_combine")
+        return y
     _check(lib().fge_moe_layer_forward(_ptr(logits), _ptr(x), t, h, e, k, inter, _ptr(w_gu_dev),
                                        _ptr(s_gu_dev), _ptr(w_dn_dev), _ptr(s_dn_dev), fmt,
                                        DTYPE_F32 if out_dtype == torch.float32 else DTYPE_BF16,

@@ -70,6 +70,8 @@ struct LayerWs {
   uint8_t* hq;
   float* hs;
   void* y;
+  int32_t* comb_count;
+  FusedCombine* comb_args;
   size_t bytes;
 };
 
@@ -96,6 +98,8 @@ LayerWs carve_layer(void* base, int64_t T, int64_t H, int64_t I, int E, int k) {
   w.hq = static_cast<uint8_t*>(take(R * I));
   w.hs = static_cast<float*>(take(R * (I / 128) * 4));
   w.y = take(R * H * 4);
+  w.comb_count = static_cast<int32_t*>(take(T * (H / 128) * 4));
+  w.comb_args = static_cast<FusedCombine*>(take(sizeof(FusedCombine)));
   w.bytes = off;
   return w;
 }
@@ -323,7 +327,8 @@ static fge_status grouped_common(const uint8_t* aq, const float* as, const int32
                                  int epilogue, void* out, float* out_scales, void* ws,
                                  size_t ws_bytes, fge_stream_t stream,
                                  const float* sa_rows = nullptr,
-                                 const int32_t* row_token = nullptr, int64_t rows_a = 0) {
+                                 const int32_t* row_token = nullptr, int64_t rows_a = 0,
+                                 const FusedCombine* comb = nullptr) {
   FGE_REQUIRE(R >= 0 && R < (1LL << 31) && N > 0 && N % 128 == 0 && N < (1LL << 24) && K > 0 &&
                   K % 128 == 0 && K < (1LL << 24),
               FGE_ERR_BAD_SHAPE);
@@ -353,6 +358,7 @@ static fge_status grouped_common(const uint8_t* aq, const float* as, const int32
   a.out = out;
   a.out_scales = out_scales;
   a.status = &static_cast<WsHeader*>(ws)->status;
+  a.comb = comb;
   fge_status st = FGE_OK;
   const cudaError_t e = launch_grouped_gemm(a, stream, &st);
   if (e != cudaSuccess) return FGE_ERR_CUDA;
@@ -485,15 +491,19 @@ fge_status fge_linear_w8a8_rows(const void* x, int64_t M, int64_t K, const uint8
                         nullptr, ws, ws_bytes, stream, xs);
 }
 
-fge_status fge_moe_layer_forward(const float* logits, const void* x, int64_t T, int64_t H, int E,
-                                 int k, int64_t I, const uint8_t* w_gu, const float* s_gu,
-                                 const uint8_t* w_dn, const float* s_dn, fge_w4_format format,
-                                 fge_dtype out_dtype, void* out, void* ws, size_t ws_bytes,
-                                 fge_stream_t stream) {
+// One MoE FFN layer: top-k gate, permutation with the G128 quantization in the row copy,
+// gate_up GEMM with the fused SwiGLU requant, down GEMM, combine.  fused_combine: the
+// combine runs inside the down GEMM's epilogue (bf16 output only) instead of as a kernel.
+static fge_status layer_forward(const float* logits, const void* x, int64_t T, int64_t H, int E,
+                                int k, int64_t I, const uint8_t* w_gu, const float* s_gu,
+                                const uint8_t* w_dn, const float* s_dn, fge_w4_format format,
+                                fge_dtype out_dtype, void* out, void* ws, size_t ws_bytes,
+                                fge_stream_t stream, bool fused_combine) {
   FGE_CHECK(cur_device_ok());
   FGE_REQUIRE(logits && x && w_gu && s_gu && w_dn && s_dn && out && ws, FGE_ERR_INVALID_ARG);
   FGE_REQUIRE(format == FGE_W4_LUT || format == FGE_W4_SUBNORMAL, FGE_ERR_INVALID_ARG);
-  FGE_REQUIRE(out_dtype == FGE_DTYPE_BF16 || out_dtype == FGE_DTYPE_F32, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(out_dtype == FGE_DTYPE_BF16 || (out_dtype == FGE_DTYPE_F32 && !fused_combine),
+              FGE_ERR_INVALID_ARG);
   FGE_REQUIRE(T >= 0 && H > 0 && H % 128 == 0 && I > 0 && I % 128 == 0, FGE_ERR_BAD_SHAPE);
   FGE_REQUIRE(E >= 1 && E <= kMaxExperts && k >= 1 && k <= E && k <= 32, FGE_ERR_BAD_SHAPE);
   FGE_REQUIRE(T * k < (1LL << 31) && (2 * I) % 256 == 0, FGE_ERR_BAD_SHAPE);
@@ -527,6 +537,16 @@ fge_status fge_moe_layer_forward(const float* logits, const void* x, int64_t T, 
     FGE_CHECK(grouped_common(w.aq, w.as, w.offsets, R, w_gu, s_gu, E, 2 * I, H, format, 0,
                              nullptr, 2, w.hq, w.hs, ws, ws_bytes, stream));
   }
+  if (fused_combine) {
+    NvtxRange r("fge.down_gemm_combine");
+    const FusedCombine comb{out, w.row_token, w.token_row, w.gates, w.comb_count, k};
+    FGE_CHECK(from_cuda(launch_combine_setup(comb, T * (H / 128), w.comb_args, stream)));
+    const fge_status st = grouped_common(w.hq, w.hs, w.offsets, R, w_dn, s_dn, E, H, I, format,
+                                         0, nullptr, 1, w.y, nullptr, ws, ws_bytes, stream,
+                                         nullptr, nullptr, 0, w.comb_args);
+    if (st == FGE_OK) ledger_note(kLedLayers);
+    return st;
+  }
   {
     NvtxRange r("fge.down_gemm");
     FGE_CHECK(grouped_common(w.hq, w.hs, w.offsets, R, w_dn, s_dn, E, H, I, format, 0, nullptr,
@@ -537,6 +557,25 @@ fge_status fge_moe_layer_forward(const float* logits, const void* x, int64_t T, 
                                                  out_f32, out, stream));
   if (st == FGE_OK) ledger_note(kLedLayers);
   return st;
+}
+
+fge_status fge_moe_layer_forward(const float* logits, const void* x, int64_t T, int64_t H, int E,
+                                 int k, int64_t I, const uint8_t* w_gu, const float* s_gu,
+                                 const uint8_t* w_dn, const float* s_dn, fge_w4_format format,
+                                 fge_dtype out_dtype, void* out, void* ws, size_t ws_bytes,
+                                 fge_stream_t stream) {
+  return layer_forward(logits, x, T, H, E, k, I, w_gu, s_gu, w_dn, s_dn, format, out_dtype, out,
+                       ws, ws_bytes, stream, false);
+}
+
+fge_status fge_moe_layer_forward_fused_combine(const float* logits, const void* x, int64_t T,
+                                               int64_t H, int E, int k, int64_t I,
+                                               const uint8_t* w_gu, const float* s_gu,
+                                               const uint8_t* w_dn, const float* s_dn,
+                                               fge_w4_format format, void* out, void* ws,
+                                               size_t ws_bytes, fge_stream_t stream) {
+  return layer_forward(logits, x, T, H, E, k, I, w_gu, s_gu, w_dn, s_dn, format, FGE_DTYPE_BF16,
+                       out, ws, ws_bytes, stream, true);
 }
 
 fge_status fge_moe_layer_per_token_dispatch(const float* logits, const void* x, int64_t T,

@@ -62,6 +62,18 @@ cudaError_t launch_w4_prepack(const uint8_t* w, const float* sw, int E, int64_t 
                               cudaStream_t s);
 
 // Grouped GEMM.  mode: 0 = int4 bank with per-group scales, 1 = e4m3 weights, per-tensor.
+// The combine folded into the down GEMM's bf16 epilogue: every routed row's 128-column
+// chunk counts its arrival per (token, chunk); the k-th arrival sums the token's k slot rows
+// of that chunk, gate-weighted in slot order, into out.
+struct FusedCombine {
+  void* out;                  // [T, N] bf16, or null (no fused combine)
+  const int32_t* row_token;   // [R] token of routed row r
+  const int32_t* token_row;   // [T, k] routed row of (token, slot)
+  const float* gates;         // [T, k]
+  int32_t* count;             // [T, N/128] arrival counters, zero before the launch
+  int k;
+};
+
 struct GroupedGemmArgs {
   const uint8_t* aq;        // [R, K] e4m3 codes
   const float* as;          // [R, K/128] (group mode)
@@ -81,7 +93,13 @@ struct GroupedGemmArgs {
   void* out;
   float* out_scales;
   int32_t* status;
+  const FusedCombine* comb;  // down GEMM, bf16 store: the combine folded in (device memory,
+                            // written by launch_combine_setup), or null
 };
+// Zeroes the arrival counters (n of them) and writes c to dst (device memory) for the down
+// GEMM's folded combine; one launch, stream-ordered.
+cudaError_t launch_combine_setup(const FusedCombine& c, int64_t n, FusedCombine* dst,
+                                 cudaStream_t s);
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st);
 
 cudaError_t launch_rmsnorm(const float* h, int64_t T, int64_t H, float eps, uint16_t* out,

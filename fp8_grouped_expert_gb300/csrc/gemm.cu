@@ -41,6 +41,8 @@ struct GemmParams {
   int dense_rows;          // offsets == nullptr: one expert owning rows [0, dense_rows)
   int swap_m;              // BN = 16 (decode sizes): tokens in the B tile; out is [swap_m, out_ld]
   int out_ld;
+  const FusedCombine* comb; // bf16 group-mode store: the combine folded into the epilogue
+                           // (device memory; null: plain store)
 };
 
 constexpr int align16(int x) { return (x + 15) / 16 * 16; }
@@ -651,7 +653,7 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
           }
           if (valid && wg == 0)
             p.out_scales[static_cast<size_t>(row) * (inter / 128) + ti.n0 / 256] = s;
-        } else if (C::kStageOut && ti.rows == 128) {
+        } else if (C::kStageOut && ti.rows == 128 && p.comb == nullptr) {
           // full tile, bf16: each warp stores its 32 rows in eight 16-column chunks from its
           // own 2 KB slice, two 1 KB halves used in turn (row r at r * 32 bytes, 16-byte
           // pieces swizzled by (r / 4) % 2 as the tensor map's 32-byte swizzle expects), so
@@ -702,6 +704,47 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
                     pack_bf16x2(lo_f32(acc2[(c * 32 + i) / 2 + 1]), hi_f32(acc2[(c * 32 + i) / 2 + 1])),
                     pack_bf16x2(lo_f32(acc2[(c * 32 + i) / 2 + 2]), hi_f32(acc2[(c * 32 + i) / 2 + 2])),
                     pack_bf16x2(lo_f32(acc2[(c * 32 + i) / 2 + 3]), hi_f32(acc2[(c * 32 + i) / 2 + 3])));
+            }
+          }
+        }
+        if constexpr (EPI == kEpiBf16) {
+          if (p.comb != nullptr) {
+            const FusedCombine cb = *p.comb;
+            // Combine folded into the epilogue.  This thread's 128 columns of routed row `row`
+            // are in y (plain stores above); after a fence it counts their arrival for
+            // (token, chunk).  The k-th arrival, whichever slot row it is, combines the chunk:
+            // the whole warp sums the token's k slot rows in slot order with the same fmaf
+            // chain as the combine kernel, so the result is bit-identical to it.
+            const int nchunk = p.N / 128;
+            const int chunk = (ti.n0 + col_a) / 128;  // the same for every lane of the warp
+            int64_t tok = 0;
+            bool last = false;
+            if (valid) {
+              tok = __ldg(cb.row_token + row);
+              __threadfence();
+              last = atomicAdd(cb.count + tok * nchunk + chunk, 1) == cb.k - 1;
+            }
+            unsigned todo = __ballot_sync(0xffffffffu, last);
+            if (todo) __threadfence();  // the other slot rows' stores, ordered by the counter
+            const int64_t c = static_cast<int64_t>(chunk) * 128 + lane * 4;
+            const uint16_t* yb = reinterpret_cast<const uint16_t*>(p.out);
+            while (todo) {
+              const int src = __ffs(todo) - 1;
+              todo &= todo - 1;
+              const int64_t t = __shfl_sync(0xffffffffu, tok, src);
+              float acc0 = 0.0f, acc1 = 0.0f, acc2c = 0.0f, acc3 = 0.0f;
+#pragma unroll 8
+              for (int j = 0; j < cb.k; ++j) {
+                const int64_t r = __ldg(cb.token_row + t * cb.k + j);
+                const float g = __ldg(cb.gates + t * cb.k + j);
+                const uint2 v = __ldcg(reinterpret_cast<const uint2*>(yb + r * p.N + c));
+                acc0 = fmaf(g, bf16_lo(v.x), acc0);
+                acc1 = fmaf(g, bf16_hi(v.x), acc1);
+                acc2c = fmaf(g, bf16_lo(v.y), acc2c);
+                acc3 = fmaf(g, bf16_hi(v.y), acc3);
+              }
+              *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(cb.out) + t * p.N + c) =
+                  make_uint2(pack_bf16x2(acc0, acc1), pack_bf16x2(acc2c, acc3));
             }
           }
         }
@@ -909,6 +952,7 @@ static cudaError_t run(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st)
   p.out = a.out;
   p.out_scales = a.out_scales;
   p.status = a.status;
+  p.comb = a.comb;
   p.E = a.E;
   p.N = static_cast<int>(a.N);
   p.K = static_cast<int>(a.K);

@@ -450,6 +450,22 @@ __global__ void combine_kernel(const void* __restrict__ y, const int32_t* __rest
   }
 }
 
+// Arrival counters of the combine folded into the down GEMM set to zero, and the combine's
+// arguments written where the GEMM reads them.
+__global__ void combine_setup_kernel(FusedCombine c, int64_t n, FusedCombine* dst) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) *dst = c;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    c.count[i] = 0;
+}
+
+cudaError_t launch_combine_setup(const FusedCombine& c, int64_t n, FusedCombine* dst,
+                                 cudaStream_t s) {
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, 4L * num_sms());
+  combine_setup_kernel<<<static_cast<int>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(c, n, dst);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_combine(const void* y, int y_f32, const int32_t* token_row,
                            const float* gates, int64_t T, int k, int64_t H, int out_f32,
                            void* out, cudaStream_t s) {

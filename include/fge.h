@@ -344,6 +344,24 @@ fge_status fge_moe_layer_forward(const float* logits, const void* x_bf16, int64_
                                  fge_dtype out_dtype, void* out, void* workspace,
                                  size_t workspace_bytes, fge_stream_t stream);
 
+/* moe_layer_forward_fused_combine -- fge_moe_layer_forward with the combine folded into the
+ * down GEMM's epilogue (the "fuse the edges" step of "FP8 grouped-expert prefill ...":
+ * gate_up -> SwiGLU -> down -> combine with no combine kernel of its own).  Every routed
+ * row's 128-column chunk is stored to the workspace's expert-output buffer as usual, then
+ * counted per (token, chunk) with a device-scope atomic; the k-th arrival -- whichever slot
+ * row lands last -- sums the token's k slot rows of that chunk, gate-weighted, in slot order
+ * with float32 fmaf, exactly as the combine kernel does.  The output is therefore
+ * bit-identical to fge_moe_layer_forward with out_dtype BF16, whatever order the tiles run
+ * in: no float atomics.  out: [T, H] bf16.  Same arguments, workspace (FGE_OP_MOE_LAYER) and
+ * errors as fge_moe_layer_forward; the arrival counters live in the workspace and are
+ * cleared on the stream by each call. */
+fge_status fge_moe_layer_forward_fused_combine(const float* logits, const void* x_bf16,
+                                               int64_t T, int64_t H, int E, int k, int64_t I,
+                                               const uint8_t* w_gu_dev, const float* s_gu_dev,
+                                               const uint8_t* w_dn_dev, const float* s_dn_dev,
+                                               fge_w4_format format, void* out, void* workspace,
+                                               size_t workspace_bytes, fge_stream_t stream);
+
 /* selftest_wait_timeout -- exercises the device failure path without faulting anything: a
  * one-warp kernel waits on an mbarrier that is never arrived on, with a budget of
  * budget_cycles (1 .. 2^32) SM clock cycles; the wait gives up, writes
