@@ -49,6 +49,7 @@ from .mx import (  # noqa: F401
     mx_block_exponent,
     mx_quant_e2m1,
     mx_dequant_e2m1,
+    grouped_gemm_mxf4_w4,
 )
 from .moe import (  # noqa: F401
     topk_gate,

@@ -17,6 +17,8 @@ an all-zero block.
 
 import numpy as np
 
+from .fp8 import int4_unpack
+
 E2M1_MAX = 6.0
 MX_BLOCK = 32
 # the eight E2M1 magnitudes, indexed by the 3-bit code (exponent bits 2..1, mantissa bit 0)
@@ -119,3 +121,40 @@ def mx_dequant_e2m1(packed, scales):
     out[:, 1::2] = table[packed >> 4]
     sc = 2.0 ** (scales.astype(np.float64) - 127.0)
     return out * np.repeat(sc, MX_BLOCK, axis=1)
+
+
+def grouped_gemm_mxf4_w4(codes, scales, offsets, w_packed, w_scale):
+    """Grouped expert GEMM with MXFP4 activations and the int4 expert banks.
+
+    "[RFC] Support FP4 (E2M1) activation dispatch in MegaMoE": the dispatched activations are
+    E2M1 with a shared scale per block and the expert GEMM consumes them in its MX main loop
+    (there, mxf8f6f4 with K = 32 per step when the other operand is 8-bit).  Reading: the
+    weight side stays this method's int4 bank with its per-(output row, 128-K group) scale,
+    which is applied to each group's partial sum as in grouped_gemm_w4a8; the activation
+    side carries one power-of-two scale per 32 values inside the group.  Definition written
+    out: for expert e and its rows r in [offsets[e], offsets[e+1]),
+        C[r, n] = sum_g  sw[e, n, g] * sum_{k in group g} a[r, k] * q[e, n, k],
+        a[r, k] = dec(code[r, k]) * 2^(scale[r, k // 32] - 127).
+    Products have at most 5 significant bits, so each group sum is exact in float64 unless
+    the four block scales of a group span more than about 45 binades; the weight scaling and
+    the outer sum are float64.
+
+    codes uint8 [R, K/2] (element 2b in the low nibble of byte b); scales uint8 [R, K/32];
+    offsets int [E+1]; w_packed uint8 [E, N, K/2]; w_scale float32 [E, N, K/128].
+    Returns float64 [R, N] (rows past offsets[E] are zero).
+    """
+    a = mx_dequant_e2m1(codes, scales)
+    r_total, kdim = a.shape
+    e_count, n, _ = np.asarray(w_packed).shape
+    groups = kdim // 128
+    out = np.zeros((r_total, n), dtype=np.float64)
+    for e in range(e_count):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 == r0:
+            continue
+        w = int4_unpack(w_packed[e], kdim).astype(np.float64)
+        sw = np.asarray(w_scale[e], dtype=np.float64)
+        for g in range(groups):
+            ks = slice(g * 128, (g + 1) * 128)
+            out[r0:r1] += (a[r0:r1, ks] @ w[:, ks].T) * sw[None, :, g]
+    return out

@@ -13,8 +13,10 @@ import pytest
 import oracle
 import oracle.fp8 as ofp8
 import oracle.moe as omoe
+import oracle.mx as omx
 import test_oracle_fp8 as pf
 import test_oracle_moe as pm
+import test_oracle_mx_gemm as pmx
 
 _NAMESPACES = (oracle, ofp8, omoe)
 
@@ -244,3 +246,35 @@ def test_w8a8_missing_weight_scale_is_caught(monkeypatch):
     orig = omoe.linear_w8a8_gemm
     _patch(monkeypatch, "linear_w8a8_gemm", lambda aq, sa, wq, sw: orig(aq, sa, wq, 1.0))
     _must_fail(pm.test_w8a8_exact_power_of_two_case)
+
+
+# --- MXFP4-activation grouped GEMM ---------------------------------------------------------------
+
+def _mx_dequant_with(block):
+    """mx_dequant_e2m1 that applies the scale of the wrong block: k // block instead of k // 32
+    (block 16: twice as many scales read; block 128: one scale per group)."""
+    def deq(packed, scales):
+        packed = np.asarray(packed, dtype=np.uint8)
+        scales = np.asarray(scales, dtype=np.uint8)
+        m, kh = packed.shape
+        table = np.array([omx.e2m1_decode(c) for c in range(16)])
+        out = np.empty((m, 2 * kh), dtype=np.float64)
+        out[:, 0::2] = table[packed & 0xF]
+        out[:, 1::2] = table[packed >> 4]
+        idx = np.minimum(np.arange(2 * kh) // block, scales.shape[1] - 1)
+        return out * 2.0 ** (scales[:, idx].astype(np.float64) - 127.0)
+    return deq
+
+
+@pytest.mark.parametrize("block", [16, 128])
+def test_mx_gemm_wrong_scale_block_is_caught(monkeypatch, block):
+    monkeypatch.setattr(omx, "mx_dequant_e2m1", _mx_dequant_with(block))
+    _must_fail(pmx.test_block_scale_placement_closed_form,
+               pmx.test_equals_w4a8_when_block_scales_agree_within_groups)
+
+
+def test_mx_gemm_wrong_scale_bias_is_caught(monkeypatch):
+    real = omx.mx_dequant_e2m1
+    monkeypatch.setattr(omx, "mx_dequant_e2m1", lambda p, s: real(p, s) * 2.0)   # bias 126
+    _must_fail(pmx.test_block_scale_placement_closed_form,
+               pmx.test_equals_w4a8_when_block_scales_agree_within_groups)
