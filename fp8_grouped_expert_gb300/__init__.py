@@ -49,6 +49,8 @@ SIGNATURES = {
     "fge_w4_prepack": [_P, _P, _I, _I64, _I64, _I, _I, _P, _P, _P],
     "fge_grouped_gemm_w4a8": [_P, _P, _P, _I64, _P, _P, _I, _I64, _I64, _I, _I, _I, _P, _P, _P,
                               _SZ, _P],
+    "fge_grouped_gemm_mxf4_w4": [_P, _P, _P, _I64, _P, _P, _I, _I64, _I64, _I, _I, _P, _P, _SZ,
+                                 _P],
     "fge_grouped_gemm_w4a8_gather": [_P, _P, _I64, _P, _P, _I64, _P, _P, _I, _I64, _I64, _I,
                                      _I, _I, _P, _P, _P, _SZ, _P],
     "fge_swiglu_quant": [_P, _I64, _I64, _P, _P, _P],
@@ -324,6 +326,33 @@ def grouped_gemm_w4a8(aq, as_, offsets, w_dev, s_dev, fmt=W4_SUBNORMAL, epilogue
                                        _ptr(scales), _ptr(ws), ws.numel(), _stream(aq)),
            "fge_grouped_gemm_w4a8")
     return (out, scales) if epilogue == "swiglu" else out
+
+
+def grouped_gemm_mxf4_w4(codes, scales, offsets, w_dev, s_dev, out_dtype=torch.float32,
+                         workspace=None, out=None):
+    """Grouped GEMM with MXFP4 activations (codes uint8 [R, K/2], scales uint8 [R, K/32], as
+    mx_quant_e2m1 returns them) and a subnormal-format int4 bank: out [R, N]."""
+    _need(codes, torch.uint8, "codes")
+    _need(scales, torch.uint8, "scales")
+    _need(offsets, torch.int32, "offsets")
+    _ensure_init(codes.device)
+    r, kh = codes.shape
+    k = 2 * kh
+    e, n, _ = w_dev.shape
+    dev = codes.device
+    ws = workspace if workspace is not None else new_workspace(
+        workspace_bytes(OP_GROUPED_GEMM), dev)
+    if out is None:
+        out = torch.zeros((r, n), dtype=out_dtype, device=dev)
+    _need(out, out_dtype, "out")
+    if tuple(out.shape) != (r, n) or tuple(scales.shape) != (r, k // 32):
+        raise FgeError("out must be [R, N] and scales [R, K/32]")
+    _check(lib().fge_grouped_gemm_mxf4_w4(_ptr(codes), _ptr(scales), _ptr(offsets), r,
+                                          _ptr(w_dev), _ptr(s_dev), e, n, k, W4_SUBNORMAL,
+                                          DTYPE_F32 if out_dtype == torch.float32 else DTYPE_BF16,
+                                          _ptr(out), _ptr(ws), ws.numel(), _stream(codes)),
+           "fge_grouped_gemm_mxf4_w4")
+    return out
 
 
 def grouped_gemm_w4a8_gather(xq, xs, row_token, offsets, w_dev, s_dev, fmt=W4_SUBNORMAL,

@@ -388,6 +388,46 @@ fge_status fge_grouped_gemm_w4a8(const uint8_t* aq, const float* as, const int32
                         out, out_scales, ws, ws_bytes, stream);
 }
 
+fge_status fge_grouped_gemm_mxf4_w4(const uint8_t* a_codes, const uint8_t* a_scales,
+                                   const int32_t* offsets, int64_t R, const uint8_t* w_dev,
+                                   const float* w_scale_dev, int E, int64_t N, int64_t K,
+                                   fge_w4_format format, fge_dtype out_dtype, void* out,
+                                   void* ws, size_t ws_bytes, fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(a_codes && a_scales && offsets && w_dev && w_scale_dev && out && ws,
+              FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(format == FGE_W4_SUBNORMAL, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(out_dtype == FGE_DTYPE_BF16 || out_dtype == FGE_DTYPE_F32, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(R >= 0 && R < (1LL << 31) && N > 0 && N % 128 == 0 && N < (1LL << 24) && K > 0 &&
+                  K % 128 == 0 && K < (1LL << 24),
+              FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(E >= 1 && E <= kMaxExperts, FGE_ERR_BAD_SHAPE);
+  // the padded-E2M1 TMA wants a 32-byte aligned base (its row stride K/2 is a multiple of 64)
+  FGE_REQUIRE((reinterpret_cast<uintptr_t>(a_codes) & 31u) == 0 && al16(a_scales) &&
+                  al16(w_dev) && al16(w_scale_dev) && al16(out) && al16(ws),
+              FGE_ERR_MISALIGNED);
+  FGE_REQUIRE(ws_bytes >= kWsHeaderBytes, FGE_ERR_WORKSPACE_TOO_SMALL);
+  if (R == 0) return FGE_OK;
+  GroupedGemmArgs a{};
+  a.aq = a_codes;
+  a.a_sf = a_scales;
+  a.offsets = offsets;
+  a.w = w_dev;
+  a.sw = w_scale_dev;
+  a.E = E;
+  a.N = N;
+  a.K = K;
+  a.R = R;
+  a.bank_format = format;
+  a.epilogue = out_dtype == FGE_DTYPE_F32 ? 0 : 1;
+  a.out = out;
+  a.status = &static_cast<WsHeader*>(ws)->status;
+  fge_status st = FGE_OK;
+  if (launch_grouped_gemm(a, static_cast<cudaStream_t>(stream), &st) != cudaSuccess)
+    return FGE_ERR_CUDA;
+  return st;
+}
+
 fge_status fge_grouped_gemm_w4a8_gather(const uint8_t* xq, const float* xs, int64_t T,
                                         const int32_t* row_token, const int32_t* offsets,
                                         int64_t R, const uint8_t* w_dev,

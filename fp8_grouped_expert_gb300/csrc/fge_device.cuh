@@ -197,6 +197,35 @@ __host__ __device__ constexpr uint32_t make_idesc_e4m3(int m, int n) {
          | (static_cast<uint32_t>(m >> 4) << 24); // M / 16
 }
 
+// Block-scaled MMA, kind::mxf8f6f4 with one power-of-two (UE8M0) scale per 32 K values
+// (scale_vec::1X): D[tmem] (+)= (A * 2^sfa) * (B * 2^sfb)^T.  The scale factors are read from
+// TMEM at sfa / sfb; the instruction descriptor's scale-factor IDs pick the byte of each
+// 32-bit TMEM cell (one byte per K = 32 step).
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t sfa_tmem,
+                                             uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of the block-scaled kind::mxf8f6f4 MMA: A E2M1 (format 5), B e4m3
+// (format 0), both K-major, D f32 (implied), UE8M0 scales (bit 23), M x N, and the byte
+// sf_id of the A and B scale cells (bits 29-30 and 4-5).
+__host__ __device__ constexpr uint32_t make_idesc_mxf4_e4m3(int m, int n, uint32_t sf_id) {
+  return (sf_id << 4)                             // B scale-factor byte
+         | (5u << 7) | (0u << 10)                 // A E2M1, B e4m3
+         | (0u << 15) | (0u << 16)                // A, B K-major
+         | (static_cast<uint32_t>(n >> 3) << 17)  // N / 8
+         | (1u << 23)                             // scale type UE8M0
+         | (static_cast<uint32_t>(m >> 4) << 24)  // M / 16
+         | (sf_id << 29);                         // A scale-factor byte
+}
+
 // Shared-memory matrix descriptor for a K-major operand in the 128-byte swizzle layout:
 // rows of 128 bytes, 8-row atoms of 1024 bytes stacked at a 1024-byte stride.  The start
 // address advances by 32 bytes per K=32 step inside the atom.
@@ -238,6 +267,18 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Registers into TMEM: lane i of the warp writes 4 consecutive 32-bit columns of TMEM lane
+// (its quarter's first lane + i) at taddr.
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t v0, uint32_t v1,
+                                                  uint32_t v2, uint32_t v3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(v0), "r"(v1), "r"(v2), "r"(v3)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------------------

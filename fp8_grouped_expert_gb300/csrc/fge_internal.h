@@ -75,7 +75,8 @@ struct FusedCombine {
 };
 
 struct GroupedGemmArgs {
-  const uint8_t* aq;        // [R, K] e4m3 codes
+  const uint8_t* aq;        // [R, K] e4m3 codes (MXFP4: [R, K/2] packed E2M1 codes)
+  const uint8_t* a_sf;      // MXFP4 activations: [R, K/32] UE8M0 block scales, else null
   const float* as;          // [R, K/128] (group mode)
   const float* sa_tensor;   // device scalar (per-tensor mode)
   const float* sa_rows;     // [R] per-row activation scales (per-tensor mode), or null

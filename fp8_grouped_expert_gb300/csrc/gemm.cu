@@ -23,6 +23,8 @@ namespace fge {
 
 enum { kBfmtInt4Lut = 0, kBfmtInt4Sub = 1, kBfmtE4m3 = 2 };
 enum { kEpiF32 = 0, kEpiBf16 = 1, kEpiSwiglu = 2 };
+// activation (A) operand: e4m3 codes, or MXFP4 (E2M1 codes, one UE8M0 scale per 32 values)
+enum { kAfmtE4m3 = 0, kAfmtMxf4 = 1 };
 // control warps (warpgroup 1); epilogue warps 8..15 keep their lane quarters
 constexpr int kProducerWarp = 6, kMmaWarp = 7;
 
@@ -41,28 +43,41 @@ struct GemmParams {
   int dense_rows;          // offsets == nullptr: one expert owning rows [0, dense_rows)
   int swap_m;              // BN = 16 (decode sizes): tokens in the B tile; out is [swap_m, out_ld]
   int out_ld;
+  const uint8_t* sf_a;     // MXFP4 activations: [R, K/32] UE8M0 block scales
   const FusedCombine* comb; // bf16 group-mode store: the combine folded into the epilogue
                            // (device memory; null: plain store)
 };
 
 constexpr int align16(int x) { return (x + 15) / 16 * 16; }
 
-template <int BN, int BFMT, int EPI>
+template <int BN, int BFMT, int EPI, int AFMT = kAfmtE4m3>
 struct Cfg {
   static constexpr bool kInt4 = BFMT != kBfmtE4m3;
+  // MXFP4 activations: the TMA expands the packed E2M1 rows into the 16-byte-padded layout
+  // the MMA reads (16 values in the low 8 bytes of every 16), so an A stage is the same
+  // 128 rows x 128 bytes as for e4m3; the block scales go to TMEM beside the accumulators
+  static constexpr bool kMxA = AFMT == kAfmtMxf4;
   static constexpr bool kGroupScale = kInt4;  // int4 path: per-group; e4m3 path: per-tensor
   static constexpr int kABytes = 128 * 128;
   static constexpr int kBLoadBytes = kInt4 ? BN * 64 : BN * 128;
   static constexpr int kBUBytes = BN * 128;
   static constexpr int kNU = kInt4 ? 2 : 0;
   static constexpr int kStageBytes = kABytes + kBLoadBytes;
+  // bytes the TMA reports per stage: the padded E2M1 copy writes only the 8 data bytes of
+  // every 16-byte chunk, half of the A tile's footprint
+  static constexpr int kStageTx = (AFMT == 1 ? kABytes / 2 : kABytes) + kBLoadBytes;
   static constexpr int kPipeBytes = 192 * 1024;
   static constexpr int kNS = (kPipeBytes - kNU * kBUBytes) / kStageBytes;
   // one warpgroup per 128 columns; the 16-column decode tile still needs all 128 lanes
   static constexpr int kEpiWarps = BN >= 128 ? BN / 32 : 4;
   static constexpr int kEpiThreads = kEpiWarps * 32;
   static constexpr int kThreads = 256 + kEpiThreads;
-  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kTmemCols = kMxA ? 512 : 2 * BN;
+  // MXFP4: TMEM columns of the activation scale ring (4 per unpack slot: lane l of every
+  // lane quarter, column j, byte b = the scale of tile row l + 32 j, K step b) and of the
+  // weight-side scales (all 2^0)
+  static constexpr int kSfaCol = 2 * BN;
+  static constexpr int kSfbCol = 2 * BN + 4 * kNU;
   // group mode: each epilogue warpgroup owns 128 columns ("half") of every TMEM buffer with
   // its own full/empty barriers, so the halves pipeline independently of each other
   static constexpr int kHalves = 1;  // one hand-off per buffer: N = BN per MMA instruction
@@ -213,12 +228,12 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <int BN, int BFMT, int EPI>
-__global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
+template <int BN, int BFMT, int EPI, int AFMT = kAfmtE4m3>
+__global__ void __launch_bounds__(Cfg<BN, BFMT, EPI, AFMT>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
-  using C = Cfg<BN, BFMT, EPI>;
+  using C = Cfg<BN, BFMT, EPI, AFMT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -308,8 +323,31 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
       const int tid = threadIdx.x;  // 0..127
       uint32_t it = 0;
       bool ok = true;
+      // MXFP4: this warp's TMEM lane quarter; the weight-side scales are all 2^0 (code 127)
+      const uint32_t quarter = static_cast<uint32_t>(warp * 32) << 16;
+      if constexpr (C::kMxA) {
+        tmem_st_32x32b_x4(tmem_base + quarter + C::kSfbCol, 0x7F7F7F7Fu, 0x7F7F7F7Fu,
+                          0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        tmem_wait_st();
+      }
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        TileInfo ti{};
+        if constexpr (C::kMxA) ti = decode_tile(t, nt_count, BN, s_off, s_mtp, E);
         for (int g = 0; g < G; ++g, ++it) {
+          // MXFP4: the four K-step scales of tile rows lane + 32 j of this group, one 32-bit
+          // word per row (rows past the tile read as 2^0; their results are never stored)
+          uint32_t sfw[4] = {0u, 0u, 0u, 0u};
+          if constexpr (C::kMxA) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int rr = lane + 32 * j;
+              sfw[j] = rr < ti.rows
+                           ? __ldg(reinterpret_cast<const uint32_t*>(
+                                       p.sf_a + static_cast<size_t>(ti.row0 + rr) * (p.K / 32)) +
+                                   g)
+                           : 0x7F7F7F7Fu;
+            }
+          }
           const uint32_t s = it % C::kNS, u = it % C::kNU;
           if (!mbar_wait(bar_full + 8 * s, (it / C::kNS) & 1, s_abort, p.status) ||
               !mbar_wait(bar_uempty + 8 * u, ((it / C::kNU) & 1) ^ 1, s_abort, p.status)) {
@@ -341,6 +379,14 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
               }
               *reinterpret_cast<uint4*>(dst + (i0 + i) * 2048) = make_uint4(a.x, a.y, b.x, b.y);
             }
+          }
+          if constexpr (C::kMxA) {
+            // the group's activation scales into this slot's TMEM columns (every lane
+            // quarter holds the same copy), complete before the MMA is told
+            tmem_st_32x32b_x4(tmem_base + quarter + C::kSfaCol + u * 4, sfw[0], sfw[1], sfw[2],
+                              sfw[3]);
+            tmem_wait_st();
+            tc_fence_before();
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -394,7 +440,7 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
                 }
               }
               if (ok) {
-                mbar_arrive_expect_tx(bar_full + 8 * s, C::kStageBytes);
+                mbar_arrive_expect_tx(bar_full + 8 * s, C::kStageTx);
                 if (!gather)
                   tma_load_2d(smem_u32(smem + C::kOffA + s * C::kABytes), &tmA, bar_full + 8 * s,
                               g * 128, ti.row0);
@@ -475,10 +521,21 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
               constexpr int kHalfN = BN / C::kHalves;
               const uint32_t d_tmem = tmem_base + a * BN + h * kHalfN;
               const uint32_t b_half = b_base + h * kHalfN * 128;
+              if constexpr (C::kMxA) {
+                const uint32_t sfa = tmem_base + C::kSfaCol + u * 4;
+                const uint32_t sfb = tmem_base + C::kSfbCol;
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f8f6f4(d_tmem, make_sdesc_sw128(a_base + kk * 32),
-                           make_sdesc_sw128(b_half + kk * 32), idesc_half, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_mxf8f6f4(d_tmem, make_sdesc_sw128(a_base + kk * 32),
+                               make_sdesc_sw128(b_half + kk * 32),
+                               make_idesc_mxf4_e4m3(128, kHalfN, static_cast<uint32_t>(kk)), sfa,
+                               sfb, kk > 0 ? 1u : 0u);
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_f8f6f4(d_tmem, make_sdesc_sw128(a_base + kk * 32),
+                             make_sdesc_sw128(b_half + kk * 32), idesc_half, kk > 0 ? 1u : 0u);
+              }
               mma_commit(bar_tfull + 8 * slot);
             }
             if (!ok) break;
@@ -535,12 +592,13 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
         // gather mode: the scales of routed row r are those of its source row row_token[r]
         const int src_row = p.row_token ? __ldg(p.row_token + (valid ? row : ti.row0))
                                         : (valid ? row : 0);
-        const float* as_row = p.as + static_cast<size_t>(src_row) * G;
+        // MXFP4: the activation scales are applied inside the MMA; here 1
+        const float* as_row = C::kMxA ? nullptr : p.as + static_cast<size_t>(src_row) * G;
         // the first two scales of a tile were requested at the start of the previous tile
-        float sa0 = pf_ok ? pf0 : (valid ? __ldg(as_row) : 0.0f);
-        float sa1 = pf_ok ? pf1 : ((valid && G > 1) ? __ldg(as_row + 1) : 0.0f);
+        float sa0 = C::kMxA ? 1.0f : (pf_ok ? pf0 : (valid ? __ldg(as_row) : 0.0f));
+        float sa1 = C::kMxA ? 1.0f : (pf_ok ? pf1 : ((valid && G > 1) ? __ldg(as_row + 1) : 0.0f));
         pf_ok = false;
-        if (t + static_cast<int>(gridDim.x) < total_tiles) {
+        if (!C::kMxA && t + static_cast<int>(gridDim.x) < total_tiles) {
           const TileInfo tn = decode_tile(t + gridDim.x, nt_count, BN, s_off, s_mtp, E);
           const bool vn = r_in < tn.rows;
           const int rn = p.row_token ? __ldg(p.row_token + (vn ? tn.row0 + r_in : tn.row0))
@@ -552,7 +610,7 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI>::kThreads, 1)
         for (int g = 0; g < G; ++g) {
           const uint32_t a = ait & 1;
           const uint32_t w = ait % C::kNSW;
-          const float sa2 = (valid && g + 2 < G) ? __ldg(as_row + g + 2) : 0.0f;
+          const float sa2 = C::kMxA ? 1.0f : ((valid && g + 2 < G) ? __ldg(as_row + g + 2) : 0.0f);
           if (!mbar_wait(bar_swfull + 8 * w, (ait / C::kNSW) & 1, s_abort, p.status) ||
               !mbar_wait(bar_tfull + 8 * (a * C::kHalves + half_slot), (ait >> 1) & 1, s_abort,
                          p.status)) {
@@ -877,6 +935,22 @@ static bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64
   return r == CUDA_SUCCESS;
 }
 
+// MXFP4 activations [rows, K] as packed E2M1 (K/2 bytes a row): boxes of 128 values x 128
+// rows, each 16 values landing in the low 8 bytes of a 16-byte smem chunk (the padded layout
+// kind::mxf8f6f4 reads), 128-byte swizzle.  Needs a 32-byte aligned base and K % 128 == 0.
+static bool make_map_e2m1_padded(CUtensorMap* m, const void* base, uint64_t k, uint64_t rows) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {k, rows};
+  cuuint64_t strides[1] = {k / 2};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Output map of the staged SwiGLU store: [rows, inner] bytes, boxes of 64 bytes x 32 rows
 // (one warp's rows) with the 64-byte swizzle.
 static bool make_map_u8_swz64(CUtensorMap* m, void* base, uint64_t inner, uint64_t rows) {
@@ -907,10 +981,10 @@ static bool make_map_bf16_out(CUtensorMap* m, void* base, uint64_t n, uint64_t r
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, int BFMT, int EPI>
+template <int BN, int BFMT, int EPI, int AFMT = kAfmtE4m3>
 static cudaError_t run(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st) {
-  using C = Cfg<BN, BFMT, EPI>;
-  auto kern = grouped_gemm_kernel<BN, BFMT, EPI>;
+  using C = Cfg<BN, BFMT, EPI, AFMT>;
+  auto kern = grouped_gemm_kernel<BN, BFMT, EPI, AFMT>;
   int dev = 0;
   cudaError_t ce = cudaGetDevice(&dev);
   if (ce != cudaSuccess) return ce;
@@ -926,8 +1000,9 @@ static cudaError_t run(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st)
   }
   CUtensorMap tmA, tmB;
   // gather mode: A is the token-ordered [rows_a, K] tensor read one row per box (4 per copy)
-  const bool okA = a.row_token ? make_map_u8(&tmA, a.aq, a.K, a.rows_a, 128, 1, true)
-                               : make_map_u8(&tmA, a.aq, a.K, a.R, 128, 128, true);
+  const bool okA = C::kMxA      ? make_map_e2m1_padded(&tmA, a.aq, a.K, a.R)
+                   : a.row_token ? make_map_u8(&tmA, a.aq, a.K, a.rows_a, 128, 1, true)
+                                 : make_map_u8(&tmA, a.aq, a.K, a.R, 128, 128, true);
   if (!okA) {
     *st = FGE_ERR_CUDA;
     return cudaSuccess;
@@ -943,6 +1018,7 @@ static cudaError_t run(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st)
   }
   GemmParams p{};
   p.as = a.as;
+  p.sf_a = a.a_sf;
   p.sw = a.per_tensor ? nullptr : a.sw;
   p.sa_tensor = a.sa_tensor;
   p.sa_rows = a.sa_rows;
@@ -1022,6 +1098,13 @@ static cudaError_t run_swapped(const GroupedGemmArgs& a, cudaStream_t s, fge_sta
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st) {
   const bool bn256 = (a.N % 256) == 0;
+  if (a.a_sf != nullptr) {
+    // MXFP4 activations: 128-column tiles (the scale columns need TMEM beside the two
+    // accumulators), subnormal int4 bank, plain store
+    ledger_note(kLedGroupedGemms);
+    return a.epilogue == 0 ? run<128, kBfmtInt4Sub, kEpiF32, kAfmtMxf4>(a, s, st)
+                           : run<128, kBfmtInt4Sub, kEpiBf16, kAfmtMxf4>(a, s, st);
+  }
   if (a.per_tensor && a.offsets == nullptr && a.row_token == nullptr && a.R <= 16) {
     ledger_note(kLedDenseDecodeTile);
     return a.epilogue == 0 ? run_swapped<kEpiF32>(a, s, st) : run_swapped<kEpiBf16>(a, s, st);

@@ -220,6 +220,29 @@ fge_status fge_grouped_gemm_w4a8(const uint8_t* aq, const float* as, const int32
                                  float* out_scales, void* workspace, size_t workspace_bytes,
                                  fge_stream_t stream);
 
+/* grouped_gemm_mxf4_w4 -- the grouped expert GEMM with MXFP4 activations: E2M1 codes with
+ * one power-of-two (UE8M0) scale per 32 values along K, the format fge_mx_quant_e2m1 writes
+ * ("[RFC] Support FP4 (E2M1) activation dispatch in MegaMoE": E2M1 dispatch halves the
+ * activation bytes; the expert GEMM consumes them in its MX main loop).  For expert e and
+ * rows r in [offsets[e], offsets[e+1]):
+ *   C[r, n] = sum_g sw[e, n, g] * sum_{k in group g} a[r, k] * q[e, n, k],
+ *   a[r, k] = e2m1(code[r, k]) * 2^(scale[r, k/32] - 127)
+ * computed with tcgen05 block-scaled MMAs (kind::mxf8f6f4, scale_vec::1X: the activation
+ * scales are applied inside the tensor core, one per K = 32 step, from TMEM), the int4 bank
+ * dequantized to e4m3 in shared memory and the weight scale promoted per 128-K group in fp32.
+ * a_codes: [R, K/2] packed E2M1 (element 2b in the low nibble of byte b), 32-byte aligned;
+ * a_scales: [R, K/32] UE8M0 codes; offsets, w_dev, w_scale_dev as fge_grouped_gemm_w4a8
+ * (FGE_W4_SUBNORMAL bank only).  out: [R, N] in out_dtype (BF16 or F32; rows past
+ * offsets[E] untouched).  N % 128 == 0, K % 128 == 0.  Workspace: FGE_OP_GROUPED_GEMM.
+ * Errors: FGE_ERR_INVALID_ARG (null pointer, other bank format or dtype), FGE_ERR_BAD_SHAPE,
+ * FGE_ERR_MISALIGNED, FGE_ERR_WORKSPACE_TOO_SMALL; device waits that run out are reported
+ * through fge_read_device_status. */
+fge_status fge_grouped_gemm_mxf4_w4(const uint8_t* a_codes, const uint8_t* a_scales,
+                                   const int32_t* offsets, int64_t R, const uint8_t* w_dev,
+                                   const float* w_scale_dev, int E, int64_t N, int64_t K,
+                                   fge_w4_format format, fge_dtype out_dtype, void* out,
+                                   void* workspace, size_t workspace_bytes, fge_stream_t stream);
+
 /* grouped_gemm_w4a8_gather -- the same GEMM with the permutation folded into the A load: the
  * A rows are gathered from the token-ordered activations by TMA row gathers (4 rows a copy)
  * instead of being read from a permuted copy, so the permute's row copy disappears.
