@@ -44,6 +44,7 @@ KNOWN_GATE_UP_TRAFFIC = {
     ("mid", "43dbc4055150c350:72b05a4e51127510"): 194.80e6,
     ("mid", "c16c58ceab18302e:38ada4bbcaee05c8"): 195.18e6,
     ("large", "c16c58ceab18302e:38ada4bbcaee05c8"): 1622.82e6,
+    ("large", "335b6bc20fa46740:387767b91fdd6f42"): 1625.56e6,
 }
 
 
@@ -364,6 +365,8 @@ def run_gpu(args):
 
     hbm, bf16, peak_kind = _peaks()
     fp8_peak = 2.0 * bf16  # fp8 dense = 2x bf16 dense (nominal ratio 4.5 / 2.25 PFLOP/s)
+    e2m1_gemm = e2m1_gemm_time(fge, torch, inp, x, logits, w_gu, s_gu, flush, dev,
+                               max(3, args.steps), fp8_peak)
     r = inp.T * inp.k
     gu_flops = 2.0 * r * (2 * inp.I) * inp.H
     gu_ms = stages["gate_up_gemm"]
@@ -431,6 +434,7 @@ def run_gpu(args):
                 "copies": "pinned host -> device and back every step, overlapped with the "
                           "neighbouring steps' layers (HostLayerPipeline, two copy streams)"},
         "gpu_launches": launches_per_step * args.steps,
+        "e2m1_gemm": e2m1_gemm,
         "e2m1_activations": {
             "quant_ms": mx_ms,
             "bytes_read": 2 * inp.T * inp.H,
@@ -472,6 +476,56 @@ def mx_quant_time(fge, torch, x, flush, dev, steps):
         times.append((a, b))
     torch.cuda.synchronize()
     return sum(a.elapsed_time(b) for a, b in times[1:]) / steps
+
+
+def e2m1_gemm_time(fge, torch, inp, x, logits, w_gu, s_gu, flush, dev, steps, fp8_peak):
+    """The gate_up GEMM shape of the layer (R = T*k routed rows, N = 2I, K = H, plain bf16
+    store) with MXFP4 activations (fge_grouped_gemm_mxf4_w4: E2M1 codes, a power-of-two scale
+    per 32 values applied in the block-scaled MMA) beside the same GEMM with e4m3 G128
+    activations (fge_grouped_gemm_w4a8), each through its C-ABI call, L2 flushed before each
+    call.  The routed activations are prepared outside the timing."""
+    stream = torch.cuda.current_stream(dev)
+    ids, _ = fge.moe_topk_gate(logits, inp.k)
+    xq, xs = fge.fp8_quant_act(x, "g128")
+    p = fge.moe_permute(ids, inp.E, xq, xs)
+    codes_t, scales_t = fge.mx_quant_e2m1(x)
+    rt = p["row_token"].long()
+    codes = codes_t.index_select(0, rt).contiguous()
+    scales = scales_t.index_select(0, rt).contiguous()
+    r = inp.T * inp.k
+    n = 2 * inp.I
+    ws = fge.new_workspace(fge.workspace_bytes(fge.OP_GROUPED_GEMM), dev)
+    y = torch.empty((r, n), dtype=torch.bfloat16, device=dev)
+    calls = {
+        "e4m3_g128": lambda: fge.grouped_gemm_w4a8(p["aq"], p["as_"], p["offsets"], w_gu, s_gu,
+                                                   out_dtype=torch.bfloat16, workspace=ws,
+                                                   out=y),
+        "mxfp4": lambda: fge.grouped_gemm_mxf4_w4(codes, scales, p["offsets"], w_gu, s_gu,
+                                                  out_dtype=torch.bfloat16, workspace=ws, out=y),
+    }
+    res = {}
+    flops = 2.0 * r * n * inp.H
+    for name, fn in calls.items():
+        fn()
+        torch.cuda.synchronize()
+        times = []
+        for i in range(steps):
+            flush.fill_(9)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            times.append((a, b))
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in times) / steps
+        res[name] = {"ms": ms, "tflops": flops / (ms / 1e3) / 1e12,
+                     "frac_of_fp8_peak": flops / (ms / 1e3) / 1e12 / fp8_peak}
+    if fge.read_device_status(ws) != 0:
+        raise RuntimeError("device status %d in the E2M1 GEMM timing" % fge.read_device_status(ws))
+    res["activation_bytes"] = {"e4m3_g128": r * inp.H + r * (inp.H // 128) * 4,
+                               "mxfp4": r * inp.H // 2 + r * (inp.H // 32)}
+    res["shape"] = {"R": r, "N": n, "K": inp.H, "E": inp.E}
+    return res
 
 
 def stage_times(fge, torch, inp, x, logits, w_gu, s_gu, w_dn, s_dn, fmt, flush, dev, steps):
