@@ -378,10 +378,20 @@ def run_gpu(args):
 
     # the HBM-bound stages of this layer against the measured copy bandwidth
     sb = stage_bytes(inp)
-    memory_kernels = {name: {"ms": stages[name], "bytes": nbytes,
+    wb = stage_write_bytes(inp)
+    write_gbs = write_ceiling_gbs(torch, dev)
+    memory_kernels = {name: {"ms": stages[name], "bytes": nbytes, "bytes_written": wb[name],
                              "hbm_gbs": nbytes / (stages[name] / 1e3) / 1e9,
-                             "hbm_frac": nbytes / (stages[name] / 1e3) / 1e9 / hbm}
+                             "hbm_frac": nbytes / (stages[name] / 1e3) / 1e9 / hbm,
+                             "floor_ms": memory_floor_ms(nbytes, wb[name], hbm, write_gbs),
+                             "frac_of_floor": memory_floor_ms(nbytes, wb[name], hbm, write_gbs)
+                                              / stages[name]}
                       for name, nbytes in sb.items()}
+    memory_kernels["ceilings"] = {
+        "copy_gbs": hbm, "write_gbs": write_gbs,
+        "what": "hbm_frac: bytes / time against the measured copy bandwidth; frac_of_floor: "
+                "max(bytes / copy bandwidth, bytes written / plain-write bandwidth) / time, "
+                "the plain-write bandwidth measured here by a 1 GiB memset"}
 
     # every other workload, each on its own line of the object (rank 0 only)
     configs = None
@@ -589,6 +599,47 @@ def stage_bytes(inp):
         # expert outputs (bf16) read once with their gates and row map; bf16 out
         "combine": r * h * 2 + r * 8 + t * h * 2,
     }
+
+
+def stage_write_bytes(inp):
+    """The written part of stage_bytes: HBM writes are slower than reads on this part (a
+    plain write stream, cudaMemset, reaches well under the copy bandwidth), so a stage that
+    mostly writes has a lower ceiling than the copy figure suggests."""
+    t, h, e, k = inp.T, inp.H, inp.E, inp.k
+    r = t * k
+    g = h // 128
+    return {
+        "topk_gate": r * 8,
+        "quant_g128": t * h + t * g * 4,
+        "permute": r * h + r * g * 4 + 2 * r * 4,
+        "permute_quant": r * h + r * g * 4 + 2 * r * 4,
+        "combine": t * h * 2,
+    }
+
+
+def memory_floor_ms(total_bytes, written_bytes, copy_gbs, write_gbs):
+    """Shortest time the bytes allow: the copy bandwidth bounds all traffic, the plain-write
+    bandwidth bounds the writes."""
+    return max(total_bytes / copy_gbs, written_bytes / write_gbs) / 1e6
+
+
+def write_ceiling_gbs(torch, dev, nbytes=1 << 30, reps=5):
+    """Plain write bandwidth: a memset of a buffer far larger than L2, median of reps."""
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    buf.zero_()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        buf.zero_()
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    ms = sorted(a.elapsed_time(b) for a, b in ts)[reps // 2]
+    del buf
+    return nbytes / (ms / 1e3) / 1e9
 
 
 def layer_work(inp, counts):

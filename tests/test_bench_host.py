@@ -94,3 +94,20 @@ def test_cpu_info_reports_the_core_count():
     import os
     info = bench.cpu_info()
     assert info["nproc"] == os.cpu_count() and info["machine"]
+
+
+def test_stage_write_bytes_within_totals():
+    inp = _Inp(16384, 4096, 128, 1536, 8)
+    tot, wr = bench.stage_bytes(inp), bench.stage_write_bytes(inp)
+    assert set(tot) == set(wr)
+    for name in tot:
+        assert 0 < wr[name] < tot[name], name
+    # the permuted copies write k rows per token read
+    assert wr["permute_quant"] > 4 * (tot["permute_quant"] - wr["permute_quant"])
+
+
+def test_memory_floor_takes_the_slower_bound():
+    # 1 GB read + 1 GB written: copy-bound at 2 GB / 6000 GB/s
+    assert bench.memory_floor_ms(2e9, 1e9, 6000.0, 4000.0) == 2e9 / 6000.0 / 1e6
+    # 0.2 GB read + 1.8 GB written: write-bound at 1.8 GB / 4000 GB/s
+    assert bench.memory_floor_ms(2e9, 1.8e9, 6000.0, 4000.0) == 1.8e9 / 4000.0 / 1e6
