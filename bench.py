@@ -730,7 +730,7 @@ def dense_sweep(fge, torch, dev, flush, reps, fp8_peak, hbm):
     res = {}
     for m in (16, 256, 2048, 8192):
         x = torch.randn((m, k), generator=gen, device=dev).to(torch.bfloat16)
-        ws = fge.new_workspace(fge.workspace_bytes(fge.OP_LINEAR_W8A8, m, k), dev)
+        ws = fge.new_workspace(fge.workspace_bytes(fge.OP_LINEAR_W8A8, m, k, n), dev)
         y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
         ms = timed_calls(torch, lambda: fge.linear_w8a8(x, wq, sw, workspace=ws, out=y), flush,
                          torch.cuda.current_stream(dev), 3, reps)

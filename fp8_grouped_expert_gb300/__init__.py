@@ -434,7 +434,7 @@ def linear_w8a8(x, wq, w_scale, workspace=None, out=None):
     m, k = x.shape
     n = wq.shape[0]
     ws = workspace if workspace is not None else new_workspace(
-        workspace_bytes(OP_LINEAR_W8A8, m, k), x.device)
+        workspace_bytes(OP_LINEAR_W8A8, m, k, n), x.device)
     y = out if out is not None else torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
     _check(lib().fge_linear_w8a8(_ptr(x), m, k, _ptr(wq), _ptr(w_scale), n, _ptr(y), _ptr(ws),
                                  ws.numel(), _stream(x)), "fge_linear_w8a8")
@@ -688,7 +688,9 @@ class StackedPrefill:
             self.layers.append(d)
         dev = self.dev
         kv = n_kv_heads * 128
-        self.ws_lin = new_workspace(workspace_bytes(OP_LINEAR_W8A8, T, H), dev)
+        # one workspace for the four projections, sized for the largest K-split scratch
+        self.ws_lin = new_workspace(max(workspace_bytes(OP_LINEAR_W8A8, T, kin, n) for kin, n in
+                                        ((H, n_heads * 128), (H, kv), (n_heads * 128, H))), dev)
         self.ws_moe = new_workspace(workspace_bytes(OP_MOE_LAYER, T, H, I, E, k), dev)
         self.xn = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         self.q = torch.empty((T, n_heads * 128), dtype=torch.bfloat16, device=dev)

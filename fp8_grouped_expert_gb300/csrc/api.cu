@@ -187,7 +187,12 @@ size_t fge_workspace_bytes(fge_op op, int64_t a, int64_t b, int64_t c, int E, in
     case FGE_OP_QUANT_PER_TENSOR: return kWsHeaderBytes;
     case FGE_OP_PERMUTE: return kWsHeaderBytes + permute_scratch_bytes(a, E);
     case FGE_OP_GROUPED_GEMM: return kWsHeaderBytes;
-    case FGE_OP_LINEAR_W8A8: return kWsHeaderBytes + align_up(static_cast<size_t>(a * b), 256);
+    case FGE_OP_LINEAR_W8A8: {
+      // with N (c > 0): also the scratch of a K split at small M
+      size_t counters = 0;
+      const size_t split = c > 0 ? dense_split_bytes(a, c, dense_ksplit(a, c, b), &counters) : 0;
+      return kWsHeaderBytes + align_up(static_cast<size_t>(a * b), 256) + split;
+    }
     case FGE_OP_MOE_LAYER: return carve_layer(nullptr, a, b, c, E, k).bytes;
     case FGE_OP_LINEAR_W8A8_ROWS:
       return kWsHeaderBytes + align_up(static_cast<size_t>(a * b), 256) +
@@ -486,6 +491,40 @@ fge_status fge_gemm_w8a8(const uint8_t* aq, const float* sa, int64_t M, int64_t 
                         out_dtype == FGE_DTYPE_F32 ? 0 : 1, y, nullptr, ws, ws_bytes, stream);
 }
 
+// The per-tensor W8A8 GEMM of the dense projection, optionally with K split over ks CTAs
+// per output tile (partials and zeroed counters in the caller's scratch).
+static fge_status dense_gemm(const uint8_t* xq, int64_t M, const uint8_t* wq,
+                             const float* w_scale, int64_t N, int64_t K, const float* sa,
+                             void* y, void* ws, size_t ws_bytes, fge_stream_t stream, int ks,
+                             float* partials, int32_t* counters) {
+  FGE_REQUIRE(M >= 0 && M < (1LL << 31) && N > 0 && N % 128 == 0 && N < (1LL << 24) && K > 0 &&
+                  K % 128 == 0 && K < (1LL << 24),
+              FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(al16(xq) && al16(wq) && al16(y) && al16(ws), FGE_ERR_MISALIGNED);
+  FGE_REQUIRE(ws_bytes >= kWsHeaderBytes, FGE_ERR_WORKSPACE_TOO_SMALL);
+  if (M == 0) return FGE_OK;
+  GroupedGemmArgs a{};
+  a.aq = xq;
+  a.sa_tensor = sa;
+  a.w = wq;
+  a.sw = w_scale;
+  a.E = 1;
+  a.N = N;
+  a.K = K;
+  a.R = M;
+  a.per_tensor = 1;
+  a.epilogue = 1;
+  a.out = y;
+  a.status = &static_cast<WsHeader*>(ws)->status;
+  a.ksplit = ks;
+  a.partials = partials;
+  a.split_count = counters;
+  fge_status st = FGE_OK;
+  if (launch_grouped_gemm(a, static_cast<cudaStream_t>(stream), &st) != cudaSuccess)
+    return FGE_ERR_CUDA;
+  return st;
+}
+
 fge_status fge_linear_w8a8(const void* x, int64_t M, int64_t K, const uint8_t* wq,
                            const float* w_scale, int64_t N, void* y, void* ws, size_t ws_bytes,
                            fge_stream_t stream) {
@@ -497,11 +536,25 @@ fge_status fge_linear_w8a8(const void* x, int64_t M, int64_t K, const uint8_t* w
               FGE_ERR_WORKSPACE_TOO_SMALL);
   NvtxRange range("fge.linear_w8a8");
   WsHeader* hdr = static_cast<WsHeader*>(ws);
-  uint8_t* xq = static_cast<uint8_t*>(ws) + kWsHeaderBytes;
+  // layout: header | K-split counters | xq | K-split partials; the split (small M: several
+  // CTAs per output tile) is used when the workspace was sized with N
+  int ks = dense_ksplit(M, N, K);
+  size_t counter_bytes = 0;
+  size_t split_bytes = dense_split_bytes(M, N, ks, &counter_bytes);
+  const size_t xq_bytes = align_up(static_cast<size_t>(M * K), 256);
+  if (ws_bytes < kWsHeaderBytes + xq_bytes + split_bytes) {
+    ks = 1;
+    counter_bytes = split_bytes = 0;
+  }
+  uint8_t* base = static_cast<uint8_t*>(ws) + kWsHeaderBytes;
+  int32_t* counters = reinterpret_cast<int32_t*>(base);
+  uint8_t* xq = base + counter_bytes;
+  float* partials = reinterpret_cast<float*>(xq + xq_bytes);
   FGE_CHECK(from_cuda(launch_quant_per_tensor(static_cast<const uint16_t*>(x), M, K, xq,
-                                              &hdr->scale, hdr, stream)));
-  return grouped_common(xq, nullptr, nullptr, M, wq, w_scale, 1, N, K, 0, 1, &hdr->scale, 1, y,
-                        nullptr, ws, ws_bytes, stream);
+                                              &hdr->scale, hdr, stream, counters,
+                                              static_cast<int>(counter_bytes / 4))));
+  return dense_gemm(xq, M, wq, w_scale, N, K, &hdr->scale, y, ws, ws_bytes, stream, ks,
+                    partials, counters);
 }
 
 fge_status fge_gemm_w8a8_rows(const uint8_t* aq, const float* sa, int64_t M, int64_t K,

@@ -38,8 +38,11 @@ cudaError_t launch_quant_rows(const uint16_t* x, int64_t M, int64_t K, uint8_t* 
                               int32_t* status, cudaStream_t s);
 cudaError_t launch_mx_quant_e2m1(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq,
                                  uint8_t* xs, cudaStream_t s);
+// zero / n_zero: words the call also sets to 0 before it returns (the K-split counters of
+// the GEMM that follows), or null / 0.
 cudaError_t launch_quant_per_tensor(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq,
-                                    float* xs, WsHeader* hdr, cudaStream_t s);
+                                    float* xs, WsHeader* hdr, cudaStream_t s,
+                                    int32_t* zero = nullptr, int n_zero = 0);
 cudaError_t launch_topk_gate(const float* logits, int64_t T, int E, int k, int32_t* ids,
                              float* gates, cudaStream_t s);
 size_t permute_scratch_bytes(int64_t T, int E);
@@ -96,7 +99,19 @@ struct GroupedGemmArgs {
   int32_t* status;
   const FusedCombine* comb;  // down GEMM, bf16 store: the combine folded in (device memory,
                             // written by launch_combine_setup), or null
+  // per-tensor (one-group) mode: K split over ksplit CTAs per output tile (0 or 1: none);
+  // partials [tiles, ksplit, 128, BN] fp32 and split_count [tiles, epilogue warps] int32,
+  // zero before the launch (the kernel leaves it zero again)
+  int ksplit;
+  float* partials;
+  int32_t* split_count;
 };
+// K split of a per-tensor (one-group) W8A8 GEMM with M activation rows, N outputs and K
+// inputs: how many CTAs share each output tile (1: no split), chosen to fill the SMs, and
+// the scratch it needs (partials and counters, bytes).
+int dense_ksplit(int64_t M, int64_t N, int64_t K);
+// Scratch of a K split: the counters (*counter_bytes, first) then the partials.
+size_t dense_split_bytes(int64_t M, int64_t N, int ksplit, size_t* counter_bytes);
 // Zeroes the arrival counters (n of them) and writes c to dst (device memory) for the down
 // GEMM's folded combine; one launch, stream-ordered.
 cudaError_t launch_combine_setup(const FusedCombine& c, int64_t n, FusedCombine* dst,

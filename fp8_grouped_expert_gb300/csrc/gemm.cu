@@ -48,6 +48,13 @@ struct GemmParams {
                            // (device memory; null: plain store)
 };
 
+// K split of the one-group (per-tensor) GEMM, a kernel argument of its own.
+struct SplitArgs {
+  float* partials;         // [tiles, ksplit, 128, BN] fp32 partials
+  int32_t* split_count;    // [tiles, epilogue warps] arrival counters (start at 0)
+  int ksplit;              // CTAs per tile, each a contiguous range of K groups (1: none)
+};
+
 constexpr int align16(int x) { return (x + 15) / 16 * 16; }
 
 template <int BN, int BFMT, int EPI, int AFMT = kAfmtE4m3>
@@ -220,6 +227,21 @@ __device__ __forceinline__ TileInfo decode_tile(int t, int nt_count, int bn, con
   return ti;
 }
 
+// K split over ks CTAs: after this warp has written its partial rows, publishes them and
+// counts its arrival for (tile, epilogue warp).  True in every lane of the ks-th warp to
+// arrive, for which every split's partials are then visible; the counter wraps back to 0.
+__device__ __forceinline__ bool split_arrive_last(int32_t* count, int ks, int lane) {
+  __threadfence();
+  __syncwarp();
+  unsigned last = 0;
+  if (lane == 0)
+    last = atomicInc(reinterpret_cast<unsigned*>(count), static_cast<unsigned>(ks - 1)) ==
+           static_cast<unsigned>(ks - 1);
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (last) __threadfence();
+  return last != 0u;
+}
+
 // Wait that ignores the abort flag (used to drain copies/MMAs already in flight).
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
@@ -232,7 +254,8 @@ template <int BN, int BFMT, int EPI, int AFMT = kAfmtE4m3>
 __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI, AFMT>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tmY, const GemmParams p,
+                        const SplitArgs sk) {
   using C = Cfg<BN, BFMT, EPI, AFMT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -314,7 +337,11 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI, AFMT>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
   const int nt_count = p.N / BN;
-  const int total_tiles = s_mtp[E] * nt_count;
+  const int base_tiles = s_mtp[E] * nt_count;
+  // one-group mode may split K over ks CTAs per tile, each taking a contiguous range of K
+  // groups; the last of them to finish adds the fp32 partials in split order
+  const int ks = C::kGroupScale ? 1 : sk.ksplit;
+  const int total_tiles = base_tiles * ks;
 
   if (warp < 4) {
     // ------------------------------------------------------------------ unpack (WG0)
@@ -414,13 +441,17 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI, AFMT>::kThreads, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile(t, nt_count, BN, s_off, s_mtp, E);
+        const int tsplit = C::kGroupScale ? 0 : t / base_tiles;
+        const TileInfo ti = decode_tile(C::kGroupScale ? t : t - tsplit * base_tiles, nt_count,
+                                        BN, s_off, s_mtp, E);
+        const int g0 = C::kGroupScale ? 0 : tsplit * G / ks;
+        const int g1 = C::kGroupScale ? G : (tsplit + 1) * G / ks;
         if (gather) {
           for (int i = lane; i < 128; i += 32)
             s_rt[i] = __ldg(p.row_token + ti.row0 + (i < ti.rows ? i : ti.rows - 1));
           __syncwarp();
         }
-        for (int g = 0; g < G; ++g, ++it) {
+        for (int g = g0; g < g1; ++g, ++it) {
           const uint32_t s = it % C::kNS;
           if (lane == 0) {
             if (!mbar_wait(bar_empty + 8 * s, ((it / C::kNS) & 1) ^ 1, s_abort, p.status)) {
@@ -485,11 +516,14 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI, AFMT>::kThreads, 1)
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
         uint32_t a = ait & 1;
+        const int tsplit = C::kGroupScale ? 0 : t / base_tiles;
+        const int g0 = C::kGroupScale ? 0 : tsplit * G / ks;
+        const int g1 = C::kGroupScale ? G : (tsplit + 1) * G / ks;
         if constexpr (!C::kGroupScale) {
           if (!mbar_wait(bar_tempty + 8 * a, ((ait >> 1) & 1) ^ 1, s_abort, p.status)) break;
           tc_fence_after();
         }
-        for (int g = 0; g < G; ++g, ++it) {
+        for (int g = g0; g < g1; ++g, ++it) {
           const uint32_t s = it % C::kNS;
           if (!mbar_wait(bar_full + 8 * s, (it / C::kNS) & 1, s_abort, p.status)) {
             ok = false;
@@ -546,7 +580,7 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI, AFMT>::kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_f8f6f4(d_tmem, make_sdesc_sw128(a_base + kk * 32),
-                         make_sdesc_sw128(b_base + kk * 32), idesc, (kk > 0 || g > 0) ? 1u : 0u);
+                         make_sdesc_sw128(b_base + kk * 32), idesc, (kk > 0 || g > g0) ? 1u : 0u);
           }
           mma_commit(bar_empty + 8 * s);
           if constexpr (C::kInt4) mma_commit(bar_uempty + 8 * u);
@@ -581,7 +615,9 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI, AFMT>::kThreads, 1)
     float pf0 = 0.0f, pf1 = 0.0f;  // group mode: next tile's first two activation scales
     bool pf_ok = false;
     for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, tile_parity ^= 1) {
-      const TileInfo ti = decode_tile(t, nt_count, BN, s_off, s_mtp, E);
+      const int split = C::kGroupScale ? 0 : t / base_tiles;
+      const int tix = C::kGroupScale ? t : t - split * base_tiles;  // output tile of this split
+      const TileInfo ti = decode_tile(tix, nt_count, BN, s_off, s_mtp, E);
       const bool valid = r_in < ti.rows;
       const int row = ti.row0 + r_in;
       if constexpr (C::kGroupScale) {
@@ -821,13 +857,46 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI, AFMT>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_tempty + 8 * a);
         ++ait;
-        if (valid) {
+        float acc[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j] = __uint_as_float(v[j]);
+        bool store = valid;
+        if (ks > 1) {
+          // K split: this split's partial row goes out; the last split adds all of them
+          float* part = sk.partials + ((static_cast<size_t>(tix) * ks + split) * 128 + r_in) * 16;
+          if (valid) {
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+              *reinterpret_cast<float4*>(part + j) =
+                  make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+          }
+          store = split_arrive_last(sk.split_count + static_cast<size_t>(tix) * C::kEpiWarps +
+                                        ewarp, ks, lane) &&
+                  valid;
+          if (store) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+            for (int s2 = 0; s2 < ks; ++s2) {
+              const float* q =
+                  sk.partials + ((static_cast<size_t>(tix) * ks + s2) * 128 + r_in) * 16;
+#pragma unroll
+              for (int j = 0; j < 16; j += 4) {
+                const float4 f = __ldcg(reinterpret_cast<const float4*>(q + j));
+                acc[j] += f.x;
+                acc[j + 1] += f.y;
+                acc[j + 2] += f.z;
+                acc[j + 3] += f.w;
+              }
+            }
+          }
+        }
+        if (store) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             if (j < p.swap_m) {
               // per-row activation scales belong to the tokens: one per column here
               const float rs = p.sa_rows ? __ldg(p.sa_rows + j) * tensor_scale : tensor_scale;
-              const float yv = rs * __uint_as_float(v[j]);
+              const float yv = rs * acc[j];
               const size_t o = static_cast<size_t>(j) * p.out_ld + row;
               if constexpr (EPI == kEpiF32)
                 reinterpret_cast<float*>(p.out)[o] = yv;
@@ -857,7 +926,16 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI, AFMT>::kThreads, 1)
           }
           const int col = (c < 4) ? col_a + c * 16 : col_b + (c - 4) * 16;
           const uint32_t* vv = v[c & 1];
-          if (valid) {
+          if (valid && ks > 1) {
+            // K split: this split's raw partial of the row goes out
+            float* part = sk.partials +
+                          ((static_cast<size_t>(tix) * ks + split) * 128 + r_in) * BN + col;
+#pragma unroll
+            for (int i = 0; i < 16; i += 4)
+              *reinterpret_cast<float4*>(part + i) =
+                  make_float4(__uint_as_float(vv[i]), __uint_as_float(vv[i + 1]),
+                              __uint_as_float(vv[i + 2]), __uint_as_float(vv[i + 3]));
+          } else if (valid) {
             if constexpr (EPI == kEpiF32) {
               float* o = reinterpret_cast<float*>(p.out) + static_cast<size_t>(row) * p.N + ti.n0 + col;
 #pragma unroll
@@ -885,6 +963,47 @@ __global__ void __launch_bounds__(Cfg<BN, BFMT, EPI, AFMT>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_tempty + 8 * a);
         ++ait;
+        if (ks > 1 &&
+            split_arrive_last(sk.split_count + static_cast<size_t>(tix) * C::kEpiWarps + ewarp, ks,
+                              lane) &&
+            valid) {
+          // the last split: every split's partial of the row added in split order, scaled
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            const int col = (c < 4) ? col_a + c * 16 : col_b + (c - 4) * 16;
+            float acc[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+            for (int s2 = 0; s2 < ks; ++s2) {
+              const float* q = sk.partials +
+                               ((static_cast<size_t>(tix) * ks + s2) * 128 + r_in) * BN + col;
+#pragma unroll
+              for (int i = 0; i < 16; i += 4) {
+                const float4 f = __ldcg(reinterpret_cast<const float4*>(q + i));
+                acc[i] += f.x;
+                acc[i + 1] += f.y;
+                acc[i + 2] += f.z;
+                acc[i + 3] += f.w;
+              }
+            }
+            if constexpr (EPI == kEpiF32) {
+              float* o = reinterpret_cast<float*>(p.out) + static_cast<size_t>(row) * p.N + ti.n0 + col;
+#pragma unroll
+              for (int i = 0; i < 16; i += 4)
+                *reinterpret_cast<float4*>(o + i) =
+                    make_float4(rs * acc[i], rs * acc[i + 1], rs * acc[i + 2], rs * acc[i + 3]);
+            } else {
+              __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * p.N + ti.n0 + col;
+#pragma unroll
+              for (int i = 0; i < 16; i += 8)
+                *reinterpret_cast<uint4*>(o + i) = make_uint4(
+                    pack_bf16x2(rs * acc[i], rs * acc[i + 1]),
+                    pack_bf16x2(rs * acc[i + 2], rs * acc[i + 3]),
+                    pack_bf16x2(rs * acc[i + 4], rs * acc[i + 5]),
+                    pack_bf16x2(rs * acc[i + 6], rs * acc[i + 7]));
+            }
+          }
+        }
       }
     }
     if constexpr (C::kStageOut) {
@@ -1019,6 +1138,7 @@ static cudaError_t run(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st)
   GemmParams p{};
   p.as = a.as;
   p.sf_a = a.a_sf;
+  const SplitArgs sk{a.partials, a.split_count, std::max(1, a.ksplit)};
   p.sw = a.per_tensor ? nullptr : a.sw;
   p.sa_tensor = a.sa_tensor;
   p.sa_rows = a.sa_rows;
@@ -1034,7 +1154,7 @@ static cudaError_t run(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st)
   p.K = static_cast<int>(a.K);
   p.G = static_cast<int>(a.K / 128);
   p.dense_rows = static_cast<int>(a.R);
-  const long tiles_bound = (a.R / 128 + a.E) * (a.N / BN);
+  const long tiles_bound = (a.R / 128 + a.E) * (a.N / BN) * std::max(1, a.ksplit);
   const int grid = static_cast<int>(std::max<long>(1, std::min<long>(num_sms(), tiles_bound)));
   CUtensorMap tmY = tmA;  // unused unless the store is staged
   bool okY = true;
@@ -1048,7 +1168,7 @@ static cudaError_t run(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st)
     *st = FGE_ERR_CUDA;
     return cudaSuccess;
   }
-  kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(tmA, tmB, tmY, p);
+  kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(tmA, tmB, tmY, p, sk);
   *st = FGE_OK;
   return cudaGetLastError();
 }
@@ -1090,10 +1210,48 @@ static cudaError_t run_swapped(const GroupedGemmArgs& a, cudaStream_t s, fge_sta
   p.dense_rows = static_cast<int>(a.N);
   p.swap_m = static_cast<int>(a.R);
   p.out_ld = static_cast<int>(a.N);
-  const int grid = static_cast<int>(std::max<long>(1, std::min<long>(num_sms(), (a.N + 127) / 128)));
-  kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(tmA, tmB, tmA, p);
+  const SplitArgs sk{a.partials, a.split_count, std::max(1, a.ksplit)};
+  const int grid = static_cast<int>(std::max<long>(
+      1, std::min<long>(num_sms(), (a.N + 127) / 128 * std::max(1, a.ksplit))));
+  kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(tmA, tmB, tmA, p, sk);
   *st = FGE_OK;
   return cudaGetLastError();
+}
+
+// Output tiles of the per-tensor GEMM and their width: the decode tile (M <= 16, 128 weight
+// rows by 16 tokens) or 128-row tiles of BN = 256 (128 when N % 256 != 0) columns.
+static void dense_tiles(int64_t M, int64_t N, int64_t* tiles, int64_t* bn, int64_t* warps) {
+  if (M <= 16) {
+    *tiles = (N + 127) / 128;
+    *bn = 16;
+    *warps = 4;
+  } else {
+    *bn = N % 256 == 0 ? 256 : 128;
+    *tiles = (M + 127) / 128 * (N / *bn);
+    *warps = *bn / 32;
+  }
+}
+
+int dense_ksplit(int64_t M, int64_t N, int64_t K) {
+  // only the decode tile splits: with 128-row tiles the last split's read-back of the others'
+  // 128 x BN partials costs more than the shorter K walk saves (measured)
+  if (M <= 0 || M > 16 || N <= 0 || K < 256) return 1;
+  int64_t tiles, bn, warps;
+  dense_tiles(M, N, &tiles, &bn, &warps);
+  // as many CTAs per tile as fit on the SMs in one wave, each with at least 2 K groups
+  int64_t ks = num_sms() / std::max<int64_t>(tiles, 1);
+  ks = std::min<int64_t>(ks, (K / 128) / 2);
+  ks = std::min<int64_t>(ks, 8);
+  return static_cast<int>(std::max<int64_t>(ks, 1));
+}
+
+size_t dense_split_bytes(int64_t M, int64_t N, int ksplit, size_t* counter_bytes) {
+  *counter_bytes = 0;
+  if (ksplit <= 1) return 0;
+  int64_t tiles, bn, warps;
+  dense_tiles(M, N, &tiles, &bn, &warps);
+  *counter_bytes = align_up(static_cast<size_t>(tiles * warps) * 4, 256);
+  return *counter_bytes + static_cast<size_t>(tiles) * ksplit * 128 * bn * 4;
 }
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st) {

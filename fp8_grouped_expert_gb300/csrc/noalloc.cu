@@ -14,8 +14,8 @@
 namespace fge {
 namespace {
 
-// Scratch: a 256-byte header (status word, amax word, activation scale) followed by the
-// e4m3 copy of the activations.  Every GPU that loads the library holds this array until
+// Scratch: a 256-byte header (status word, amax word, activation scale), the counters of a K
+// split, the e4m3 copy of the activations and the K split's partials.  Every GPU that loads the library holds this array until
 // the process exits.
 constexpr size_t kNoallocScratchBytes = size_t(16) << 20;  // 16 MiB
 constexpr size_t kNoallocMaxActBytes = kNoallocScratchBytes - kWsHeaderBytes;
@@ -72,14 +72,29 @@ fge_status noalloc_run(const void* x, int64_t M, int64_t K, const uint8_t* wq,
   const fge_status st = scratch_for_current_device(&scratch);
   if (st != FGE_OK) return st;
   WsHeader* hdr = static_cast<WsHeader*>(scratch);
-  uint8_t* xq = static_cast<uint8_t*>(scratch) + kWsHeaderBytes;
+  // Layout as fge_linear_w8a8's workspace: header | K-split counters | xq | K-split partials.
+  // The K split is the one fge_linear_w8a8 takes (so the two agree bit for bit) whenever its
+  // scratch fits beside the activations; otherwise the GEMM runs unsplit.
+  int ks = dense_ksplit(M, N, K);
+  size_t counter_bytes = 0;
+  size_t split_bytes = dense_split_bytes(M, N, ks, &counter_bytes);
+  const size_t xq_bytes = align_up(static_cast<size_t>(M * K), 256);
+  if (kWsHeaderBytes + xq_bytes + split_bytes > kNoallocScratchBytes) {
+    ks = 1;
+    counter_bytes = split_bytes = 0;
+  }
+  uint8_t* base = static_cast<uint8_t*>(scratch) + kWsHeaderBytes;
+  int32_t* counters = reinterpret_cast<int32_t*>(base);
+  uint8_t* xq = base + counter_bytes;
+  float* partials = reinterpret_cast<float*>(xq + xq_bytes);
 
-  // The array keeps the previous call's contents: the status word is cleared here and the
-  // amax word by the quantization launcher, before anything reads them.
+  // The array keeps the previous call's contents: the status word is cleared here, the amax
+  // word and the split counters by the quantization launcher, before anything reads them.
   if (cudaMemsetAsync(&hdr->status, 0, sizeof(int32_t), stream) != cudaSuccess)
     return FGE_ERR_CUDA;
   if (launch_quant_per_tensor(static_cast<const uint16_t*>(x), M, K, xq, &hdr->scale, hdr,
-                              stream) != cudaSuccess)
+                              stream, counters, static_cast<int>(counter_bytes / 4)) !=
+      cudaSuccess)
     return FGE_ERR_CUDA;
 
   GroupedGemmArgs a{};
@@ -99,6 +114,9 @@ fge_status noalloc_run(const void* x, int64_t M, int64_t K, const uint8_t* wq,
   a.out = y;
   a.out_scales = nullptr;
   a.status = &hdr->status;
+  a.ksplit = ks;
+  a.partials = partials;
+  a.split_count = counters;
   fge_status gst = FGE_OK;
   if (launch_grouped_gemm(a, stream, &gst) != cudaSuccess) return FGE_ERR_CUDA;
   return gst;

@@ -15,24 +15,47 @@ constexpr int kQuantUnroll = 4;
 
 // Per-tensor pass 1: amax over the tensor, combined across blocks with atomicMax on the
 // float bits (|x| >= 0, so the unsigned order of the bits is the float order).
+// Folds the 8 bf16 values of v into the running amax m and the non-finite detector bad.
+__device__ __forceinline__ void amax_fold8(const uint4& v, float& m, float& bad) {
+  m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
+                     fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)))));
+  m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))),
+                     fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)))));
+  bad = nonfinite_fold(nonfinite_fold(nonfinite_fold(nonfinite_fold(bad, bf16_lo(v.x)),
+                                                     bf16_hi(v.x)),
+                                      bf16_lo(v.y)),
+                       bf16_hi(v.y));
+  bad = nonfinite_fold(nonfinite_fold(nonfinite_fold(nonfinite_fold(bad, bf16_lo(v.z)),
+                                                     bf16_hi(v.z)),
+                                      bf16_lo(v.w)),
+                       bf16_hi(v.w));
+}
+
+// The e4m3 codes of 8 bf16 values divided by s (IEEE division, round to nearest even).
+__device__ __forceinline__ uint2 cast8(const uint4& v, float s) {
+  uint2 q;
+  q.x = cvt_e4m3x4(__fdiv_rn(bf16_lo(v.x), s), __fdiv_rn(bf16_hi(v.x), s),
+                   __fdiv_rn(bf16_lo(v.y), s), __fdiv_rn(bf16_hi(v.y), s));
+  q.y = cvt_e4m3x4(__fdiv_rn(bf16_lo(v.z), s), __fdiv_rn(bf16_hi(v.z), s),
+                   __fdiv_rn(bf16_lo(v.w), s), __fdiv_rn(bf16_hi(v.w), s));
+  return q;
+}
+
 __global__ void amax_kernel(const uint4* __restrict__ x, int64_t n8, uint32_t* __restrict__ amax_bits,
                             int32_t* status) {
   float m = 0.0f, bad = 0.0f;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const uint4 v = __ldg(x + i);
-    m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
-                       fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)))));
-    m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))),
-                       fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)))));
-    bad = nonfinite_fold(nonfinite_fold(nonfinite_fold(nonfinite_fold(bad, bf16_lo(v.x)),
-                                                       bf16_hi(v.x)),
-                                        bf16_lo(v.y)),
-                         bf16_hi(v.y));
-    bad = nonfinite_fold(nonfinite_fold(nonfinite_fold(nonfinite_fold(bad, bf16_lo(v.z)),
-                                                       bf16_hi(v.z)),
-                                        bf16_lo(v.w)),
-                         bf16_hi(v.w));
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  // kQuantUnroll independent 16-byte loads in flight per thread and trip
+  for (int64_t i0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i0 < n8;
+       i0 += stride * kQuantUnroll) {
+    uint4 v[kQuantUnroll];
+#pragma unroll
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const int64_t i = i0 + u * stride;
+      v[u] = i < n8 ? __ldg(x + i) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kQuantUnroll; ++u) amax_fold8(v[u], m, bad);
   }
   report_nonfinite(status, bad);
 #pragma unroll
@@ -58,15 +81,20 @@ __global__ void cast_per_tensor_kernel(const uint4* __restrict__ x, int64_t n8,
     xs[0] = s;
     if (scale_out) *scale_out = s;
   }
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const uint4 v = __ldg(x + i);
-    uint2 q;
-    q.x = cvt_e4m3x4(__fdiv_rn(bf16_lo(v.x), s), __fdiv_rn(bf16_hi(v.x), s),
-                     __fdiv_rn(bf16_lo(v.y), s), __fdiv_rn(bf16_hi(v.y), s));
-    q.y = cvt_e4m3x4(__fdiv_rn(bf16_lo(v.z), s), __fdiv_rn(bf16_hi(v.z), s),
-                     __fdiv_rn(bf16_lo(v.w), s), __fdiv_rn(bf16_hi(v.w), s));
-    xq[i] = q;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i0 < n8;
+       i0 += stride * kQuantUnroll) {
+    uint4 v[kQuantUnroll];
+#pragma unroll
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const int64_t i = i0 + u * stride;
+      v[u] = i < n8 ? __ldg(x + i) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < n8) xq[i] = cast8(v[u], s);
+    }
   }
 }
 
@@ -81,34 +109,33 @@ __global__ void quant_row_kernel(const uint4* __restrict__ x, int64_t M, int64_t
   for (int64_t r = wid; r < M; r += nw) {
     const uint4* xr = x + r * n8_row;
     float amax = 0.0f, bad = 0.0f;
-    for (int64_t i = lane; i < n8_row; i += 32) {
-      const uint4 v = __ldg(xr + i);
-      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
-                               fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)))));
-      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))),
-                               fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)))));
-      bad = nonfinite_fold(nonfinite_fold(nonfinite_fold(nonfinite_fold(bad, bf16_lo(v.x)),
-                                                         bf16_hi(v.x)),
-                                          bf16_lo(v.y)),
-                           bf16_hi(v.y));
-      bad = nonfinite_fold(nonfinite_fold(nonfinite_fold(nonfinite_fold(bad, bf16_lo(v.z)),
-                                                         bf16_hi(v.z)),
-                                          bf16_lo(v.w)),
-                           bf16_hi(v.w));
+    for (int64_t i0 = lane; i0 < n8_row; i0 += 32 * kQuantUnroll) {
+      uint4 v[kQuantUnroll];
+#pragma unroll
+      for (int u = 0; u < kQuantUnroll; ++u) {
+        const int64_t i = i0 + 32 * u;
+        v[u] = i < n8_row ? __ldg(xr + i) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kQuantUnroll; ++u) amax_fold8(v[u], amax, bad);
     }
     report_nonfinite(status, bad);
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
     const float s = scale_from_amax(amax);
     uint2* qr = xq + r * n8_row;
-    for (int64_t i = lane; i < n8_row; i += 32) {
-      const uint4 v = __ldg(xr + i);
-      uint2 q;
-      q.x = cvt_e4m3x4(__fdiv_rn(bf16_lo(v.x), s), __fdiv_rn(bf16_hi(v.x), s),
-                       __fdiv_rn(bf16_lo(v.y), s), __fdiv_rn(bf16_hi(v.y), s));
-      q.y = cvt_e4m3x4(__fdiv_rn(bf16_lo(v.z), s), __fdiv_rn(bf16_hi(v.z), s),
-                       __fdiv_rn(bf16_lo(v.w), s), __fdiv_rn(bf16_hi(v.w), s));
-      qr[i] = q;
+    for (int64_t i0 = lane; i0 < n8_row; i0 += 32 * kQuantUnroll) {
+      uint4 v[kQuantUnroll];
+#pragma unroll
+      for (int u = 0; u < kQuantUnroll; ++u) {
+        const int64_t i = i0 + 32 * u;
+        v[u] = i < n8_row ? __ldg(xr + i) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kQuantUnroll; ++u) {
+        const int64_t i = i0 + 32 * u;
+        if (i < n8_row) qr[i] = cast8(v[u], s);
+      }
     }
     if (lane == 0) xs[r] = s;
   }
@@ -182,12 +209,72 @@ cudaError_t launch_quant_rows(const uint16_t* x, int64_t M, int64_t K, uint8_t* 
   return cudaGetLastError();
 }
 
+// Per-tensor quantization of a small tensor (decode sizes) in one CTA: each thread holds its
+// kSmallPer 16-byte chunks in registers, the block reduces the amax, and the same registers
+// are cast -- one launch, one read, no atomics.  The amax and the codes are those of the
+// two-pass kernels (a max does not depend on the order of its operands).
+constexpr int kSmallThreads = 1024, kSmallPer = 8;
+
+__global__ void __launch_bounds__(kSmallThreads, 1)
+    quant_tensor_small_kernel(const uint4* __restrict__ x, int64_t n8, uint2* __restrict__ xq,
+                              float* __restrict__ xs, float* __restrict__ scale_out,
+                              int32_t* status, int32_t* zero, int n_zero) {
+  for (int i = threadIdx.x; i < n_zero; i += kSmallThreads) zero[i] = 0;
+  uint4 v[kSmallPer];
+  float m = 0.0f, bad = 0.0f;
+#pragma unroll
+  for (int u = 0; u < kSmallPer; ++u) {
+    const int64_t i = threadIdx.x + static_cast<int64_t>(u) * kSmallThreads;
+    v[u] = i < n8 ? __ldg(x + i) : make_uint4(0, 0, 0, 0);
+    amax_fold8(v[u], m, bad);
+  }
+  report_nonfinite(status, bad);
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+  __shared__ float red[32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = red[threadIdx.x & 31];
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+  const float sc = scale_from_amax(m);
+  if (threadIdx.x == 0) {
+    xs[0] = sc;
+    if (scale_out) *scale_out = sc;
+  }
+#pragma unroll
+  for (int u = 0; u < kSmallPer; ++u) {
+    const int64_t i = threadIdx.x + static_cast<int64_t>(u) * kSmallThreads;
+    if (i < n8) xq[i] = cast8(v[u], sc);
+  }
+}
+
 cudaError_t launch_quant_per_tensor(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq,
-                                    float* xs, WsHeader* hdr, cudaStream_t s) {
+                                    float* xs, WsHeader* hdr, cudaStream_t s, int32_t* zero,
+                                    int n_zero) {
   const int64_t n8 = M * K / 8;
-  cudaError_t e = cudaMemsetAsync(&hdr->amax_bits, 0, sizeof(uint32_t), s);
+  if (n8 <= static_cast<int64_t>(kSmallThreads) * kSmallPer) {
+    quant_tensor_small_kernel<<<1, kSmallThreads, 0, s>>>(
+        reinterpret_cast<const uint4*>(x), n8, reinterpret_cast<uint2*>(xq), xs, &hdr->scale,
+        &hdr->status, zero, n_zero);
+    return cudaGetLastError();
+  }
+  // the amax word, and the words to clear when they follow the header directly (one memset)
+  uint8_t* hdr_end = reinterpret_cast<uint8_t*>(hdr) + sizeof(WsHeader);
+  const bool adjacent = n_zero > 0 && reinterpret_cast<uint8_t*>(zero) == hdr_end;
+  cudaError_t e = cudaMemsetAsync(&hdr->amax_bits, 0,
+                                  adjacent ? static_cast<size_t>(hdr_end - reinterpret_cast<uint8_t*>(
+                                                                               &hdr->amax_bits)) +
+                                                 static_cast<size_t>(n_zero) * 4
+                                           : sizeof(uint32_t),
+                                  s);
   if (e != cudaSuccess) return e;
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((n8 + 255) / 256, num_sms() * 4)));
+  if (n_zero > 0 && !adjacent) {
+    e = cudaMemsetAsync(zero, 0, static_cast<size_t>(n_zero) * 4, s);
+    if (e != cudaSuccess) return e;
+  }
+  const int grid = static_cast<int>(
+      std::max<int64_t>(1, std::min<int64_t>((n8 + 255) / 256, num_sms() * 8)));
   if (n8 > 0) {
     amax_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), n8, &hdr->amax_bits,
                                      &hdr->status);

@@ -79,7 +79,7 @@ typedef enum {
   FGE_OP_QUANT_PER_TENSOR = 0, /* args: (M, K) */
   FGE_OP_PERMUTE = 1,          /* args: (T, H, -, E, k) */
   FGE_OP_GROUPED_GEMM = 2,     /* args: unused */
-  FGE_OP_LINEAR_W8A8 = 3,      /* args: (M, K) */
+  FGE_OP_LINEAR_W8A8 = 3,      /* args: (M, K, N); N = 0: no K-split scratch */
   FGE_OP_MOE_LAYER = 4,        /* args: (T, H, I, E, k) */
   FGE_OP_DISPATCH_BASELINE = 5, /* args: (T, H, I, E, k) */
   FGE_OP_LINEAR_W8A8_ROWS = 6   /* args: (M, K) */
@@ -288,7 +288,13 @@ fge_status fge_gemm_w8a8(const uint8_t* aq, const float* sa, int64_t M, int64_t 
 /* linear_w8a8 -- the whole dense projection in one call, as the "Module fp8_ffi" prefill
  * call does it: per-tensor amax, scale, e4m3 cast, then the W8A8 GEMM, one stream, no host
  * sync.  x_bf16: [M, K]; wq: [N, K] e4m3 with device scalar w_scale; y_bf16: [M, N].
- * Workspace: FGE_OP_LINEAR_W8A8 (holds the quantized activation and the scale block). */
+ * Workspace: FGE_OP_LINEAR_W8A8 (holds the quantized activation and the scale block).  At
+ * decode sizes (M <= 16) the GEMM splits K over several CTAs per 128-feature tile (as many as
+ * fill the SMs in one wave, each at least two 128-wide K groups); the last of them to finish
+ * adds the fp32 partials in split order, so the result does not depend on timing.  That needs
+ * scratch for the partials: size the workspace with N
+ * (fge_workspace_bytes(FGE_OP_LINEAR_W8A8, M, K, N)); a workspace sized without it runs the
+ * GEMM unsplit. */
 fge_status fge_linear_w8a8(const void* x_bf16, int64_t M, int64_t K, const uint8_t* wq,
                            const float* w_scale, int64_t N, void* y_bf16, void* workspace,
                            size_t workspace_bytes, fge_stream_t stream);
