@@ -14,6 +14,16 @@ namespace fge {
 constexpr int kChunkTokens = 128;  // tokens per permutation chunk
 
 // ------------------------------------------------------------------------------ top-k
+// Float bits mapped to an unsigned key with the same order (negative values reversed).
+// -0 and +0 compare equal as floats, so both take the key of +0.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = f == 0.0f ? 0u : __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// One warp per token: lane l holds logits l, l + 32, ...; k rounds, each taking the largest
+// untaken logit (ties to the lower expert id) with two warp reductions: the maximum key,
+// then the lowest id among the lanes holding it.
 template <int PER>
 __global__ void topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k,
                             int32_t* __restrict__ ids, float* __restrict__ gates) {
@@ -31,29 +41,31 @@ __global__ void topk_kernel(const float* __restrict__ logits, int64_t T, int E, 
     float my_val = 0.0f;
     int my_id = 0;
     for (int j = 0; j < k; ++j) {
-      float best = -INFINITY;
+      // this lane's best untaken logit (the lowest id among equal ones: i ascending)
+      uint32_t best = 0u;
       int bi = 0x7fffffff;
 #pragma unroll
       for (int i = 0; i < PER; ++i) {
         const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && (v[i] > best || (v[i] == best && e < bi))) {
-          best = v[i];
+        const uint32_t key = order_key(v[i]);
+        if (e < E && !((taken >> i) & 1u) && (bi == 0x7fffffff || key > best)) {
+          best = key;
           bi = e;
         }
       }
+      const uint32_t top = __reduce_max_sync(0xffffffffu, best);
+      const int id = static_cast<int>(__reduce_min_sync(
+          0xffffffffu, static_cast<uint32_t>(bi != 0x7fffffff && best == top ? bi : 0x7fffffff)));
+      if ((id & 31) == lane) taken |= 1u << (id >> 5);
+      // the chosen logit itself, from the lane that holds it
+      float chosen = 0.0f;
 #pragma unroll
-      for (int d = 16; d > 0; d >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, best, d);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
-        if (ov > best || (ov == best && oi < bi)) {
-          best = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      for (int i = 0; i < PER; ++i)
+        if (lane + 32 * i == id) chosen = v[i];
+      chosen = __shfl_sync(0xffffffffu, chosen, id & 31);
       if (lane == j) {
-        my_val = best;
-        my_id = bi;
+        my_id = id;
+        my_val = chosen;
       }
     }
     const float m = __shfl_sync(0xffffffffu, my_val, 0);
