@@ -69,6 +69,8 @@ def lib():
             "fo_moe_layer_forward": (i32, [f32p, f32p, i64, i64, i32, i32, i64, u8p, f32p, u8p,
                                            f32p, i32, f32p]),
             "fo_mx_quant_e2m1": (None, [f32p, i64, i64, u8p, u8p]),
+            "fo_grouped_gemm_mxf4_w4": (None, [u8p, u8p, i32p, i32, u8p, f32p, i64, i64, i64,
+                                               f64p]),
             "fo_rmsnorm": (None, [f32p, i64, i64, f32p]),
             "fo_router_logits": (None, [f32p, f32p, i64, i64, i32, f32p]),
             "fo_identity_attention": (None, [f32p, i64, i32, i32, f32p]),
@@ -241,6 +243,21 @@ def mx_quant_e2m1(x):
     lib().fo_mx_quant_e2m1(_p(x, ctypes.c_float), m, k, _p(packed, ctypes.c_uint8),
                            _p(scales, ctypes.c_uint8))
     return packed, scales
+
+
+def grouped_gemm_mxf4_w4(codes, scales, offsets, w_packed, w_scale):
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    offsets = _c(offsets, np.int32)
+    w = _c(w_packed, np.uint8)
+    sw = _c(w_scale, np.float32)
+    r, kh = codes.shape
+    e, n, _ = w.shape
+    out = np.empty((r, n), dtype=np.float64)
+    lib().fo_grouped_gemm_mxf4_w4(_p(codes, ctypes.c_uint8), _p(scales, ctypes.c_uint8),
+                                  _p(offsets, ctypes.c_int32), e, _p(w, ctypes.c_uint8),
+                                  _p(sw, ctypes.c_float), n, 2 * kh, r, _p(out, ctypes.c_double))
+    return out
 
 
 def rmsnorm(h):

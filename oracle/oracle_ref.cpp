@@ -474,6 +474,46 @@ void fo_mx_quant_e2m1(const float* x, int64_t M, int64_t K, uint8_t* packed, uin
   }
 }
 
+// Grouped expert GEMM with MXFP4 activations: for expert e and its rows,
+//   C[r, n] = sum_g sw[e, n, g] * sum_{k in g} a[r, k] * q[e, n, k],
+//   a[r, k] = e2m1(code) * 2^(scale[r, k / 32] - 127).
+// Here the E2M1 value is decoded from its fields (sign bit 3; exponent bits 2..1, bias 1;
+// mantissa bit 0; exponent 0 is the subnormal step 0.5) and scaled with ldexp; plain loops,
+// float64 throughout.  codes [R, K/2] (element 2b in the low nibble); scales [R, K/32].
+static double e2m1_field_value(int code) {
+  const int e = (code >> 1) & 3, m = code & 1;
+  const double mag = e == 0 ? 0.5 * m : std::ldexp(1.0 + 0.5 * m, e - 1);
+  return (code & 8) ? -mag : mag;
+}
+
+void fo_grouped_gemm_mxf4_w4(const uint8_t* codes, const uint8_t* scales, const int32_t* offsets,
+                             int E, const uint8_t* w, const float* sw, int64_t N, int64_t K,
+                             int64_t R, double* out) {
+  const int64_t G = K / kGroup;
+  for (int64_t i = 0; i < R * N; ++i) out[i] = 0.0;
+  std::vector<double> arow(K);
+  for (int e = 0; e < E; ++e) {
+    const int64_t r0 = offsets[e], r1 = offsets[e + 1];
+    for (int64_t r = r0; r < r1; ++r) {
+      for (int64_t kk = 0; kk < K; ++kk) {
+        const uint8_t byte = codes[r * (K / 2) + kk / 2];
+        const int code = (kk & 1) ? (byte >> 4) : (byte & 0xF);
+        arow[kk] = std::ldexp(e2m1_field_value(code), static_cast<int>(scales[r * (K / 32) + kk / 32]) - 127);
+      }
+      for (int64_t n = 0; n < N; ++n) {
+        const uint8_t* wrow = w + (static_cast<int64_t>(e) * N + n) * (K / 2);
+        double acc = 0.0;
+        for (int64_t g = 0; g < G; ++g) {
+          double part = 0.0;
+          for (int64_t kk = g * kGroup; kk < (g + 1) * kGroup; ++kk) part += arow[kk] * int4_at(wrow, kk);
+          acc += static_cast<double>(sw[(static_cast<int64_t>(e) * N + n) * G + g]) * part;
+        }
+        out[r * N + n] = acc;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------ stacked-layer helpers
 // The stacked prefill workload's glue, not a page step.  Readings: a pre-norm block whose
 // RMSNorm has unit gain and eps 1e-6, computed in float64 and rounded to bfloat16; router

@@ -296,3 +296,21 @@ def test_stacked_prefill_equals_numpy():
                 np.sqrt((hc.astype(np.float64) ** 2).sum() * (hn.astype(np.float64) ** 2).sum()))
     assert cos >= 0.99999, cos
     assert all(np.array_equal(a, b) for a, b in zip(rc, rn))
+
+
+def test_mx_grouped_gemm_equals_numpy():
+    # the C++ restatement (E2M1 values from their fields, ldexp scaling, per-element loops)
+    # against the numpy one (decode table, dequantized matrix, matmul per group), routed rows
+    # with an empty expert and block scales spread over several binades
+    rng = np.random.default_rng(17)
+    counts = [40, 0, 23, 1]
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    r, k, n = int(offsets[-1]), 384, 48
+    codes = rng.integers(0, 256, (r, k // 2)).astype(np.uint8)
+    scales = rng.integers(115, 140, (r, k // 32)).astype(np.uint8)
+    q = rng.integers(-8, 8, (4, n, k))
+    wp = (q[..., 0::2] & 0xF | (q[..., 1::2] & 0xF) << 4).astype(np.uint8)
+    sw = rng.uniform(0.002, 0.02, (4, n, k // 128)).astype(np.float32)
+    got = cpp.grouped_gemm_mxf4_w4(codes, scales, offsets, wp, sw)
+    ref = oracle.grouped_gemm_mxf4_w4(codes, scales, offsets, wp, sw)
+    assert np.array_equal(got, ref)
