@@ -4,15 +4,19 @@
 // dense W8A8 projection ("feat(qwen4_exp): load-time per-tensor FP8 dense projections").
 //
 // Per CTA (one per SM), warp roles:
-//   warps 0-3   unpack: int4 tile (shared memory) -> e4m3 in the 128-byte swizzle layout
+//   warps 0-3   unpack: int4 tile (shared memory) -> e4m3 in the 128-byte swizzle layout;
+//               with MXFP4 activations also the K group's block scales into TMEM
 //   warp  6     TMA producer: A tile [128 rows x 128 K] + B tile per K group
-//   warp  7     TMEM allocator and single-thread tcgen05.mma issuer (kind::f8f6f4)
+//   warp  7     TMEM allocator and single-thread tcgen05.mma issuer (kind::f8f6f4, or the
+//               block-scaled kind::mxf8f6f4 for MXFP4 activations)
 //   warps 4-5   idle
 //   warps 8..   epilogue warpgroups: per-group fp32 promotion acc += as*sw*P from TMEM,
-//               then the store / SwiGLU + requant epilogue
+//               then the store / SwiGLU + requant epilogue (optionally the folded combine)
 // A K group (128 values) is exactly one 128-byte swizzle atom row, so each pipeline
 // stage carries one group and each group is 4 MMAs of K = 32 into a fresh TMEM buffer.
 // Two TMEM buffers (2 x BN columns) let the MMA run one group ahead of the promotion.
+// Run with one group (per-tensor scales) the whole K accumulates in TMEM; at decode sizes
+// K may be split over several CTAs per output tile (SplitArgs).
 #include <algorithm>
 #include <mutex>
 #include <cudaTypedefs.h>
