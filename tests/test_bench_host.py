@@ -49,9 +49,17 @@ def test_job_value_counts_every_rank():
 
 def test_kernel_key_tracks_the_gemm_sources():
     key = bench._kernel_key()
-    parts = key.split(":")
-    assert len(parts) == 2 and all(len(p) == 16 for p in parts)
-    int(parts[0], 16), int(parts[1], 16)
+    tag, a, b = key.split(":")
+    assert tag == "code" and len(a) == 16 and len(b) == 16
+    int(a, 16), int(b, 16)
+
+
+def test_kernel_key_ignores_comments_but_not_code():
+    src = "int f(int x) {\n  // a note\n  return x + 1;  /* another\n note */\n}\n"
+    same = "int f(int x) {\n  // the note, reworded\n  return x + 1;\n}\n"
+    other = "int f(int x) {\n  // a note\n  return x + 2;\n}\n"
+    assert bench._strip_comments(src) == bench._strip_comments(same)
+    assert bench._strip_comments(src) != bench._strip_comments(other)
 
 
 class _Inp:
