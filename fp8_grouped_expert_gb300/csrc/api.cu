@@ -715,7 +715,7 @@ fge_status fge_router_logits(const void* xn, const float* w, int64_t T, int64_t 
                              float* logits, fge_stream_t stream) {
   FGE_CHECK(cur_device_ok());
   FGE_REQUIRE(xn && w && logits, FGE_ERR_INVALID_ARG);
-  FGE_REQUIRE(T >= 0 && H > 0 && H % 256 == 0 && E >= 1, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(T >= 0 && H > 0 && H % 256 == 0 && H <= 7168 && E >= 1, FGE_ERR_BAD_SHAPE);
   FGE_REQUIRE(al16(xn) && al16(w), FGE_ERR_MISALIGNED);
   return from_cuda(launch_router(static_cast<const uint16_t*>(xn), w, T, H, E, logits, stream));
 }

@@ -42,32 +42,81 @@ __global__ void rmsnorm_kernel(const float* __restrict__ h, int64_t H, float eps
 }
 
 // One warp per (token, expert): fp32 dot product over H in a fixed lane-strided order.
-__global__ void router_kernel(const uint16_t* __restrict__ xn, const float* __restrict__ wr,
-                              int64_t T, int64_t H, int E, float* __restrict__ logits) {
-  const int lane = threadIdx.x & 31;
-  const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
-  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t item = wid; item < T * E; item += nw) {
-    const int64_t t = item / E, e = item % E;
-    const uint16_t* x = xn + t * H;
-    const float* w = wr + e * H;
-    float acc = 0.0f;
-    for (int64_t i = lane * 8; i < H; i += 256) {
-      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + i));
-      const float4 w0 = __ldg(reinterpret_cast<const float4*>(w + i));
-      const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + i + 4));
-      acc = fmaf(bf16_lo(xv.x), w0.x, acc);
-      acc = fmaf(bf16_hi(xv.x), w0.y, acc);
-      acc = fmaf(bf16_lo(xv.y), w0.z, acc);
-      acc = fmaf(bf16_hi(xv.y), w0.w, acc);
-      acc = fmaf(bf16_lo(xv.z), w1.x, acc);
-      acc = fmaf(bf16_hi(xv.z), w1.y, acc);
-      acc = fmaf(bf16_lo(xv.w), w1.z, acc);
-      acc = fmaf(bf16_hi(xv.w), w1.w, acc);
+// Router logits, logits[t, e] = sum_k xn[t, k] * wr[e, k] in fp32.  One block per kRouterTok
+// tokens: their bf16 rows stay in shared memory.  Each warp takes kRouterExp experts at a
+// time; lane l accumulates the products at k = 8 l + 256 i for every token of the block and
+// each of those experts, so a row chunk read from shared memory serves kRouterExp experts and
+// a router chunk read from L2 serves every token.  The warp then adds its lanes' sums.
+constexpr int kRouterTok = 16, kRouterExp = 4;
+
+__global__ void __launch_bounds__(256)
+    router_kernel(const uint16_t* __restrict__ xn, const float* __restrict__ wr, int64_t T,
+                  int64_t H, int E, float* __restrict__ logits) {
+  extern __shared__ uint4 sx[];  // [kRouterTok][H / 8], 8 bf16 each
+  const int64_t t0 = blockIdx.x * static_cast<int64_t>(kRouterTok);
+  const int nt = static_cast<int>(T - t0 < kRouterTok ? T - t0 : kRouterTok);
+  const int64_t row8 = H / 8;
+  for (int64_t i0 = threadIdx.x; i0 < kRouterTok * row8; i0 += 4 * blockDim.x) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {  // four loads in flight per thread
+      const int64_t i = i0 + u * blockDim.x;
+      const int r = static_cast<int>(i / row8);
+      v[u] = (i < kRouterTok * row8 && r < nt)
+                 ? __ldg(reinterpret_cast<const uint4*>(xn + (t0 + r) * H) + (i - r * row8))
+                 : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int d = 16; d > 0; d >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, d);
-    if (lane == 0) logits[item] = acc;
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * blockDim.x;
+      if (i < kRouterTok * row8) sx[i] = v[u];
+    }
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+  for (int e0 = warp * kRouterExp; e0 < E; e0 += nwarps * kRouterExp) {
+    float acc[kRouterExp][kRouterTok];
+#pragma unroll
+    for (int j = 0; j < kRouterExp; ++j)
+#pragma unroll
+      for (int r = 0; r < kRouterTok; ++r) acc[j][r] = 0.0f;
+    for (int64_t i = lane * 8; i < H; i += 256) {
+      float wv[kRouterExp][8];
+#pragma unroll
+      for (int j = 0; j < kRouterExp; ++j) {
+        const int e = min(e0 + j, E - 1);  // experts past E repeat the last; never stored
+        const float4 w0 = __ldg(reinterpret_cast<const float4*>(wr + e * H + i));
+        const float4 w1 = __ldg(reinterpret_cast<const float4*>(wr + e * H + i + 4));
+        wv[j][0] = w0.x; wv[j][1] = w0.y; wv[j][2] = w0.z; wv[j][3] = w0.w;
+        wv[j][4] = w1.x; wv[j][5] = w1.y; wv[j][6] = w1.z; wv[j][7] = w1.w;
+      }
+#pragma unroll
+      for (int r = 0; r < kRouterTok; ++r) {
+        const uint4 xv = sx[r * row8 + i / 8];
+        const float x[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
+                            bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
+#pragma unroll
+        for (int j = 0; j < kRouterExp; ++j) {
+          float a = acc[j][r];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) a = fmaf(x[c], wv[j][c], a);
+          acc[j][r] = a;
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kRouterExp; ++j)
+#pragma unroll
+      for (int r = 0; r < kRouterTok; ++r)
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) acc[j][r] += __shfl_xor_sync(0xffffffffu, acc[j][r], d);
+#pragma unroll
+    for (int j = 0; j < kRouterExp; ++j)
+#pragma unroll
+      for (int r = 0; r < kRouterTok; ++r)
+        if (lane == (j * kRouterTok + r) % 32 && r < nt && e0 + j < E)
+          logits[(t0 + r) * E + e0 + j] = acc[j][r];
   }
 }
 
@@ -111,8 +160,16 @@ cudaError_t launch_rmsnorm(const float* h, int64_t T, int64_t H, float eps, uint
 cudaError_t launch_router(const uint16_t* xn, const float* wr, int64_t T, int64_t H, int E,
                           float* logits, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const int grid = static_cast<int>(std::min<int64_t>((T * E + 7) / 8, num_sms() * 16));
-  router_kernel<<<grid, 256, 0, s>>>(xn, wr, T, H, E, logits);
+  const int smem = static_cast<int>(kRouterTok * H * 2);  // H <= 7168: at most 224 KB
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return ce;
+  // the limit is raised once per device to the largest row the call accepts
+  if (!device_kernel_ready(dev, reinterpret_cast<const void*>(router_kernel),
+                           kRouterTok * 7168 * 2, 0))
+    return cudaErrorInvalidConfiguration;
+  const unsigned grid = static_cast<unsigned>((T + kRouterTok - 1) / kRouterTok);
+  router_kernel<<<grid, 256, smem, s>>>(xn, wr, T, H, E, logits);
   return cudaGetLastError();
 }
 

@@ -402,8 +402,9 @@ fge_status fge_selftest_wait_timeout(void* workspace, int64_t budget_cycles,
 
 /* Glue of the stacked prefill (not page steps; RMSNorm, router, attention stand-in).
  * rmsnorm: out_bf16[t] = h[t] / sqrt(mean(h[t]^2) + eps), h float [T, H].
- * router_logits: logits[t, e] = sum_h xn[t, h] * w[e, h] (fp32, sequential in h);
- *   xn bf16 [T, H], w float [E, H].
+ * router_logits: logits[t, e] = sum_h xn[t, h] * w[e, h] in fp32 (lane l of a warp sums the
+ *   products at h = 256 i + 8 l + c, c < 8, in order, then the warp adds its 32 lane sums);
+ *   xn bf16 [T, H], w float [E, H]; H a multiple of 256, at most 7168.
  * identity_attention: attn[t, h*128 + d] = v[t, (h / (n_heads / n_kv_heads))*128 + d];
  *   v bf16 [T, n_kv_heads*128], attn bf16 [T, n_heads*128].
  * residual_add: h[i] += y[i] for i < n, h float, y in y_dtype. */
