@@ -12,6 +12,7 @@
 namespace fge {
 
 constexpr int kChunkTokens = 128;  // tokens per permutation chunk
+constexpr int kQuantPairs = 4;     // group pairs whose loads a warp keeps in flight
 
 // ------------------------------------------------------------------------------ top-k
 // Float bits mapped to an unsigned key with the same order (negative values reversed).
@@ -21,51 +22,93 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// One warp per token: lane l holds logits l, l + 32, ...; k rounds, each taking the largest
-// untaken logit (ties to the lower expert id) with two warp reductions: the maximum key,
-// then the lowest id among the lanes holding it.
+// The float a key stands for (the inverse of order_key; -0 comes back as +0).
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// One warp per token: lane l holds the keys of logits l, l + 32, ...; k rounds, each taking
+// the largest untaken key (ties to the lower expert id) with two warp reductions: the maximum
+// key, then the lowest id among the lanes offering it.  The chosen logit is read back from
+// the key.  Up to four keys a lane (E <= 128) are sorted once, by key descending and id
+// ascending, so a lane always offers its first entry and the winner shifts its list by one;
+// with more keys a lane rescans its untaken keys every round.
 template <int PER>
 __global__ void topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k,
                             int32_t* __restrict__ ids, float* __restrict__ gates) {
+  constexpr uint32_t kNone = 0x7fffffffu;
   const int lane = threadIdx.x & 31;
   const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   for (int64_t t = wid; t < T; t += nw) {
-    float v[PER];
+    uint32_t key[PER], id[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int e = lane + 32 * i;
-      v[i] = e < E ? __ldg(logits + t * E + e) : -FLT_MAX;
+      key[i] = e < E ? order_key(__ldg(logits + t * E + e)) : 0u;
+      id[i] = e < E ? static_cast<uint32_t>(e) : kNone;  // slots past E: offered last, never won
     }
-    uint32_t taken = 0;
     float my_val = 0.0f;
     int my_id = 0;
-    for (int j = 0; j < k; ++j) {
-      // this lane's best untaken logit (the lowest id among equal ones: i ascending)
-      uint32_t best = 0u;
-      int bi = 0x7fffffff;
+    if constexpr (PER <= 4) {
+      // sorting network on (key descending, id ascending): a total order, so the result is
+      // the same whatever the network
+      auto cswap = [&](int a, int b) {
+        const bool sw = key[b] > key[a] || (key[b] == key[a] && id[b] < id[a]);
+        const uint32_t ka = key[a], ia = id[a];
+        key[a] = sw ? key[b] : ka;
+        id[a] = sw ? id[b] : ia;
+        key[b] = sw ? ka : key[b];
+        id[b] = sw ? ia : id[b];
+      };
+      if constexpr (PER >= 2) cswap(0, 1);
+      if constexpr (PER == 3) {
+        cswap(1, 2);
+        cswap(0, 1);
+      }
+      if constexpr (PER == 4) {
+        cswap(2, 3);
+        cswap(0, 2);
+        cswap(1, 3);
+        cswap(1, 2);
+      }
+      for (int j = 0; j < k; ++j) {
+        const uint32_t top = __reduce_max_sync(0xffffffffu, key[0]);
+        const uint32_t win = __reduce_min_sync(0xffffffffu, key[0] == top ? id[0] : kNone);
+        if (id[0] == win) {
 #pragma unroll
-      for (int i = 0; i < PER; ++i) {
-        const int e = lane + 32 * i;
-        const uint32_t key = order_key(v[i]);
-        if (e < E && !((taken >> i) & 1u) && (bi == 0x7fffffff || key > best)) {
-          best = key;
-          bi = e;
+          for (int i = 0; i + 1 < PER; ++i) {
+            key[i] = key[i + 1];
+            id[i] = id[i + 1];
+          }
+          key[PER - 1] = 0u;
+          id[PER - 1] = kNone;
+        }
+        if (lane == j) {
+          my_id = static_cast<int>(win);
+          my_val = key_value(top);
         }
       }
-      const uint32_t top = __reduce_max_sync(0xffffffffu, best);
-      const int id = static_cast<int>(__reduce_min_sync(
-          0xffffffffu, static_cast<uint32_t>(bi != 0x7fffffff && best == top ? bi : 0x7fffffff)));
-      if ((id & 31) == lane) taken |= 1u << (id >> 5);
-      // the chosen logit itself, from the lane that holds it
-      float chosen = 0.0f;
+    } else {
+      uint32_t taken = 0;
+      for (int j = 0; j < k; ++j) {
+        // this lane's best untaken key (the lowest id among equal ones: i ascending)
+        uint32_t best = 0u, bid = kNone;
+        int bi = -1;
 #pragma unroll
-      for (int i = 0; i < PER; ++i)
-        if (lane + 32 * i == id) chosen = v[i];
-      chosen = __shfl_sync(0xffffffffu, chosen, id & 31);
-      if (lane == j) {
-        my_id = id;
-        my_val = chosen;
+        for (int i = 0; i < PER; ++i) {
+          const bool better = !((taken >> i) & 1u) && id[i] != kNone && (bi < 0 || key[i] > best);
+          best = better ? key[i] : best;
+          bid = better ? id[i] : bid;
+          bi = better ? i : bi;
+        }
+        const uint32_t top = __reduce_max_sync(0xffffffffu, best);
+        const uint32_t win = __reduce_min_sync(0xffffffffu, best == top ? bid : kNone);
+        if (bi >= 0 && bid == win) taken |= 1u << bi;
+        if (lane == j) {
+          my_id = static_cast<int>(win);
+          my_val = key_value(top);
+        }
       }
     }
     const float m = __shfl_sync(0xffffffffu, my_val, 0);
@@ -308,9 +351,6 @@ __global__ void permute_copy_kernel(const uint8_t* __restrict__ xq, const float*
 // each 128-value group exactly as quant_g128_kernel does (16 lanes x 8 values, shuffle amax,
 // s = amax / 448, IEEE division, e4m3 round to nearest even) and writes the codes and the
 // scale to the token's k expert rows.  Two groups per warp step.
-// kIdentity: the plain G128 quantization of x (k = 1, row t to row t, no token_row), the
-// same row-per-warp structure writing each row's codes and scales contiguously.
-template <bool kIdentity>
 __global__ void permute_quant_copy_kernel(const uint4* __restrict__ x, int64_t T, int k,
                                           int64_t H, const int32_t* __restrict__ token_row,
                                           uint8_t* __restrict__ aq, float* __restrict__ as,
@@ -322,8 +362,7 @@ __global__ void permute_quant_copy_kernel(const uint4* __restrict__ x, int64_t T
   const int64_t G = H / 128;
   constexpr int U = 4;  // group pairs per trip: their loads are issued together
   for (int64_t t = wid; t < T; t += nw) {
-    const int my_row = kIdentity ? static_cast<int>(t)
-                                 : (lane < k ? __ldg(token_row + t * k + lane) : 0);
+    const int my_row = lane < k ? __ldg(token_row + t * k + lane) : 0;
     for (int64_t g0 = 0; g0 < G; g0 += 2 * U) {  // all lanes iterate; shuffles stay full
       uint4 v[U];
 #pragma unroll
@@ -372,8 +411,8 @@ cudaError_t launch_permute_quant(const int32_t* ids, int64_t T, int k, int E,
                                  token_row, nullptr, nullptr, scratch, s);
   if (e != cudaSuccess || T == 0) return e;
   const int grid = static_cast<int>(std::min<int64_t>((T + 7) / 8, num_sms() * 8));
-  permute_quant_copy_kernel<false><<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), T, k,
-                                                        H, token_row, aq, as, status);
+  permute_quant_copy_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), T, k, H,
+                                                 token_row, aq, as, status);
   return cudaGetLastError();
 }
 
@@ -491,14 +530,65 @@ cudaError_t launch_combine(const void* y, int y_f32, const int32_t* token_row,
   return cudaGetLastError();
 }
 
-// The stand-alone G128 activation quantization: the quantizing copy in its identity form
-// (one warp per row, the row's codes and scales written contiguously).
+// The stand-alone G128 activation quantization.  Rows hold whole groups (K % 128 == 0), so
+// the tensor is a flat array of M * K / 128 groups whose scales are stored in the same order;
+// each half-warp quantizes one group exactly as the quantizing copy above does, and the warps
+// stride over group pairs with kQuantPairs pairs' loads in flight, so that every warp gets
+// the same share of the tensor whatever M and K are.
+__global__ void __launch_bounds__(256, 5)
+    quant_g128_kernel(const uint4* __restrict__ x, int64_t ngroups,
+                                  uint2* __restrict__ xq, float* __restrict__ xs,
+                                  int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4, hl = lane & 15;
+  const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t npairs = (ngroups + 1) / 2;
+  for (int64_t p0 = wid; p0 < npairs; p0 += nw * kQuantPairs) {  // warp-uniform trips
+    uint4 v[kQuantPairs];
+#pragma unroll
+    for (int u = 0; u < kQuantPairs; ++u) {
+      const int64_t g = 2 * (p0 + u * nw) + half;
+      v[u] = g < ngroups ? __ldcs(x + g * 16 + hl) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kQuantPairs; ++u) {
+      const int64_t g = 2 * (p0 + u * nw) + half;
+      const float f[8] = {bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y),
+                          bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w)};
+      float amax = 0.0f, bad = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        amax = fmaxf(amax, fabsf(f[i]));
+        bad = nonfinite_fold(bad, f[i]);
+      }
+      report_nonfinite(status, bad);
+#pragma unroll
+      for (int d = 8; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+      const float sc = scale_from_amax(amax);
+      if (g < ngroups) {
+        uint2 q;
+        q.x = cvt_e4m3x4(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc), __fdiv_rn(f[2], sc),
+                         __fdiv_rn(f[3], sc));
+        q.y = cvt_e4m3x4(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc), __fdiv_rn(f[6], sc),
+                         __fdiv_rn(f[7], sc));
+        __stcs(xq + g * 16 + hl, q);
+        if (hl == 0) xs[g] = sc;
+      }
+    }
+  }
+}
+
 cudaError_t launch_quant_g128(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,
                               int32_t* status, cudaStream_t s) {
-  if (M == 0) return cudaSuccess;
-  const int grid = static_cast<int>(std::min<int64_t>((M + 7) / 8, num_sms() * 8));
-  permute_quant_copy_kernel<true><<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), M, 1, K,
-                                                       nullptr, xq, xs, status);
+  const int64_t ngroups = M * (K / 128);
+  if (ngroups == 0) return cudaSuccess;
+  const int64_t pairs = (ngroups + 1) / 2;
+  // five blocks of 256 threads are resident per SM (launch bounds): one wave
+  const int grid = static_cast<int>(std::min<int64_t>(
+      (pairs + 8 * kQuantPairs - 1) / (8 * kQuantPairs), num_sms() * 5));
+  quant_g128_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), ngroups,
+                                         reinterpret_cast<uint2*>(xq), xs, status);
   return cudaGetLastError();
 }
 

@@ -52,13 +52,26 @@ def test_quant_zero_input_scale_floor(fge):
     assert np.all(host(xs) == 1.0) and not host(xq).any()
 
 
-@pytest.mark.parametrize("t,e,k", [(64, 8, 2), (4096, 64, 8), (1000, 128, 8), (33, 256, 32)])
+@pytest.mark.parametrize("t,e,k", [(64, 8, 2), (4096, 64, 8), (1000, 128, 8), (33, 256, 32),
+                                   (500, 96, 8), (300, 100, 6), (257, 40, 32), (77, 1000, 16)])
 def test_topk_gate(fge, t, e, k):
     rng = np.random.default_rng(t + e)
     lg = rng.standard_normal((t, e)).astype(np.float32)
     lg[: t // 4] = np.round(lg[: t // 4] * 2) / 2            # many exact ties
     ids, gates = fge.moe_topk_gate(to_dev(lg), k)
     rid, rg = oracle.topk_gate(lg, k)
+    assert np.array_equal(host(ids), rid)
+    np.testing.assert_allclose(host(gates), rg, rtol=2e-6, atol=0)
+
+
+def test_topk_gate_signed_zeros_tie(fge):
+    # -0 and +0 are equal logits: among them the lower expert id is taken first
+    rng = np.random.default_rng(5)
+    lg = np.where(rng.random((256, 64)) < 0.5, np.float32(-0.0), np.float32(0.0))
+    lg[:, 40] = -1.0
+    lg[::3, 7] = 2.0
+    ids, gates = fge.moe_topk_gate(to_dev(lg.astype(np.float32)), 4)
+    rid, rg = oracle.topk_gate(lg.astype(np.float32), 4)
     assert np.array_equal(host(ids), rid)
     np.testing.assert_allclose(host(gates), rg, rtol=2e-6, atol=0)
 
