@@ -169,23 +169,29 @@ def clear_device_status(ws):
 
 
 # ------------------------------------------------------------------------------ ops
-def fp8_quant_act(x, mode="g128", workspace=None):
+def fp8_quant_act(x, mode="g128", workspace=None, out=None):
     """x: bf16 [M, K] -> (xq uint8 [M, K], xs float32 [M, K/128] ("g128"), [M] ("row") or
-    [1] ("tensor"))."""
+    [1] ("tensor")).  out: an (xq, xs) pair of those shapes to write into."""
     _need(x, torch.bfloat16, "x")
     _ensure_init(x.device)
     m, k = x.shape
-    xq = torch.empty((m, k), dtype=torch.uint8, device=x.device)
+    n_scales = {"g128": (m, k // 128), "row": (m,)}.get(mode, (1,))
+    if out is not None:
+        xq, xs = out
+        _need(xq, torch.uint8, "xq")
+        _need(xs, torch.float32, "xs")
+        if tuple(xq.shape) != (m, k) or tuple(xs.shape) != n_scales:
+            raise ValueError("out shapes must be %s and %s" % ((m, k), n_scales))
+    else:
+        xq = torch.empty((m, k), dtype=torch.uint8, device=x.device)
+        xs = torch.empty(n_scales, dtype=torch.float32, device=x.device)
     if mode == "g128":
-        xs = torch.empty((m, k // 128), dtype=torch.float32, device=x.device)
         code = lib().fge_fp8_quant_act(_ptr(x), m, k, SCALE_PER_TOKEN_G128, _ptr(xq), _ptr(xs),
                                        None, 0, _stream(x))
     elif mode == "row":
-        xs = torch.empty((m,), dtype=torch.float32, device=x.device)
         code = lib().fge_fp8_quant_act(_ptr(x), m, k, SCALE_PER_ROW, _ptr(xq), _ptr(xs),
                                        None, 0, _stream(x))
     else:
-        xs = torch.empty((1,), dtype=torch.float32, device=x.device)
         ws = workspace if workspace is not None else new_workspace(
             workspace_bytes(OP_QUANT_PER_TENSOR, m, k), x.device)
         code = lib().fge_fp8_quant_act(_ptr(x), m, k, SCALE_PER_TENSOR, _ptr(xq), _ptr(xs),
@@ -412,7 +418,7 @@ def moe_combine(y, token_row, gates, out_dtype=torch.bfloat16):
     return out
 
 
-def gemm_w8a8(aq, sa, wq, sw, out_dtype=torch.bfloat16, workspace=None):
+def gemm_w8a8(aq, sa, wq, sw, out_dtype=torch.bfloat16, workspace=None, out=None):
     _need(aq, torch.uint8, "aq")
     _need(wq, torch.uint8, "wq")
     _ensure_init(aq.device)
@@ -420,7 +426,11 @@ def gemm_w8a8(aq, sa, wq, sw, out_dtype=torch.bfloat16, workspace=None):
     n = wq.shape[0]
     ws = workspace if workspace is not None else new_workspace(
         workspace_bytes(OP_GROUPED_GEMM), aq.device)
-    y = torch.empty((m, n), dtype=out_dtype, device=aq.device)
+    if out is not None:
+        _need(out, out_dtype, "out")
+        if tuple(out.shape) != (m, n):
+            raise ValueError("out must be [%d, %d]" % (m, n))
+    y = out if out is not None else torch.empty((m, n), dtype=out_dtype, device=aq.device)
     _check(lib().fge_gemm_w8a8(_ptr(aq), _ptr(sa), m, k, _ptr(wq), _ptr(sw), n,
                                DTYPE_F32 if out_dtype == torch.float32 else DTYPE_BF16, _ptr(y),
                                _ptr(ws), ws.numel(), _stream(aq)), "fge_gemm_w8a8")
@@ -648,7 +658,8 @@ def residual_add(h, y):
 # --------------------------------------------------------------------- stacked prefill
 class StackedPrefill:
     """L pre-norm blocks of the stacked prefill workload, every step a C-ABI call:
-    RMSNorm -> per-tensor W8A8 q/k/v -> identity attention on v -> W8A8 o -> fp32 residual
+    RMSNorm -> per-tensor W8A8 q/k/v (one quantization, q and k on side streams) ->
+    identity attention on v -> W8A8 o -> fp32 residual
     -> RMSNorm -> fp32 router -> MoE layer (top-k, quant, permute, grouped GEMMs, combine)
     -> fp32 residual.
 
@@ -688,9 +699,15 @@ class StackedPrefill:
             self.layers.append(d)
         dev = self.dev
         kv = n_kv_heads * 128
-        # one workspace for the four projections, sized for the largest K-split scratch
-        self.ws_lin = new_workspace(max(workspace_bytes(OP_LINEAR_W8A8, T, kin, n) for kin, n in
-                                        ((H, n_heads * 128), (H, kv), (n_heads * 128, H))), dev)
+        # the o projection quantizes its own input; q, k and v share one per-tensor
+        # quantization of the normed hidden state, and q and k run on side streams next to
+        # the rest of the layer (the identity attention reads only v)
+        self.ws_lin = new_workspace(workspace_bytes(OP_LINEAR_W8A8, T, n_heads * 128, H), dev)
+        self.ws_qt = new_workspace(workspace_bytes(OP_QUANT_PER_TENSOR, T, H), dev)
+        self.ws_proj = [new_workspace(workspace_bytes(OP_GROUPED_GEMM), dev) for _ in range(3)]
+        self.side = [torch.cuda.Stream(dev) for _ in range(2)]
+        self.xq = torch.empty((T, H), dtype=torch.uint8, device=dev)
+        self.xs = torch.empty((1,), dtype=torch.float32, device=dev)
         self.ws_moe = new_workspace(workspace_bytes(OP_MOE_LAYER, T, H, I, E, k), dev)
         self.xn = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         self.q = torch.empty((T, n_heads * 128), dtype=torch.bfloat16, device=dev)
@@ -706,10 +723,15 @@ class StackedPrefill:
         selects which layer indices to run (all, in order, by default)."""
         for li in (range(len(self.layers)) if layers is None else layers):
             d = self.layers[li]
+            main = torch.cuda.current_stream(self.dev)
             rmsnorm(h, out=self.xn)
-            linear_w8a8(self.xn, d["wq"], d["sq"], workspace=self.ws_lin, out=self.q)
-            linear_w8a8(self.xn, d["wk"], d["sk"], workspace=self.ws_lin, out=self.kk)
-            linear_w8a8(self.xn, d["wv"], d["sv"], workspace=self.ws_lin, out=self.v)
+            fp8_quant_act(self.xn, "tensor", workspace=self.ws_qt, out=(self.xq, self.xs))
+            for side, w, sc, ws, y in zip(self.side, ("wq", "wk"), ("sq", "sk"),
+                                          self.ws_proj, (self.q, self.kk)):
+                side.wait_stream(main)
+                with torch.cuda.stream(side):
+                    gemm_w8a8(self.xq, self.xs, d[w], d[sc], workspace=ws, out=y)
+            gemm_w8a8(self.xq, self.xs, d["wv"], d["sv"], workspace=self.ws_proj[2], out=self.v)
             identity_attention(self.v, self.n_heads, self.n_kv, out=self.attn)
             linear_w8a8(self.attn, d["wo"], d["so"], workspace=self.ws_lin, out=self.o)
             residual_add(h, self.o)
@@ -719,4 +741,6 @@ class StackedPrefill:
                               d["w_dn"], d["s_dn"], fmt=self.fmt, workspace=self.ws_moe,
                               out=self.y)
             residual_add(h, self.y)
+            for side in self.side:  # before the next layer rewrites xq, q and kk
+                main.wait_stream(side)
         return h
