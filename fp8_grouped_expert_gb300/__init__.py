@@ -72,6 +72,7 @@ SIGNATURES = {
     "fge_router_logits": [_P, _P, _I64, _I64, _I, _P, _P],
     "fge_identity_attention": [_P, _I64, _I, _I, _P, _P],
     "fge_residual_add": [_P, _P, _I, _I64, _P],
+    "fge_residual_rmsnorm": [_P, _P, _I, _I64, _I64, ctypes.c_float, _P, _P],
 }
 _RESTYPES = {"fge_version": ctypes.c_int, "fge_status_string": ctypes.c_char_p,
              "fge_workspace_bytes": ctypes.c_size_t}
@@ -655,6 +656,20 @@ def residual_add(h, y):
     return h
 
 
+def residual_rmsnorm(h, y, eps=1e-6, out=None):
+    """h += y, then rmsnorm(h) as bf16 (the same bits as residual_add then rmsnorm)."""
+    _need(h, torch.float32, "h")
+    _ensure_init(h.device)
+    if tuple(y.shape) != tuple(h.shape):
+        raise ValueError("y must have h's shape")
+    t, d = h.shape
+    xn = out if out is not None else torch.empty((t, d), dtype=torch.bfloat16, device=h.device)
+    _check(lib().fge_residual_rmsnorm(_ptr(h), _ptr(y),
+                                      DTYPE_F32 if y.dtype == torch.float32 else DTYPE_BF16,
+                                      t, d, eps, _ptr(xn), _stream(h)), "fge_residual_rmsnorm")
+    return xn
+
+
 # --------------------------------------------------------------------- stacked prefill
 class StackedPrefill:
     """L pre-norm blocks of the stacked prefill workload, every step a C-ABI call:
@@ -720,11 +735,15 @@ class StackedPrefill:
 
     def forward(self, h, layers=None):
         """h: float32 [T, H] on the device, updated in place and returned.  ``layers``
-        selects which layer indices to run (all, in order, by default)."""
-        for li in (range(len(self.layers)) if layers is None else layers):
+        selects which layer indices to run (all, in order, by default).  Each residual add
+        that a norm follows runs fused with it (fge_residual_rmsnorm, the same bits)."""
+        order = list(range(len(self.layers)) if layers is None else layers)
+        if not order:
+            return h
+        rmsnorm(h, out=self.xn)
+        for n, li in enumerate(order):
             d = self.layers[li]
             main = torch.cuda.current_stream(self.dev)
-            rmsnorm(h, out=self.xn)
             fp8_quant_act(self.xn, "tensor", workspace=self.ws_qt, out=(self.xq, self.xs))
             for side, w, sc, ws, y in zip(self.side, ("wq", "wk"), ("sq", "sk"),
                                           self.ws_proj, (self.q, self.kk)):
@@ -734,13 +753,15 @@ class StackedPrefill:
             gemm_w8a8(self.xq, self.xs, d["wv"], d["sv"], workspace=self.ws_proj[2], out=self.v)
             identity_attention(self.v, self.n_heads, self.n_kv, out=self.attn)
             linear_w8a8(self.attn, d["wo"], d["so"], workspace=self.ws_lin, out=self.o)
-            residual_add(h, self.o)
-            rmsnorm(h, out=self.xn)
+            residual_rmsnorm(h, self.o, out=self.xn)
             router_logits(self.xn, d["w_router"], out=self.logits)
             moe_layer_forward(self.logits, self.xn, self.k, self.I, d["w_gu"], d["s_gu"],
                               d["w_dn"], d["s_dn"], fmt=self.fmt, workspace=self.ws_moe,
                               out=self.y)
-            residual_add(h, self.y)
+            if n + 1 < len(order):
+                residual_rmsnorm(h, self.y, out=self.xn)  # the next layer's first norm
+            else:
+                residual_add(h, self.y)
             for side in self.side:  # before the next layer rewrites xq, q and kk
                 main.wait_stream(side)
         return h

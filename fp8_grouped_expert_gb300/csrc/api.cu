@@ -715,7 +715,8 @@ fge_status fge_router_logits(const void* xn, const float* w, int64_t T, int64_t 
                              float* logits, fge_stream_t stream) {
   FGE_CHECK(cur_device_ok());
   FGE_REQUIRE(xn && w && logits, FGE_ERR_INVALID_ARG);
-  FGE_REQUIRE(T >= 0 && H > 0 && H % 256 == 0 && H <= 7168 && E >= 1, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(T >= 0 && H > 0 && H % 256 == 0 && H <= 7168 && E >= 1 && E <= 65536,
+              FGE_ERR_BAD_SHAPE);
   FGE_REQUIRE(al16(xn) && al16(w), FGE_ERR_MISALIGNED);
   return from_cuda(launch_router(static_cast<const uint16_t*>(xn), w, T, H, E, logits, stream));
 }
@@ -738,6 +739,17 @@ fge_status fge_residual_add(float* h, const void* y, fge_dtype y_dtype, int64_t 
   FGE_REQUIRE(n >= 0 && n % 4 == 0, FGE_ERR_BAD_SHAPE);
   FGE_REQUIRE(al16(h) && al16(y), FGE_ERR_MISALIGNED);
   return from_cuda(launch_residual_add(h, y, y_dtype == FGE_DTYPE_F32, n, stream));
+}
+
+fge_status fge_residual_rmsnorm(float* h, const void* y, fge_dtype y_dtype, int64_t T,
+                                int64_t H, float eps, void* out, fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(h && y && out, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(y_dtype == FGE_DTYPE_BF16 || y_dtype == FGE_DTYPE_F32, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(T >= 0 && H > 0 && H % 8 == 0, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(al16(h) && al16(y) && al16(out), FGE_ERR_MISALIGNED);
+  return from_cuda(launch_residual_rmsnorm(h, y, y_dtype == FGE_DTYPE_F32, T, H, eps,
+                                           static_cast<uint16_t*>(out), stream));
 }
 
 }  // extern "C"

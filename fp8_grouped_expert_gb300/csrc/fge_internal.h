@@ -125,6 +125,8 @@ cudaError_t launch_router(const uint16_t* xn, const float* wr, int64_t T, int64_
 cudaError_t launch_identity_attention(const uint16_t* v, int64_t T, int n_heads, int n_kv,
                                       uint16_t* attn, cudaStream_t s);
 cudaError_t launch_residual_add(float* h, const void* y, int y_f32, int64_t n, cudaStream_t s);
+cudaError_t launch_residual_rmsnorm(float* h, const void* y, int y_f32, int64_t T, int64_t H,
+                                    float eps, uint16_t* out, cudaStream_t s);
 
 cudaError_t launch_per_token_dispatch(const uint16_t* x, const int32_t* ids, int64_t T, int k,
                                       int64_t H, int64_t I, const uint8_t* w_gu,

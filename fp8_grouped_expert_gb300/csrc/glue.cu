@@ -7,12 +7,28 @@
 namespace fge {
 
 // One block per row: sum of squares in fp32, then h / sqrt(mean + eps) rounded to bf16.
-__global__ void rmsnorm_kernel(const float* __restrict__ h, int64_t H, float eps,
-                               uint16_t* __restrict__ out) {
-  const float* row = h + blockIdx.x * H;
+// ADD: the residual add first, h[t] += y[t] (y bf16 or float, YF32), the updated row written
+// back; each thread adds and squares the same elements in the same order as the separate
+// residual add followed by the plain norm, so the two give the same bits.
+template <bool ADD, bool YF32>
+__global__ void rmsnorm_kernel(float* __restrict__ h, const void* __restrict__ y, int64_t H,
+                               float eps, uint16_t* __restrict__ out) {
+  float* row = h + blockIdx.x * H;
   float ss = 0.0f;
   for (int64_t i = threadIdx.x * 4; i < H; i += blockDim.x * 4) {
-    const float4 v = *reinterpret_cast<const float4*>(row + i);
+    float4 v = *reinterpret_cast<const float4*>(row + i);
+    if constexpr (ADD) {
+      if constexpr (YF32) {
+        const float4 b =
+            *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(y) + blockIdx.x * H + i);
+        v.x += b.x; v.y += b.y; v.z += b.z; v.w += b.w;
+      } else {
+        const uint2 b = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(y) +
+                                                        blockIdx.x * H + i);
+        v.x += bf16_lo(b.x); v.y += bf16_hi(b.x); v.z += bf16_lo(b.y); v.w += bf16_hi(b.y);
+      }
+      *reinterpret_cast<float4*>(row + i) = v;
+    }
     ss = fmaf(v.x, v.x, ss);
     ss = fmaf(v.y, v.y, ss);
     ss = fmaf(v.z, v.z, ss);
@@ -32,6 +48,7 @@ __global__ void rmsnorm_kernel(const float* __restrict__ h, int64_t H, float eps
   __syncthreads();
   const float denom = __fsqrt_rn(__fdiv_rn(red[0], static_cast<float>(H)) + eps);
   uint16_t* orow = out + blockIdx.x * H;
+  // each thread reads back only the elements it wrote itself
   for (int64_t i = threadIdx.x * 4; i < H; i += blockDim.x * 4) {
     const float4 v = *reinterpret_cast<const float4*>(row + i);
     uint2 o;
@@ -41,9 +58,8 @@ __global__ void rmsnorm_kernel(const float* __restrict__ h, int64_t H, float eps
   }
 }
 
-// One warp per (token, expert): fp32 dot product over H in a fixed lane-strided order.
 // Router logits, logits[t, e] = sum_k xn[t, k] * wr[e, k] in fp32.  One block per kRouterTok
-// tokens: their bf16 rows stay in shared memory.  Each warp takes kRouterExp experts at a
+// tokens and 32 experts: the tokens' bf16 rows stay in shared memory.  Each warp takes kRouterExp experts at a
 // time; lane l accumulates the products at k = 8 l + 256 i for every token of the block and
 // each of those experts, so a row chunk read from shared memory serves kRouterExp experts and
 // a router chunk read from L2 serves every token.  The warp then adds its lanes' sums.
@@ -75,7 +91,9 @@ __global__ void __launch_bounds__(256)
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
-  for (int e0 = warp * kRouterExp; e0 < E; e0 += nwarps * kRouterExp) {
+  const int e_end = min(E, static_cast<int>(blockIdx.y + 1) * nwarps * kRouterExp);
+  for (int e0 = static_cast<int>(blockIdx.y) * nwarps * kRouterExp + warp * kRouterExp; e0 < e_end;
+       e0 += nwarps * kRouterExp) {
     float acc[kRouterExp][kRouterTok];
 #pragma unroll
     for (int j = 0; j < kRouterExp; ++j)
@@ -153,7 +171,18 @@ __global__ void residual_add_kernel(float* __restrict__ h, const void* __restric
 cudaError_t launch_rmsnorm(const float* h, int64_t T, int64_t H, float eps, uint16_t* out,
                            cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  rmsnorm_kernel<<<static_cast<unsigned>(T), 256, 0, s>>>(h, H, eps, out);
+  rmsnorm_kernel<false, false><<<static_cast<unsigned>(T), 256, 0, s>>>(
+      const_cast<float*>(h), nullptr, H, eps, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_residual_rmsnorm(float* h, const void* y, int y_f32, int64_t T, int64_t H,
+                                    float eps, uint16_t* out, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  if (y_f32)
+    rmsnorm_kernel<true, true><<<static_cast<unsigned>(T), 256, 0, s>>>(h, y, H, eps, out);
+  else
+    rmsnorm_kernel<true, false><<<static_cast<unsigned>(T), 256, 0, s>>>(h, y, H, eps, out);
   return cudaGetLastError();
 }
 
@@ -168,7 +197,9 @@ cudaError_t launch_router(const uint16_t* xn, const float* wr, int64_t T, int64_
   if (!device_kernel_ready(dev, reinterpret_cast<const void*>(router_kernel),
                            kRouterTok * 7168 * 2, 0))
     return cudaErrorInvalidConfiguration;
-  const unsigned grid = static_cast<unsigned>((T + kRouterTok - 1) / kRouterTok);
+  // blocks split the experts too (32 per block), so that a small T still fills the SMs
+  const dim3 grid(static_cast<unsigned>((T + kRouterTok - 1) / kRouterTok),
+                  static_cast<unsigned>((E + 8 * kRouterExp - 1) / (8 * kRouterExp)));
   router_kernel<<<grid, 256, smem, s>>>(xn, wr, T, H, E, logits);
   return cudaGetLastError();
 }

@@ -404,10 +404,13 @@ fge_status fge_selftest_wait_timeout(void* workspace, int64_t budget_cycles,
  * rmsnorm: out_bf16[t] = h[t] / sqrt(mean(h[t]^2) + eps), h float [T, H].
  * router_logits: logits[t, e] = sum_h xn[t, h] * w[e, h] in fp32 (lane l of a warp sums the
  *   products at h = 256 i + 8 l + c, c < 8, in order, then the warp adds its 32 lane sums);
- *   xn bf16 [T, H], w float [E, H]; H a multiple of 256, at most 7168.
+ *   xn bf16 [T, H], w float [E, H]; H a multiple of 256, at most 7168; E at most 65536.
  * identity_attention: attn[t, h*128 + d] = v[t, (h / (n_heads / n_kv_heads))*128 + d];
  *   v bf16 [T, n_kv_heads*128], attn bf16 [T, n_heads*128].
- * residual_add: h[i] += y[i] for i < n, h float, y in y_dtype. */
+ * residual_add: h[i] += y[i] for i < n, h float, y in y_dtype.
+ * residual_rmsnorm: residual_add over [T, H] followed by rmsnorm of the updated h into
+ *   out_bf16, in one pass per row; the same bits as the two calls in turn.  H % 8 == 0;
+ *   h, y, out 16-byte aligned. */
 fge_status fge_rmsnorm(const float* h, int64_t T, int64_t H, float eps, void* out_bf16,
                        fge_stream_t stream);
 fge_status fge_router_logits(const void* xn_bf16, const float* w_router, int64_t T, int64_t H,
@@ -416,6 +419,8 @@ fge_status fge_identity_attention(const void* v_bf16, int64_t T, int n_heads, in
                                   void* attn_bf16, fge_stream_t stream);
 fge_status fge_residual_add(float* h, const void* y, fge_dtype y_dtype, int64_t n,
                             fge_stream_t stream);
+fge_status fge_residual_rmsnorm(float* h, const void* y, fge_dtype y_dtype, int64_t T,
+                                int64_t H, float eps, void* out_bf16, fge_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -90,6 +90,33 @@ def _model(fge, st):
                               sh["n_heads"], sh["n_kv_heads"], "cuda")
 
 
+@pytest.mark.parametrize("t,h,y_dtype", [(37, 2048, torch.bfloat16), (300, 264, torch.float32),
+                                         (1, 4096, torch.bfloat16)])
+def test_residual_rmsnorm_equals_the_two_calls(fge, t, h, y_dtype):
+    # the fused call gives the same bits as residual_add then rmsnorm, for h and for the norm,
+    # and the norm stays within one bf16 step of the oracle's
+    rng = np.random.default_rng(t + h)
+    h0 = (rng.standard_normal((t, h)) * np.exp(rng.uniform(-3, 3, (t, 1)))).astype(np.float32)
+    y = torch.from_numpy(rng.standard_normal((t, h)).astype(np.float32)).to(y_dtype).to("cuda")
+    h1, h2 = to_dev(h0), to_dev(h0)
+    fge.residual_add(h1, y)
+    xn1 = fge.rmsnorm(h1)
+    xn2 = fge.residual_rmsnorm(h2, y)
+    assert torch.equal(h1, h2)
+    assert torch.equal(xn1.view(torch.int16), xn2.view(torch.int16))
+    ref_h = h0 + y.float().cpu().numpy()
+    assert np.array_equal(host(h2), ref_h)
+    ref = oracle.rmsnorm(ref_h).astype(np.float64)
+    got = host(xn2).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= bf16_ulp(ref) * 1.0001)
+
+
+def test_residual_rmsnorm_refusals(fge):
+    h = torch.zeros((4, 12), dtype=torch.float32, device="cuda")      # H % 8 != 0
+    with pytest.raises(fge.FgeError):
+        fge.residual_rmsnorm(h, torch.zeros_like(h))
+
+
 @pytest.fixture(scope="module")
 def stack12():
     return stacked_inputs(12, seed=1)     # the seed the oracle self-drift study uses
