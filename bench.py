@@ -268,7 +268,7 @@ def run_gpu(args):
         step()
     torch.cuda.synchronize()
     # the layer call is stream-ordered with no host sync and shape-only branches, so it can
-    # be captured once as a CUDA graph and replayed: the 9 kernels launch without host gaps
+    # be captured once as a CUDA graph and replayed: the 8 kernels launch without host gaps
     run_step = step
     if not args.no_graph:
         graph = torch.cuda.CUDAGraph()
@@ -302,7 +302,7 @@ def run_gpu(args):
     status = fge.read_device_status(ws)
     if status != 0:
         raise RuntimeError("device status %d after the timed steps" % status)
-    launches_per_step = 9   # topk, quant, permute x4, gate_up, down, combine
+    launches_per_step = 8   # topk, permute count/scan/rank, quantizing row copy, gate_up, down, combine
     ms = job_step_ms(ms, dev)
     value = job_value(inp.T, world, ms)
 
