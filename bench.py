@@ -213,9 +213,11 @@ def run_reference(args):
 
 
 def _config(inp, note=None):
-    c = {"workload": "%s MoE layer prefill: T=%d tokens, H=%d, E=%d experts, I=%d, top-%d, "
+    routing = (", Zipf(1.1)-skewed routing, 1%% outlier channels x20" if inp.name == "large"
+               else "")
+    c = {"workload": "%s MoE layer prefill: T=%d tokens, H=%d, E=%d experts, I=%d, top-%d%s, "
                      "int4 experts, e4m3 activations"
-                     % (inp.name, inp.T, inp.H, inp.E, inp.I, inp.k),
+                     % (inp.name, inp.T, inp.H, inp.E, inp.I, inp.k, routing),
          "T": inp.T, "H": inp.H, "E": inp.E, "I": inp.I, "k": inp.k,
          "global_batch": inp.T, "seq_len": inp.T, "parallelism": "replicas",
          "l2": "flushed (256 MB write) before every timed step; resident int4 banks + "
