@@ -213,7 +213,7 @@ def run_reference(args):
 
 
 def _config(inp, note=None):
-    routing = (", Zipf(1.1)-skewed routing, 1%% outlier channels x20" if inp.name == "large"
+    routing = (", Zipf(1.1)-skewed routing, 1% outlier channels x20" if inp.name == "large"
                else "")
     c = {"workload": "%s MoE layer prefill: T=%d tokens, H=%d, E=%d experts, I=%d, top-%d%s, "
                      "int4 experts, e4m3 activations"
