@@ -7,6 +7,7 @@
 #include <cuda_fp4.h>
 
 #include "fge_device.cuh"
+#include "quotient.cuh"
 
 namespace fge {
 
@@ -31,13 +32,24 @@ __device__ __forceinline__ void amax_fold8(const uint4& v, float& m, float& bad)
                        bf16_hi(v.w));
 }
 
-// The e4m3 codes of 8 bf16 values divided by s (IEEE division, round to nearest even).
-__device__ __forceinline__ uint2 cast8(const uint4& v, float s) {
+// The e4m3 codes of 8 bf16 values divided by s (the IEEE quotient, then round to nearest
+// even).  y = RN(1/s) and fast = quot_fast_ok(s), both from the caller: the quotient comes
+// from the reciprocal (quotient.cuh) when s is in that method's range, else by division.
+// A NaN value gives a NaN quotient either way.
+__device__ __forceinline__ uint2 cast8(const uint4& v, float s, float y, bool fast) {
+  const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                      bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+  float d[8];
+  if (fast) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d[i] = quot_rn(f[i], s, y);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d[i] = __fdiv_rn(f[i], s);
+  }
   uint2 q;
-  q.x = cvt_e4m3x4(__fdiv_rn(bf16_lo(v.x), s), __fdiv_rn(bf16_hi(v.x), s),
-                   __fdiv_rn(bf16_lo(v.y), s), __fdiv_rn(bf16_hi(v.y), s));
-  q.y = cvt_e4m3x4(__fdiv_rn(bf16_lo(v.z), s), __fdiv_rn(bf16_hi(v.z), s),
-                   __fdiv_rn(bf16_lo(v.w), s), __fdiv_rn(bf16_hi(v.w), s));
+  q.x = cvt_e4m3x4(d[0], d[1], d[2], d[3]);
+  q.y = cvt_e4m3x4(d[4], d[5], d[6], d[7]);
   return q;
 }
 
@@ -77,6 +89,8 @@ __global__ void cast_per_tensor_kernel(const uint4* __restrict__ x, int64_t n8,
                                        uint2* __restrict__ xq, float* __restrict__ xs,
                                        float* __restrict__ scale_out) {
   const float s = scale_from_amax(__uint_as_float(*amax_bits));
+  const float y = __frcp_rn(s);
+  const bool fast = quot_fast_ok(s);
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     xs[0] = s;
     if (scale_out) *scale_out = s;
@@ -93,7 +107,7 @@ __global__ void cast_per_tensor_kernel(const uint4* __restrict__ x, int64_t n8,
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
       const int64_t i = i0 + u * stride;
-      if (i < n8) xq[i] = cast8(v[u], s);
+      if (i < n8) xq[i] = cast8(v[u], s, y, fast);
     }
   }
 }
@@ -123,6 +137,8 @@ __global__ void quant_row_kernel(const uint4* __restrict__ x, int64_t M, int64_t
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
     const float s = scale_from_amax(amax);
+    const float y = __frcp_rn(s);
+    const bool fast = quot_fast_ok(s);
     uint2* qr = xq + r * n8_row;
     for (int64_t i0 = lane; i0 < n8_row; i0 += 32 * kQuantUnroll) {
       uint4 v[kQuantUnroll];
@@ -134,7 +150,7 @@ __global__ void quant_row_kernel(const uint4* __restrict__ x, int64_t M, int64_t
 #pragma unroll
       for (int u = 0; u < kQuantUnroll; ++u) {
         const int64_t i = i0 + 32 * u;
-        if (i < n8_row) qr[i] = cast8(v[u], s);
+        if (i < n8_row) qr[i] = cast8(v[u], s, y, fast);
       }
     }
     if (lane == 0) xs[r] = s;
@@ -238,6 +254,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
   const float sc = scale_from_amax(m);
+  const float y = __frcp_rn(sc);
+  const bool fast = quot_fast_ok(sc);
   if (threadIdx.x == 0) {
     xs[0] = sc;
     if (scale_out) *scale_out = sc;
@@ -245,7 +263,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
 #pragma unroll
   for (int u = 0; u < kSmallPer; ++u) {
     const int64_t i = threadIdx.x + static_cast<int64_t>(u) * kSmallThreads;
-    if (i < n8) xq[i] = cast8(v[u], sc);
+    if (i < n8) xq[i] = cast8(v[u], sc, y, fast);
   }
 }
 

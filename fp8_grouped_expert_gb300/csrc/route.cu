@@ -8,6 +8,7 @@
 #include <cfloat>
 
 #include "fge_device.cuh"
+#include "quotient.cuh"
 
 namespace fge {
 
@@ -347,9 +348,28 @@ __global__ void permute_copy_kernel(const uint8_t* __restrict__ xq, const float*
   }
 }
 
+// The e4m3 codes of a lane's 8 values of one 128-value group, each the code of the IEEE
+// quotient x / sc: from one reciprocal of sc (quotient.cuh) unless sc is out of that
+// method's range or one of the lane's values is not finite (bad != 0), then by division.
+__device__ __forceinline__ uint2 cast8_g(const float (&f)[8], float sc, float bad) {
+  float d[8];
+  if (quot_fast_ok(sc) && bad == 0.0f) {
+    const float y = __frcp_rn(sc);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d[i] = quot_rn(f[i], sc, y);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d[i] = __fdiv_rn(f[i], sc);
+  }
+  uint2 q;
+  q.x = cvt_e4m3x4(d[0], d[1], d[2], d[3]);
+  q.y = cvt_e4m3x4(d[4], d[5], d[6], d[7]);
+  return q;
+}
+
 // (4') quantize and copy in one pass: one warp per token reads its bf16 row once, quantizes
 // each 128-value group exactly as quant_g128_kernel does (16 lanes x 8 values, shuffle amax,
-// s = amax / 448, IEEE division, e4m3 round to nearest even) and writes the codes and the
+// s = amax / 448, the IEEE quotient x / s, e4m3 round to nearest even) and writes the codes and the
 // scale to the token's k expert rows.  Two groups per warp step.
 __global__ void permute_quant_copy_kernel(const uint4* __restrict__ x, int64_t T, int k,
                                           int64_t H, const int32_t* __restrict__ token_row,
@@ -386,11 +406,7 @@ __global__ void permute_quant_copy_kernel(const uint4* __restrict__ x, int64_t T
 #pragma unroll
         for (int d = 8; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
         const float sc = scale_from_amax(amax);
-        uint2 q;
-        q.x = cvt_e4m3x4(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc), __fdiv_rn(f[2], sc),
-                         __fdiv_rn(f[3], sc));
-        q.y = cvt_e4m3x4(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc), __fdiv_rn(f[6], sc),
-                         __fdiv_rn(f[7], sc));
+        const uint2 q = cast8_g(f, sc, bad);
         for (int j = 0; j < k; ++j) {
           const int64_t r = __shfl_sync(0xffffffffu, my_row, j);
           if (in) {
@@ -567,12 +583,7 @@ __global__ void __launch_bounds__(256, 5)
       for (int d = 8; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
       const float sc = scale_from_amax(amax);
       if (g < ngroups) {
-        uint2 q;
-        q.x = cvt_e4m3x4(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc), __fdiv_rn(f[2], sc),
-                         __fdiv_rn(f[3], sc));
-        q.y = cvt_e4m3x4(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc), __fdiv_rn(f[6], sc),
-                         __fdiv_rn(f[7], sc));
-        __stcs(xq + g * 16 + hl, q);
+        __stcs(xq + g * 16 + hl, cast8_g(f, sc, bad));
         if (hl == 0) xs[g] = sc;
       }
     }
