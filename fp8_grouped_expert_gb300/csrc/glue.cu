@@ -59,10 +59,11 @@ __global__ void rmsnorm_kernel(float* __restrict__ h, const void* __restrict__ y
 }
 
 // Router logits, logits[t, e] = sum_k xn[t, k] * wr[e, k] in fp32.  One block per kRouterTok
-// tokens and 32 experts: the tokens' bf16 rows stay in shared memory.  Each warp takes kRouterExp experts at a
-// time; lane l accumulates the products at k = 8 l + 256 i for every token of the block and
-// each of those experts, so a row chunk read from shared memory serves kRouterExp experts and
-// a router chunk read from L2 serves every token.  The warp then adds its lanes' sums.
+// tokens and 32 experts: the tokens' bf16 rows stay in shared memory.  Each warp takes
+// kRouterExp experts at a time; lane l accumulates the products at k = 8 l + 256 i for every
+// token of the block and each of those experts, so a row chunk read from shared memory serves
+// kRouterExp experts and a router chunk read from L2 serves every token.  The warp then adds
+// its lanes' sums.
 constexpr int kRouterTok = 16, kRouterExp = 4;
 
 __global__ void __launch_bounds__(256)
@@ -92,8 +93,8 @@ __global__ void __launch_bounds__(256)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
   const int e_end = min(E, static_cast<int>(blockIdx.y + 1) * nwarps * kRouterExp);
-  for (int e0 = static_cast<int>(blockIdx.y) * nwarps * kRouterExp + warp * kRouterExp; e0 < e_end;
-       e0 += nwarps * kRouterExp) {
+  for (int e0 = static_cast<int>(blockIdx.y) * nwarps * kRouterExp + warp * kRouterExp;
+       e0 < e_end; e0 += nwarps * kRouterExp) {
     float acc[kRouterExp][kRouterTok];
 #pragma unroll
     for (int j = 0; j < kRouterExp; ++j)
