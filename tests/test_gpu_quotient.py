@@ -107,3 +107,39 @@ def test_per_tensor_codes_on_hard_quotients(fge):
         q_ref, s_ref = oracle.quant_act_per_tensor(row[None, :])
         assert float(xs.cpu().numpy()[0]) == float(s_ref)
         assert np.array_equal(xq.cpu().numpy(), q_ref)
+
+
+def _tiny_rows(seed):
+    """Groups whose scale falls on either side of 2^-90 (below it the quantizers divide, above
+    it they use the reciprocal and the correction), holding subnormal bfloat16 values, signed
+    zeros and values across the group's whole range."""
+    rng = np.random.default_rng(seed)
+    groups = []
+    for e_amax in (-120, -100, -82, -81, -80, -60, -20, 0, 20, 100, 127):
+        g = rng.uniform(-1.0, 1.0, 128).astype(np.float32) * np.float32(2.0 ** e_amax)
+        g[0] = np.float32(2.0 ** e_amax) * np.float32(1.5)            # the group's amax
+        g[1:9] = np.float32(2.0 ** -133) * np.arange(1, 9)            # bf16 subnormals
+        g[9], g[10] = np.float32(0.0), np.float32(-0.0)
+        g[11:20] *= -1
+        groups.append(torch.from_numpy(g).to(torch.bfloat16).float().numpy())
+    while len(groups) % 4:
+        groups.append(np.zeros(128, np.float32))
+    return np.stack(groups).reshape(-1, 512)
+
+
+def test_quantizers_across_the_reciprocal_range(fge):
+    rows = _tiny_rows(11)
+    xq, xs = fge.fp8_quant_act(_bf16(rows), "g128")
+    q_ref, s_ref = oracle.quant_act_g128(rows)
+    assert np.array_equal(xs.cpu().numpy(), s_ref)
+    assert np.array_equal(xq.cpu().numpy(), q_ref)
+    r1 = rows.reshape(-1, 128)
+    xq, xs = fge.fp8_quant_act(_bf16(r1), "row")
+    q_ref, s_ref = oracle.quant_act_per_row(r1)
+    assert np.array_equal(xs.cpu().numpy(), s_ref)
+    assert np.array_equal(xq.cpu().numpy(), q_ref)
+    for g in r1:                                      # each group as its own tensor
+        xq, xs = fge.fp8_quant_act(_bf16(g[None, :]), "tensor")
+        q_ref, s_ref = oracle.quant_act_per_tensor(g[None, :])
+        assert float(xs.cpu().numpy()[0]) == float(s_ref)
+        assert np.array_equal(xq.cpu().numpy(), q_ref)
