@@ -131,7 +131,9 @@ fge_status fge_read_device_status(const void* workspace, fge_stream_t stream, in
  * fp8_ffi" (amax reduce, scale finalize, e4m3 quantize, one stream, no host sync):
  *   amax = max|x| over the group (G128) or the whole tensor (PER_TENSOR);
  *   s = amax / 448 (IEEE float division; s = 1 when amax = 0; s >= 2^-126);
- *   q = e4m3(x / s), round to nearest even, saturating at +-448.
+ *   q = e4m3(x / s), round to nearest even, saturating at +-448, where x / s is the IEEE
+ *   float32 quotient (formed from one rounded reciprocal of s and an exact-residual
+ *   correction, which equals the division for every bf16 x).
  * PER_ROW takes the amax over each row's K elements (the row-wise activation scales that
  * "feat(qwen4_exp) ..." measures against per-tensor, section "Limits").
  * x_bf16: [M, K] bf16.  xq: [M, K] e4m3 codes (out).  xs: [M, K/128] float (G128), [M] float
