@@ -575,6 +575,7 @@ def stage_times(fge, torch, inp, x, logits, w_gu, s_gu, w_dn, s_dn, fmt, flush, 
     hq = torch.empty((r, inp.I), dtype=torch.uint8, device=dev)
     hs = torch.empty((r, inp.I // 128), dtype=torch.float32, device=dev)
     y = torch.empty((r, inp.H), dtype=torch.bfloat16, device=dev)
+    cws = ws if (inp.H % 2048 == 0 and inp.k <= 8) else None
     for _ in range(steps + 1):
         ids, gates = timed("topk_gate", lambda: fge.moe_topk_gate(logits, inp.k))
         xq, xs = timed("quant_g128", lambda: fge.fp8_quant_act(x, "g128"))
@@ -586,7 +587,8 @@ def stage_times(fge, torch, inp, x, logits, w_gu, s_gu, w_dn, s_dn, fmt, flush, 
         timed("down_gemm", lambda: fge.grouped_gemm_w4a8(
             hq, hs, p["offsets"], w_dn, s_dn, fmt=fmt, out_dtype=torch.bfloat16, workspace=ws,
             out=y))
-        timed("combine", lambda: fge.moe_combine(y, p["token_row"], gates))
+        # the layer's own combine (slot rows staged by bulk copies) where it applies
+        timed("combine", lambda: fge.moe_combine(y, p["token_row"], gates, workspace=cws))
     torch.cuda.synchronize()
     # the first pass includes allocator warm-up; drop it
     return {k: sum(a.elapsed_time(b) for a, b in v[1:]) / (len(v) - 1) for k, v in acc.items()}

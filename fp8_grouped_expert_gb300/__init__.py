@@ -55,6 +55,7 @@ SIGNATURES = {
                                      _I, _I, _P, _P, _P, _SZ, _P],
     "fge_swiglu_quant": [_P, _I64, _I64, _P, _P, _P],
     "fge_moe_combine": [_P, _I, _P, _P, _I64, _I, _I64, _I, _P, _P],
+    "fge_moe_combine_staged": [_P, _P, _P, _I64, _I, _I64, _I, _P, _P, _SZ, _P],
     "fge_gemm_w8a8": [_P, _P, _I64, _I64, _P, _P, _I64, _I, _P, _P, _SZ, _P],
     "fge_linear_w8a8": [_P, _I64, _I64, _P, _P, _I64, _P, _P, _SZ, _P],
     "fge_gemm_w8a8_rows": [_P, _P, _I64, _I64, _P, _P, _I64, _I, _P, _P, _SZ, _P],
@@ -405,13 +406,22 @@ def swiglu_quant(c, inter):
     return hq, hs
 
 
-def moe_combine(y, token_row, gates, out_dtype=torch.bfloat16):
+def moe_combine(y, token_row, gates, out_dtype=torch.bfloat16, workspace=None):
+    """out[t] = sum_j gates[t, j] * y[token_row[t, j]].  With a workspace (>= 256 bytes),
+    bf16 y, k <= 8 and H % 2048 == 0: fge_moe_combine_staged, the layer's own combine."""
     _need(token_row, torch.int32, "token_row")
     _need(gates, torch.float32, "gates")
     _ensure_init(y.device)
     t, k = token_row.shape
     h = y.shape[1]
     out = torch.empty((t, h), dtype=out_dtype, device=y.device)
+    if workspace is not None:
+        _need(y, torch.bfloat16, "y")
+        _check(lib().fge_moe_combine_staged(
+            _ptr(y), _ptr(token_row), _ptr(gates), t, k, h,
+            DTYPE_F32 if out_dtype == torch.float32 else DTYPE_BF16, _ptr(out), _ptr(workspace),
+            workspace.numel(), _stream(y)), "fge_moe_combine_staged")
+        return out
     _check(lib().fge_moe_combine(_ptr(y), DTYPE_F32 if y.dtype == torch.float32 else DTYPE_BF16,
                                  _ptr(token_row), _ptr(gates), t, k, h,
                                  DTYPE_F32 if out_dtype == torch.float32 else DTYPE_BF16,

@@ -481,6 +481,21 @@ fge_status fge_moe_combine(const void* y, fge_dtype y_dtype, const int32_t* toke
                                   out_dtype == FGE_DTYPE_F32, out, stream));
 }
 
+fge_status fge_moe_combine_staged(const void* y_bf16, const int32_t* token_row,
+                                  const float* gates, int64_t T, int k, int64_t H,
+                                  fge_dtype out_dtype, void* out, void* ws, size_t ws_bytes,
+                                  fge_stream_t stream) {
+  FGE_CHECK(cur_device_ok());
+  FGE_REQUIRE(y_bf16 && token_row && gates && out && ws, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(out_dtype == FGE_DTYPE_BF16 || out_dtype == FGE_DTYPE_F32, FGE_ERR_INVALID_ARG);
+  FGE_REQUIRE(T >= 0 && k >= 1 && k <= 8 && H > 0 && H % 2048 == 0, FGE_ERR_BAD_SHAPE);
+  FGE_REQUIRE(al16(y_bf16) && al16(out) && al16(ws), FGE_ERR_MISALIGNED);
+  FGE_REQUIRE(ws_bytes >= sizeof(WsHeader), FGE_ERR_WORKSPACE_TOO_SMALL);
+  return from_cuda(launch_combine(y_bf16, 0, token_row, gates, T, k, H,
+                                  out_dtype == FGE_DTYPE_F32, out, stream,
+                                  &static_cast<WsHeader*>(ws)->status));
+}
+
 fge_status fge_gemm_w8a8(const uint8_t* aq, const float* sa, int64_t M, int64_t K,
                          const uint8_t* wq, const float* sw, int64_t N, fge_dtype out_dtype,
                          void* y, void* ws, size_t ws_bytes, fge_stream_t stream) {
@@ -647,7 +662,7 @@ static fge_status layer_forward(const float* logits, const void* x, int64_t T, i
   }
   NvtxRange r("fge.combine");
   const fge_status st = from_cuda(launch_combine(w.y, out_f32, w.token_row, w.gates, T, k, H,
-                                                 out_f32, out, stream));
+                                                 out_f32, out, stream, &w.hdr->status));
   if (st == FGE_OK) ledger_note(kLedLayers);
   return st;
 }

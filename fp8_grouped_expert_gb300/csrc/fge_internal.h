@@ -55,9 +55,11 @@ cudaError_t launch_permute_quant(const int32_t* ids, int64_t T, int k, int E,
                                  const uint16_t* x, int64_t H, int32_t* offsets,
                                  int32_t* row_token, int32_t* token_row, uint8_t* aq, float* as,
                                  void* scratch, int32_t* status, cudaStream_t s);
+// status (may be null): with a status word, the bf16 case with k <= 8 and H % 2048 == 0
+// runs the bulk-copy combine, whose bounded waits report there; otherwise the plain kernel.
 cudaError_t launch_combine(const void* y, int y_f32, const int32_t* token_row,
                            const float* gates, int64_t T, int k, int64_t H, int out_f32,
-                           void* out, cudaStream_t s);
+                           void* out, cudaStream_t s, int32_t* status = nullptr);
 cudaError_t launch_swiglu_quant(const float* c, int64_t R, int64_t I, uint8_t* hq, float* hs,
                                 cudaStream_t s);
 cudaError_t launch_w4_prepack(const uint8_t* w, const float* sw, int E, int64_t N, int64_t K,

@@ -517,6 +517,99 @@ __global__ void combine_kernel(const void* __restrict__ y, const int32_t* __rest
   }
 }
 
+// The layer's combine (bf16 y, k <= 8, H a multiple of 2048) through bulk copies.  An item
+// is (token t, 2048-column block); its k slot rows' blocks of y are 4 KB each and
+// contiguous, so a producer warp copies them into a shared-memory stage with k
+// cp.async.bulk copies counted on the stage's mbarrier, and eight consumer warps sum them in
+// slot order with the same fmaf chain as combine_kernel (thread i owns columns 8 i .. 8 i + 7
+// of the block), so the results are the same bits.  Three stages keep three items' 96 KB in
+// flight per CTA, two CTAs per SM, without holding the rows in registers.  Every wait is
+// bounded: one that runs out records FGE_ERR_DEVICE_TIMEOUT in *status and the CTA stops.
+constexpr int kCombCols = 2048, kCombStages = 3, kCombMaxK = 8;
+constexpr int kCombStageBytes = kCombMaxK * kCombCols * 2;
+constexpr int kCombSmem = kCombStages * kCombStageBytes + 2 * kCombStages * 8;
+
+__device__ __forceinline__ void comb_bulk_load(uint32_t smem_dst, const void* src, uint32_t bytes,
+                                               uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+template <bool OF32>
+__global__ void __launch_bounds__(288)
+    combine_bulk_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ token_row,
+                        const float* __restrict__ gates, int64_t T, int k, int64_t H,
+                        void* __restrict__ out, int32_t* status) {
+  extern __shared__ __align__(128) uint8_t csm[];
+  __shared__ int s_abort;
+  const uint32_t stage0 = smem_u32(csm);
+  const uint32_t full0 = stage0 + kCombStages * kCombStageBytes;
+  const uint32_t empty0 = full0 + 8 * kCombStages;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kCombStages; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, 8);
+    }
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int64_t nb = H / kCombCols;
+  const int64_t items = T * nb;
+  uint32_t it = 0;
+  if (warp == 8) {
+    // producer: lane j < k copies slot row j's block of the item
+    for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+      const uint32_t st = it % kCombStages;
+      if (!mbar_wait(empty0 + 8 * st, ((it / kCombStages) & 1) ^ 1, &s_abort, status)) break;
+      const int64_t t = item / nb;
+      const int64_t c0 = (item - t * nb) * kCombCols;
+      if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, static_cast<uint32_t>(k) * kCombCols * 2);
+      __syncwarp();
+      if (lane < k) {
+        const int64_t r = __ldg(token_row + t * k + lane);
+        comb_bulk_load(stage0 + st * kCombStageBytes + lane * (kCombCols * 2), y + r * H + c0,
+                       kCombCols * 2, full0 + 8 * st);
+      }
+    }
+  } else {
+    for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+      const uint32_t st = it % kCombStages;
+      const int64_t t = item / nb;
+      const int64_t c0 = (item - t * nb) * kCombCols;
+      const float my_gate = lane < k ? __ldg(gates + t * k + lane) : 0.0f;
+      if (!mbar_wait(full0 + 8 * st, (it / kCombStages) & 1, &s_abort, status)) break;
+      const uint8_t* src = csm + st * kCombStageBytes + threadIdx.x * 16;
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        const float g = __shfl_sync(0xffffffffu, my_gate, j);
+        const uint4 a = *reinterpret_cast<const uint4*>(src + j * (kCombCols * 2));
+        const float v[8] = {bf16_lo(a.x), bf16_hi(a.x), bf16_lo(a.y), bf16_hi(a.y),
+                            bf16_lo(a.z), bf16_hi(a.z), bf16_lo(a.w), bf16_hi(a.w)};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, v[i], acc[i]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * st);
+      const int64_t col = c0 + threadIdx.x * 8;
+      if constexpr (OF32) {
+        float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + t * H + col);
+        o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      } else {
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + t * H + col) =
+            make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                       pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+      }
+    }
+  }
+}
+
 // Arrival counters of the combine folded into the down GEMM set to zero, and the combine's
 // arguments written where the GEMM reads them.
 __global__ void combine_setup_kernel(FusedCombine c, int64_t n, FusedCombine* dst) {
@@ -535,8 +628,27 @@ cudaError_t launch_combine_setup(const FusedCombine& c, int64_t n, FusedCombine*
 
 cudaError_t launch_combine(const void* y, int y_f32, const int32_t* token_row,
                            const float* gates, int64_t T, int k, int64_t H, int out_f32,
-                           void* out, cudaStream_t s) {
+                           void* out, cudaStream_t s, int32_t* status) {
   if (T == 0) return cudaSuccess;
+  if (status && !y_f32 && k <= kCombMaxK && H % kCombCols == 0) {
+    int dev = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) return ce;
+    const void* kern = out_f32 ? reinterpret_cast<const void*>(combine_bulk_kernel<true>)
+                               : reinterpret_cast<const void*>(combine_bulk_kernel<false>);
+    if (device_kernel_ready(dev, kern, kCombSmem, 0)) {
+      const int64_t items = T * (H / kCombCols);
+      const int grid = static_cast<int>(std::min<int64_t>(items, 2LL * num_sms()));
+      const uint16_t* yb = static_cast<const uint16_t*>(y);
+      if (out_f32)
+        combine_bulk_kernel<true><<<grid, 288, kCombSmem, s>>>(yb, token_row, gates, T, k, H,
+                                                               out, status);
+      else
+        combine_bulk_kernel<false><<<grid, 288, kCombSmem, s>>>(yb, token_row, gates, T, k, H,
+                                                                out, status);
+      return cudaGetLastError();
+    }
+  }
   const int64_t items = T * ((H + 2047) / 2048);
   const int grid = static_cast<int>(std::min<int64_t>((items + 7) / 8, num_sms() * 8));
   if (y_f32 && out_f32) combine_kernel<true, true><<<grid, 256, 0, s>>>(y, token_row, gates, T, k, H, out);

@@ -273,6 +273,18 @@ fge_status fge_moe_combine(const void* y, fge_dtype y_dtype, const int32_t* toke
                            const float* gates, int64_t T, int k, int64_t H,
                            fge_dtype out_dtype, void* out, fge_stream_t stream);
 
+/* moe_combine_staged -- the same sums, bit for bit, as the MoE layer computes them for a
+ * bf16 y: each (token, 2048-column block) gathers its k slot rows' blocks into shared memory
+ * with bulk copies (no per-thread loads in flight), then sums them in slot order.
+ * y_bf16: [T*k, H] bf16, k <= 8, H % 2048 == 0; token_row, gates, out as moe_combine.
+ * workspace: at least 256 bytes (its status word receives FGE_ERR_DEVICE_TIMEOUT if a
+ * copy never lands; read with fge_read_device_status).  Errors: FGE_ERR_BAD_SHAPE outside
+ * those sizes, FGE_ERR_MISALIGNED, FGE_ERR_WORKSPACE_TOO_SMALL. */
+fge_status fge_moe_combine_staged(const void* y_bf16, const int32_t* token_row,
+                                  const float* gates, int64_t T, int k, int64_t H,
+                                  fge_dtype out_dtype, void* out, void* workspace,
+                                  size_t workspace_bytes, fge_stream_t stream);
+
 /* gemm_w8a8 -- dense per-tensor W8A8 GEMM, the grouped kernel run with one expert
  * ("feat(qwen4_exp) ..." section "What this adds"; "Module fp8_ffi": activation scale
  * folded with the weight scale into one device scalar):  y = (sa * sw) * aq @ wq^T.

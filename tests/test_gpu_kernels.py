@@ -114,6 +114,47 @@ def test_combine(fge, y_dtype, out_dtype):
         assert np.all(np.abs(got - ref) <= bf16_ulp(ref) + 1e-6 * absref)
 
 
+@pytest.mark.parametrize("t,e,k,h,out_dtype", [(333, 64, 8, 2048, torch.bfloat16),
+                                               (97, 16, 1, 4096, torch.bfloat16),
+                                               (1000, 32, 3, 2048, torch.float32),
+                                               (1, 8, 8, 6144, torch.bfloat16)])
+def test_combine_staged_equals_plain(fge, t, e, k, h, out_dtype):
+    # the layer's combine (slot rows staged in shared memory by bulk copies) gives the plain
+    # kernel's bits, and meets the oracle's rule
+    rng = np.random.default_rng(t + h)
+    ids, gates = oracle.topk_gate(rng.standard_normal((t, e)).astype(np.float32), k)
+    p = oracle.moe_permute(ids, e, np.zeros((t, 128), np.uint8), np.zeros((t, 1), np.float32))
+    y = to_bf16(rng.standard_normal((t * k, h)).astype(np.float32))[1]
+    yd, tr, gd = to_dev(y).to(torch.bfloat16), to_dev(p["token_row"]), to_dev(gates)
+    ws = fge.new_workspace(256, yd.device)
+    fge.clear_device_status(ws)
+    staged = fge.moe_combine(yd, tr, gd, out_dtype=out_dtype, workspace=ws)
+    plain = fge.moe_combine(yd, tr, gd, out_dtype=out_dtype)
+    assert fge.read_device_status(ws) == 0
+    assert torch.equal(staged, plain)
+    ref = oracle.moe_combine(y, p["token_row"], gates)
+    absref = oracle.moe_combine(np.abs(y), p["token_row"], gates)
+    got = host(staged).astype(np.float64)
+    ulp = bf16_ulp(ref) if out_dtype == torch.bfloat16 else 1e-6 * np.abs(ref)
+    assert np.all(np.abs(got - ref) <= ulp + 1e-6 * absref)
+
+
+def test_combine_staged_refusals(fge):
+    t, k, h = 16, 2, 2048
+    y = torch.zeros((t * k, h), dtype=torch.bfloat16, device="cuda")
+    tr = torch.zeros((t, k), dtype=torch.int32, device="cuda")
+    g = torch.zeros((t, k), dtype=torch.float32, device="cuda")
+    ws = fge.new_workspace(256, y.device)
+    with pytest.raises(fge.FgeError):           # H not a multiple of 2048
+        fge.moe_combine(y[:, :1024].contiguous(), tr, g, workspace=ws)
+    big = torch.zeros((t, 9), dtype=torch.int32, device="cuda")
+    with pytest.raises(fge.FgeError):           # k > 8
+        fge.moe_combine(torch.zeros((t * 9, h), dtype=torch.bfloat16, device="cuda"), big,
+                        torch.zeros((t, 9), dtype=torch.float32, device="cuda"), workspace=ws)
+    with pytest.raises(fge.FgeError):           # the workspace holds no status header
+        fge.moe_combine(y, tr, g, workspace=fge.new_workspace(256, y.device)[:128])
+
+
 def test_swiglu_quant_unfused(fge):
     rng = np.random.default_rng(6)
     r, inter = 500, 768

@@ -91,3 +91,24 @@ def test_host_pipeline_matches_layer_calls(fge):
         pipe.finish()
         for i in range(3):
             np.testing.assert_array_equal(outs[i].float().numpy(), refs[i])
+
+
+@pytest.mark.parametrize("name,t", [("mid", 4096), ("large", 1536)])
+def test_layer_equals_its_stage_calls(fge, name, t):
+    """The layer call (whose combine at H % 2048 == 0 runs on bulk copies into shared memory)
+    equals the same stages called one by one through the C ABI, ending with the plain
+    combine kernel of fge_moe_combine, bit for bit."""
+    inp = moe_inputs(name, seed=3, T=t)
+    w_gu, s_gu = fge.w4_prepack(to_dev(inp.w_gu), to_dev(inp.s_gu), gate_up_interleave=True)
+    w_dn, s_dn = fge.w4_prepack(to_dev(inp.w_dn), to_dev(inp.s_dn))
+    lg, x = to_dev(inp.logits), bf16_dev(inp.x_bits)
+    layer = host(fge.moe_layer_forward(lg, x, inp.k, inp.I, w_gu, s_gu, w_dn, s_dn))
+    ids, gates = fge.moe_topk_gate(lg, inp.k)
+    p = fge.moe_permute_quant(ids, inp.E, x)
+    hq, hs = fge.grouped_gemm_w4a8(p["aq"], p["as_"], p["offsets"], w_gu, s_gu,
+                                   epilogue="swiglu")
+    y = fge.grouped_gemm_w4a8(hq, hs, p["offsets"], w_dn, s_dn, out_dtype=torch.bfloat16)
+    staged = host(fge.moe_combine(y, p["token_row"], gates))
+    torch.cuda.synchronize()
+    assert np.all(np.isfinite(layer))
+    np.testing.assert_array_equal(layer, staged)
