@@ -534,7 +534,7 @@ class HostLayerPipeline:
 
     submit() enqueues one step and returns at once; finish() waits for every step.  With
     graphs=True (the default) the layer call of each slot is captured once as a CUDA graph
-    and replayed, so its 9 kernels launch without host gaps."""
+    and replayed, so its 8 kernels launch without host gaps."""
 
     def __init__(self, tokens, hidden, experts, k, inter, w_gu_dev, s_gu_dev, w_dn_dev,
                  s_dn_dev, fmt=W4_SUBNORMAL, out_dtype=torch.bfloat16, device=None,
