@@ -253,7 +253,7 @@ __global__ void permute_scan_kernel(int32_t* __restrict__ chunk_counts, int64_t 
 // each warp walks its slice in (token, slot) order.  Lanes hold consecutive entries; a
 // token's k experts are distinct, so lanes sharing an expert belong to different tokens and
 // their lane order is the token order.  The result equals a serial walk of the chunk.
-constexpr int kRankWarps = 4;
+constexpr int kRankWarps = 8;
 
 __global__ void permute_rank_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int E,
                                     const int32_t* __restrict__ chunk_base,
