@@ -15,7 +15,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfge.so")
-SOURCES = ["api.cu", "quant.cu", "route.cu", "gemm.cu", "glue.cu", "noalloc.cu", "selftest.cu", "dispatch.cu"]
+SOURCES = ["api.cu", "quant.cu", "route.cu", "gemm.cu", "glue.cu", "noalloc.cu", "selftest.cu", "dispatch.cu",
+           "decode.cu"]
 HEADERS = ["fge_device.cuh", "fge_internal.h", os.path.join("..", "..", "include", "fge.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

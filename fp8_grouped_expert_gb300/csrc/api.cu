@@ -365,7 +365,7 @@ static fge_status grouped_common(const uint8_t* aq, const float* as, const int32
   a.status = &static_cast<WsHeader*>(ws)->status;
   a.comb = comb;
   fge_status st = FGE_OK;
-  const cudaError_t e = launch_grouped_gemm(a, stream, &st);
+  const cudaError_t e = launch_one_group_gemm(a, stream, &st);
   if (e != cudaSuccess) return FGE_ERR_CUDA;
   return st;
 }
@@ -428,7 +428,7 @@ fge_status fge_grouped_gemm_mxf4_w4(const uint8_t* a_codes, const uint8_t* a_sca
   a.out = out;
   a.status = &static_cast<WsHeader*>(ws)->status;
   fge_status st = FGE_OK;
-  if (launch_grouped_gemm(a, static_cast<cudaStream_t>(stream), &st) != cudaSuccess)
+  if (launch_one_group_gemm(a, static_cast<cudaStream_t>(stream), &st) != cudaSuccess)
     return FGE_ERR_CUDA;
   return st;
 }
@@ -535,7 +535,7 @@ static fge_status dense_gemm(const uint8_t* xq, int64_t M, const uint8_t* wq,
   a.partials = partials;
   a.split_count = counters;
   fge_status st = FGE_OK;
-  if (launch_grouped_gemm(a, static_cast<cudaStream_t>(stream), &st) != cudaSuccess)
+  if (launch_one_group_gemm(a, static_cast<cudaStream_t>(stream), &st) != cudaSuccess)
     return FGE_ERR_CUDA;
   return st;
 }

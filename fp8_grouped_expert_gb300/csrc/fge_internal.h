@@ -119,6 +119,11 @@ size_t dense_split_bytes(int64_t M, int64_t N, int ksplit, size_t* counter_bytes
 cudaError_t launch_combine_setup(const FusedCombine& c, int64_t n, FusedCombine* dst,
                                  cudaStream_t s);
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st);
+// launch_grouped_gemm, except that a one-group (dense W8A8) GEMM of at most 16 rows with
+// N % 16 == 0, K % 64 == 0 and K <= 2560 runs the decode kernel of decode.cu instead
+// (weights streamed once by bulk copies, warp-level MMAs; a programmatic dependent launch),
+// which needs no K-split scratch.
+cudaError_t launch_one_group_gemm(const GroupedGemmArgs& a, cudaStream_t s, fge_status* st);
 
 cudaError_t launch_rmsnorm(const float* h, int64_t T, int64_t H, float eps, uint16_t* out,
                            cudaStream_t s);

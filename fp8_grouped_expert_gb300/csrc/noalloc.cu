@@ -118,7 +118,7 @@ fge_status noalloc_run(const void* x, int64_t M, int64_t K, const uint8_t* wq,
   a.partials = partials;
   a.split_count = counters;
   fge_status gst = FGE_OK;
-  if (launch_grouped_gemm(a, stream, &gst) != cudaSuccess) return FGE_ERR_CUDA;
+  if (launch_one_group_gemm(a, stream, &gst) != cudaSuccess) return FGE_ERR_CUDA;
   return gst;
 }
 

@@ -117,6 +117,8 @@ __global__ void cast_per_tensor_kernel(const uint4* __restrict__ x, int64_t n8,
 __global__ void quant_row_kernel(const uint4* __restrict__ x, int64_t M, int64_t n8_row,
                                  uint2* __restrict__ xq, float* __restrict__ xs,
                                  int32_t* status) {
+  // a decode-size projection's GEMM may launch now (see quant_tensor_small_kernel)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -235,6 +237,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     quant_tensor_small_kernel(const uint4* __restrict__ x, int64_t n8, uint2* __restrict__ xq,
                               float* __restrict__ xs, float* __restrict__ scale_out,
                               int32_t* status, int32_t* zero, int n_zero) {
+  // a decode-size projection's GEMM may launch now and start streaming its weights; it
+  // waits for this kernel's results before reading them
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int i = threadIdx.x; i < n_zero; i += kSmallThreads) zero[i] = 0;
   uint4 v[kSmallPer];
   float m = 0.0f, bad = 0.0f;

@@ -107,7 +107,8 @@ size_t fge_workspace_bytes(fge_op op, int64_t a, int64_t b, int64_t c, int E, in
  *                      shape, alignment, workspace size, device not initialised, ...);
  *   layers             fge_moe_layer_forward calls that enqueued their kernels;
  *   grouped_gemms      grouped W4A8 GEMM launches (stand-alone or inside a layer);
- *   dense_decode_tile  dense W8A8 GEMMs run with the 16-token decode tile (M <= 16);
+ *   dense_decode_tile  dense W8A8 projections run at decode sizes (M <= 16: the weight-
+ *                      streaming decode kernel; otherwise the 16-token decode tile);
  *   dense_row_tile     dense W8A8 GEMMs run with 128-row tiles. */
 typedef struct {
   uint64_t calls;
@@ -290,9 +291,12 @@ fge_status fge_moe_combine_staged(const void* y_bf16, const int32_t* token_row,
  * folded with the weight scale into one device scalar):  y = (sa * sw) * aq @ wq^T.
  * aq: [M, K] e4m3; sa, sw: device float scalars; wq: [N, K] e4m3; y: [M, N] in out_dtype.
  * At decode sizes (M <= 16; also in fge_gemm_w8a8_rows, fge_linear_w8a8* and the
- * allocation-free call) the kernel swaps its operands: the weights fill the 128-row side of
- * the MMA and the activations one 16-row tile, and y is written transposed back to [M, N];
- * the arithmetic and the result are the same.
+ * allocation-free call) with K <= 2560, a weight-streaming kernel runs instead: each block
+ * copies 16 weight rows into shared memory with bulk copies and eight warps split K with
+ * warp-level e4m3 MMAs, the partial sums added in warp order (deterministic); it is launched
+ * as a programmatic dependent of the kernel before it, so its weight stream overlaps that
+ * kernel's end.  With a larger K the grouped kernel swaps its operands: the weights fill the
+ * 128-row side of the MMA and the activations one 16-row tile, y written transposed back.
  * Workspace: FGE_OP_GROUPED_GEMM. */
 fge_status fge_gemm_w8a8(const uint8_t* aq, const float* sa, int64_t M, int64_t K,
                          const uint8_t* wq, const float* sw, int64_t N, fge_dtype out_dtype,
@@ -303,7 +307,8 @@ fge_status fge_gemm_w8a8(const uint8_t* aq, const float* sa, int64_t M, int64_t 
  * call does it: per-tensor amax, scale, e4m3 cast, then the W8A8 GEMM, one stream, no host
  * sync.  x_bf16: [M, K]; wq: [N, K] e4m3 with device scalar w_scale; y_bf16: [M, N].
  * Workspace: FGE_OP_LINEAR_W8A8 (holds the quantized activation and the scale block).  At
- * decode sizes (M <= 16) the GEMM splits K over several CTAs per 128-feature tile (as many as
+ * decode sizes (M <= 16) the GEMM is the decode kernel described at fge_gemm_w8a8 when
+ * K <= 2560; with a larger K it splits K over several CTAs per 128-feature tile (as many as
  * fill the SMs in one wave, each at least two 128-wide K groups); the last of them to finish
  * adds the fp32 partials in split order, so the result does not depend on timing.  That needs
  * scratch for the partials: size the workspace with N

@@ -31,14 +31,16 @@ def test_dense_full_size(fge, m):
     check_gemm(y[rows], ref, absref, True)
 
 
-@pytest.mark.parametrize("m", [1, 5, 16])
-def test_decode_split_k_exact_and_repeatable(fge, m):
-    # Decode sizes split K over several CTAs per 128-feature tile and add the fp32 partials
-    # in split order.  Integer activations and weights with power-of-two scales keep every
-    # partial and every sum exact, so the result must equal the oracle bit for bit, and five
-    # calls must agree bit for bit.
-    rng = np.random.default_rng(70 + m)
-    n, k = 6656, 2560
+@pytest.mark.parametrize("m,k", [(1, 2560), (5, 2560), (16, 2560), (9, 1408), (3, 4096),
+                                 (16, 4096)])
+def test_decode_sizes_exact_and_repeatable(fge, m, k):
+    # Decode sizes: up to K = 2560 the weight-streaming decode kernel (warp MMAs, eight warps
+    # splitting K, partials added in warp order), beyond it the grouped kernel's 16-token
+    # tile with K split over several CTAs per 128-feature tile.  Integer activations and
+    # weights with power-of-two scales keep every partial and every sum exact, so the result
+    # must equal the oracle bit for bit, and five calls must agree bit for bit.
+    rng = np.random.default_rng(70 + m + k)
+    n = 6656
     x = rng.integers(-8, 9, (m, k)).astype(np.float32)
     x[0, 0] = 448.0                                   # amax 448: activation scale exactly 1
     w = rng.integers(-8, 9, (n, k)).astype(np.float32)
