@@ -227,47 +227,72 @@ cudaError_t launch_quant_rows(const uint16_t* x, int64_t M, int64_t K, uint8_t* 
   return cudaGetLastError();
 }
 
-// Per-tensor quantization of a small tensor (decode sizes) in one CTA: each thread holds its
-// kSmallPer 16-byte chunks in registers, the block reduces the amax, and the same registers
-// are cast -- one launch, one read, no atomics.  The amax and the codes are those of the
-// two-pass kernels (a max does not depend on the order of its operands).
-constexpr int kSmallThreads = 1024, kSmallPer = 8;
+// Per-tensor quantization of a small tensor (decode sizes) in one launch: a cluster of
+// kSmallCtas CTAs, each thread holding its kSmallPer 16-byte chunks in registers; every CTA
+// reduces its amax, the cluster exchanges the CTA maxima through distributed shared memory,
+// and the same registers are cast -- one read, no atomics, no second launch.  The amax and
+// the codes are those of the two-pass kernels (a max does not depend on the order of its
+// operands).  Chunk i belongs to thread i % (kSmallCtas * kSmallThreads) of the cluster.
+constexpr int kSmallCtas = 8, kSmallThreads = 128, kSmallPer = 8;
 
-__global__ void __launch_bounds__(kSmallThreads, 1)
+__global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallThreads)
     quant_tensor_small_kernel(const uint4* __restrict__ x, int64_t n8, uint2* __restrict__ xq,
                               float* __restrict__ xs, float* __restrict__ scale_out,
                               int32_t* status, int32_t* zero, int n_zero) {
   // a decode-size projection's GEMM may launch now and start streaming its weights; it
   // waits for this kernel's results before reading them
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  for (int i = threadIdx.x; i < n_zero; i += kSmallThreads) zero[i] = 0;
+  __shared__ float red[kSmallThreads / 32];
+  __shared__ float cta_amax;
+  const int gt = blockIdx.x * kSmallThreads + threadIdx.x;
+  constexpr int kAll = kSmallCtas * kSmallThreads;
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < n_zero; i += kSmallThreads) zero[i] = 0;
   uint4 v[kSmallPer];
   float m = 0.0f, bad = 0.0f;
 #pragma unroll
   for (int u = 0; u < kSmallPer; ++u) {
-    const int64_t i = threadIdx.x + static_cast<int64_t>(u) * kSmallThreads;
+    const int64_t i = gt + static_cast<int64_t>(u) * kAll;
     v[u] = i < n8 ? __ldg(x + i) : make_uint4(0, 0, 0, 0);
     amax_fold8(v[u], m, bad);
   }
   report_nonfinite(status, bad);
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
-  __shared__ float red[32];
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
   __syncthreads();
-  m = red[threadIdx.x & 31];
+  if (threadIdx.x == 0) {
+    float c = red[0];
 #pragma unroll
-  for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+    for (int w = 1; w < kSmallThreads / 32; ++w) c = fmaxf(c, red[w]);
+    cta_amax = c;
+  }
+  // every CTA's maximum is published before any CTA reads them
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+  m = 0.0f;
+  const uint32_t local = smem_u32(&cta_amax);
+#pragma unroll
+  for (int r = 0; r < kSmallCtas; ++r) {
+    uint32_t remote;
+    float c;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(r));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(c) : "r"(remote) : "memory");
+    m = fmaxf(m, c);
+  }
+  // no CTA leaves (and gives up its shared memory) while another may still read it
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
   const float sc = scale_from_amax(m);
   const float y = __frcp_rn(sc);
   const bool fast = quot_fast_ok(sc);
-  if (threadIdx.x == 0) {
+  if (gt == 0) {
     xs[0] = sc;
     if (scale_out) *scale_out = sc;
   }
 #pragma unroll
   for (int u = 0; u < kSmallPer; ++u) {
-    const int64_t i = threadIdx.x + static_cast<int64_t>(u) * kSmallThreads;
+    const int64_t i = gt + static_cast<int64_t>(u) * kAll;
     if (i < n8) xq[i] = cast8(v[u], sc, y, fast);
   }
 }
@@ -276,8 +301,8 @@ cudaError_t launch_quant_per_tensor(const uint16_t* x, int64_t M, int64_t K, uin
                                     float* xs, WsHeader* hdr, cudaStream_t s, int32_t* zero,
                                     int n_zero) {
   const int64_t n8 = M * K / 8;
-  if (n8 <= static_cast<int64_t>(kSmallThreads) * kSmallPer) {
-    quant_tensor_small_kernel<<<1, kSmallThreads, 0, s>>>(
+  if (n8 <= static_cast<int64_t>(kSmallCtas) * kSmallThreads * kSmallPer) {
+    quant_tensor_small_kernel<<<kSmallCtas, kSmallThreads, 0, s>>>(
         reinterpret_cast<const uint4*>(x), n8, reinterpret_cast<uint2*>(xq), xs, &hdr->scale,
         &hdr->status, zero, n_zero);
     return cudaGetLastError();
