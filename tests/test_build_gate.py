@@ -57,3 +57,21 @@ def test_grouped_gemm_spills_stay_within_budget():
             assert stores == 0 and loads == 0, (key, stores, loads)
         else:
             assert stores <= BUDGET[key], (key, stores, BUDGET[key])
+
+
+@pytest.mark.skipif(not os.path.exists(os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"),
+                                                    "bin", "nvcc")), reason="no nvcc")
+@pytest.mark.parametrize("src", ["decode.cu", "route.cu", "quant.cu", "glue.cu", "dispatch.cu"])
+def test_other_kernels_do_not_spill(src):
+    # the routing, quantization, combine, decode-projection and glue kernels keep every
+    # value in registers (several hold loads in flight or bulk-copy state across waits)
+    nvcc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    csrc = os.path.join(ROOT, "fp8_grouped_expert_gb300", "csrc")
+    r = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3",
+                        "-std=c++17", "-I" + os.path.join(ROOT, "include"), "-I" + csrc,
+                        "-Xptxas", "-v", "-c", os.path.join(csrc, src), "-o", os.devnull],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-2000:]
+    spills = re.findall(r"(\d+) bytes spill stores, (\d+) bytes spill loads", r.stderr)
+    assert spills, "ptxas reported no kernels"
+    assert all(s == "0" and l == "0" for s, l in spills), (src, spills)
