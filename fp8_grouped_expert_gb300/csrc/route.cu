@@ -15,6 +15,31 @@ namespace fge {
 constexpr int kChunkTokens = 128;  // tokens per permutation chunk
 constexpr int kQuantPairs = 4;     // group pairs whose loads a warp keeps in flight
 
+// The routing kernels run as a chain of programmatic dependent launches: each starts with
+// griddepcontrol.wait (nothing it reads from the kernel before it is touched earlier, so the
+// results are those of plain stream order) and then lets its own dependent launch, so the
+// launch of the next kernel overlaps this one instead of following its end.
+__device__ __forceinline__ void chain_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                  cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ------------------------------------------------------------------------------ top-k
 // Float bits mapped to an unsigned key with the same order (negative values reversed).
 // -0 and +0 compare equal as floats, so both take the key of +0.
@@ -37,6 +62,7 @@ __device__ __forceinline__ float key_value(uint32_t key) {
 template <int PER>
 __global__ void topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k,
                             int32_t* __restrict__ ids, float* __restrict__ gates) {
+  chain_enter();
   constexpr uint32_t kNone = 0x7fffffffu;
   const int lane = threadIdx.x & 31;
   const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
@@ -129,13 +155,13 @@ cudaError_t launch_topk_gate(const float* logits, int64_t T, int E, int k, int32
   if (T == 0) return cudaSuccess;
   const int grid = static_cast<int>(std::min<int64_t>((T + 7) / 8, num_sms() * 16));
   const int per = (E + 31) / 32;
-  if (per <= 1) topk_kernel<1><<<grid, 256, 0, s>>>(logits, T, E, k, ids, gates);
-  else if (per <= 2) topk_kernel<2><<<grid, 256, 0, s>>>(logits, T, E, k, ids, gates);
-  else if (per <= 4) topk_kernel<4><<<grid, 256, 0, s>>>(logits, T, E, k, ids, gates);
-  else if (per <= 8) topk_kernel<8><<<grid, 256, 0, s>>>(logits, T, E, k, ids, gates);
-  else if (per <= 16) topk_kernel<16><<<grid, 256, 0, s>>>(logits, T, E, k, ids, gates);
-  else topk_kernel<32><<<grid, 256, 0, s>>>(logits, T, E, k, ids, gates);
-  return cudaGetLastError();
+  const dim3 g(grid), b(256);
+  if (per <= 1) return launch_chained(topk_kernel<1>, g, b, 0, s, logits, T, E, k, ids, gates);
+  if (per <= 2) return launch_chained(topk_kernel<2>, g, b, 0, s, logits, T, E, k, ids, gates);
+  if (per <= 4) return launch_chained(topk_kernel<4>, g, b, 0, s, logits, T, E, k, ids, gates);
+  if (per <= 8) return launch_chained(topk_kernel<8>, g, b, 0, s, logits, T, E, k, ids, gates);
+  if (per <= 16) return launch_chained(topk_kernel<16>, g, b, 0, s, logits, T, E, k, ids, gates);
+  return launch_chained(topk_kernel<32>, g, b, 0, s, logits, T, E, k, ids, gates);
 }
 
 // ------------------------------------------------------------------------ permutation
@@ -147,6 +173,7 @@ size_t permute_scratch_bytes(int64_t T, int E) {
 // (1) per-chunk expert histogram
 __global__ void permute_count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int E,
                                      int32_t* __restrict__ chunk_counts) {
+  chain_enter();
   extern __shared__ int hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -164,6 +191,7 @@ __global__ void permute_count_kernel(const int32_t* __restrict__ ids, int64_t T,
 // dependent loads per thread is chunks / P long instead of chunks.
 __global__ void permute_scan_kernel(int32_t* __restrict__ chunk_counts, int64_t chunks, int E,
                                     int32_t* __restrict__ offsets) {
+  chain_enter();
   __shared__ int part_sum[1024];   // slice sums, then slice bases within the expert
   __shared__ int totals[1024];     // per expert: total, then the expert's first row
   __shared__ int warp_sums[32];
@@ -259,6 +287,7 @@ __global__ void permute_rank_kernel(const int32_t* __restrict__ ids, int64_t T, 
                                     const int32_t* __restrict__ chunk_base,
                                     int32_t* __restrict__ row_token,
                                     int32_t* __restrict__ token_row) {
+  chain_enter();
   extern __shared__ int sm[];
   int* cnt = sm;                          // [kRankWarps][E]: slice counts, then slice bases
   int* sid = sm + kRankWarps * E;         // the chunk's ids
@@ -319,6 +348,7 @@ __global__ void permute_copy_kernel(const uint8_t* __restrict__ xq, const float*
                                     int64_t T, int k, int64_t H,
                                     const int32_t* __restrict__ token_row,
                                     uint8_t* __restrict__ aq, float* __restrict__ as) {
+  chain_enter();
   const int lane = threadIdx.x & 31;
   const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -375,6 +405,7 @@ __global__ void permute_quant_copy_kernel(const uint4* __restrict__ x, int64_t T
                                           int64_t H, const int32_t* __restrict__ token_row,
                                           uint8_t* __restrict__ aq, float* __restrict__ as,
                                           int32_t* status) {
+  chain_enter();
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4, hl = lane & 15;
   const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
@@ -427,9 +458,8 @@ cudaError_t launch_permute_quant(const int32_t* ids, int64_t T, int k, int E,
                                  token_row, nullptr, nullptr, scratch, s);
   if (e != cudaSuccess || T == 0) return e;
   const int grid = static_cast<int>(std::min<int64_t>((T + 7) / 8, num_sms() * 8));
-  permute_quant_copy_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), T, k, H,
-                                                 token_row, aq, as, status);
-  return cudaGetLastError();
+  return launch_chained(permute_quant_copy_kernel, dim3(grid), dim3(256), 0, s,
+                        reinterpret_cast<const uint4*>(x), T, k, H, token_row, aq, as, status);
 }
 
 cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, const uint8_t* xq,
@@ -439,22 +469,21 @@ cudaError_t launch_permute(const int32_t* ids, int64_t T, int k, int E, const ui
   const int64_t chunks = (T + kChunkTokens - 1) / kChunkTokens;
   int32_t* cc = reinterpret_cast<int32_t*>(scratch);
   if (chunks > 0) {
-    permute_count_kernel<<<static_cast<int>(chunks), 256, E * sizeof(int), s>>>(ids, T, k, E, cc);
-    cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_chained(permute_count_kernel, dim3(static_cast<int>(chunks)),
+                                         dim3(256), E * sizeof(int), s, ids, T, k, E, cc);
     if (e != cudaSuccess) return e;
   }
-  permute_scan_kernel<<<1, 1024, 0, s>>>(cc, chunks, E, offsets);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_chained(permute_scan_kernel, dim3(1), dim3(1024), 0, s, cc, chunks, E,
+                                 offsets);
   if (e != cudaSuccess || chunks == 0) return e;
-  permute_rank_kernel<<<static_cast<int>(chunks), 32 * kRankWarps,
-                        (kRankWarps * E + kChunkTokens * k) * sizeof(int), s>>>(
-      ids, T, k, E, cc, row_token, token_row);
-  e = cudaGetLastError();
+  e = launch_chained(permute_rank_kernel, dim3(static_cast<int>(chunks)), dim3(32 * kRankWarps),
+                     (kRankWarps * E + kChunkTokens * k) * sizeof(int), s, ids, T, k, E, cc,
+                     row_token, token_row);
   if (e != cudaSuccess) return e;
   if (aq == nullptr) return cudaSuccess;  // index-only: the GEMM gathers rows by row_token
   const int grid = static_cast<int>(std::min<int64_t>((T + 7) / 8, num_sms() * 8));
-  permute_copy_kernel<<<grid, 256, 0, s>>>(xq, xs, T, k, H, token_row, aq, as);
-  return cudaGetLastError();
+  return launch_chained(permute_copy_kernel, dim3(grid), dim3(256), 0, s, xq, xs, T, k, H,
+                        token_row, aq, as);
 }
 
 // ----------------------------------------------------------------------------- combine
