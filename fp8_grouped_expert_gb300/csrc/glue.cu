@@ -2,6 +2,7 @@
 // logits, the identity stand-in for the attention core, and the fp32 residual add.
 #include <algorithm>
 
+#include "chain.cuh"
 #include "fge_device.cuh"
 
 namespace fge {
@@ -13,6 +14,7 @@ namespace fge {
 template <bool ADD, bool YF32>
 __global__ void rmsnorm_kernel(float* __restrict__ h, const void* __restrict__ y, int64_t H,
                                float eps, uint16_t* __restrict__ out) {
+  chain_enter();
   float* row = h + blockIdx.x * H;
   float ss = 0.0f;
   for (int64_t i = threadIdx.x * 4; i < H; i += blockDim.x * 4) {
@@ -69,6 +71,7 @@ constexpr int kRouterTok = 16, kRouterExp = 4;
 __global__ void __launch_bounds__(256)
     router_kernel(const uint16_t* __restrict__ xn, const float* __restrict__ wr, int64_t T,
                   int64_t H, int E, float* __restrict__ logits) {
+  chain_enter();
   extern __shared__ uint4 sx[];  // [kRouterTok][H / 8], 8 bf16 each
   const int64_t t0 = blockIdx.x * static_cast<int64_t>(kRouterTok);
   const int nt = static_cast<int>(T - t0 < kRouterTok ? T - t0 : kRouterTok);
@@ -142,6 +145,7 @@ __global__ void __launch_bounds__(256)
 // attn[t, h*128 + d] = v[t, (h / rep)*128 + d], 16-byte copies.
 __global__ void identity_attention_kernel(const uint4* __restrict__ v, int64_t T, int n_heads,
                                           int n_kv, uint4* __restrict__ attn) {
+  chain_enter();
   const int rep = n_heads / n_kv;
   const int64_t per_row = static_cast<int64_t>(n_heads) * 16;  // 128 bf16 = 16 uint4 per head
   const int64_t total = T * per_row;
@@ -155,6 +159,7 @@ __global__ void identity_attention_kernel(const uint4* __restrict__ v, int64_t T
 
 template <bool YF32>
 __global__ void residual_add_kernel(float* __restrict__ h, const void* __restrict__ y, int64_t n) {
+  chain_enter();
   for (int64_t i = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) * 4; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x * 4) {
     float4 a = *reinterpret_cast<float4*>(h + i);
@@ -172,19 +177,17 @@ __global__ void residual_add_kernel(float* __restrict__ h, const void* __restric
 cudaError_t launch_rmsnorm(const float* h, int64_t T, int64_t H, float eps, uint16_t* out,
                            cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  rmsnorm_kernel<false, false><<<static_cast<unsigned>(T), 256, 0, s>>>(
-      const_cast<float*>(h), nullptr, H, eps, out);
-  return cudaGetLastError();
+  return launch_chained(rmsnorm_kernel<false, false>, dim3(static_cast<unsigned>(T)), dim3(256), 0,
+                        s, const_cast<float*>(h), static_cast<const void*>(nullptr), H, eps, out);
 }
 
 cudaError_t launch_residual_rmsnorm(float* h, const void* y, int y_f32, int64_t T, int64_t H,
                                     float eps, uint16_t* out, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(T)), block(256);
   if (y_f32)
-    rmsnorm_kernel<true, true><<<static_cast<unsigned>(T), 256, 0, s>>>(h, y, H, eps, out);
-  else
-    rmsnorm_kernel<true, false><<<static_cast<unsigned>(T), 256, 0, s>>>(h, y, H, eps, out);
-  return cudaGetLastError();
+    return launch_chained(rmsnorm_kernel<true, true>, grid, block, 0, s, h, y, H, eps, out);
+  return launch_chained(rmsnorm_kernel<true, false>, grid, block, 0, s, h, y, H, eps, out);
 }
 
 cudaError_t launch_router(const uint16_t* xn, const float* wr, int64_t T, int64_t H, int E,
@@ -201,25 +204,24 @@ cudaError_t launch_router(const uint16_t* xn, const float* wr, int64_t T, int64_
   // blocks split the experts too (32 per block), so that a small T still fills the SMs
   const dim3 grid(static_cast<unsigned>((T + kRouterTok - 1) / kRouterTok),
                   static_cast<unsigned>((E + 8 * kRouterExp - 1) / (8 * kRouterExp)));
-  router_kernel<<<grid, 256, smem, s>>>(xn, wr, T, H, E, logits);
-  return cudaGetLastError();
+  return launch_chained(router_kernel, grid, dim3(256), static_cast<size_t>(smem), s, xn, wr, T,
+                        H, E, logits);
 }
 
 cudaError_t launch_identity_attention(const uint16_t* v, int64_t T, int n_heads, int n_kv,
                                       uint16_t* attn, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int grid = num_sms() * 8;
-  identity_attention_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(v), T, n_heads,
-                                                 n_kv, reinterpret_cast<uint4*>(attn));
-  return cudaGetLastError();
+  return launch_chained(identity_attention_kernel, dim3(grid), dim3(256), 0, s,
+                        reinterpret_cast<const uint4*>(v), T, n_heads, n_kv,
+                        reinterpret_cast<uint4*>(attn));
 }
 
 cudaError_t launch_residual_add(float* h, const void* y, int y_f32, int64_t n, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   const int grid = static_cast<int>(std::min<int64_t>((n / 4 + 255) / 256, num_sms() * 8));
-  if (y_f32) residual_add_kernel<true><<<grid, 256, 0, s>>>(h, y, n);
-  else residual_add_kernel<false><<<grid, 256, 0, s>>>(h, y, n);
-  return cudaGetLastError();
+  if (y_f32) return launch_chained(residual_add_kernel<true>, dim3(grid), dim3(256), 0, s, h, y, n);
+  return launch_chained(residual_add_kernel<false>, dim3(grid), dim3(256), 0, s, h, y, n);
 }
 
 }  // namespace fge

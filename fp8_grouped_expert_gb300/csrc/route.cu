@@ -8,6 +8,7 @@
 #include <cfloat>
 
 #include "fge_device.cuh"
+#include "chain.cuh"
 #include "quotient.cuh"
 
 namespace fge {
@@ -15,30 +16,6 @@ namespace fge {
 constexpr int kChunkTokens = 128;  // tokens per permutation chunk
 constexpr int kQuantPairs = 4;     // group pairs whose loads a warp keeps in flight
 
-// The routing kernels run as a chain of programmatic dependent launches: each starts with
-// griddepcontrol.wait (nothing it reads from the kernel before it is touched earlier, so the
-// results are those of plain stream order) and then lets its own dependent launch, so the
-// launch of the next kernel overlaps this one instead of following its end.
-__device__ __forceinline__ void chain_enter() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-template <typename... KArgs, typename... Args>
-static cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                                  cudaStream_t s, Args... args) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
-}
 
 // ------------------------------------------------------------------------------ top-k
 // Float bits mapped to an unsigned key with the same order (negative values reversed).
