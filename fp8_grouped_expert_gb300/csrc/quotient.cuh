@@ -4,10 +4,14 @@
 // correction step, "Computation of elementary functions on the IBM RISC System/6000
 // processor", 1990).  For the inputs here -- x a bfloat16 value (at most 8 significant
 // bits), s a normal float in [2^-90, 2^120] -- that holds for every pair of significands
-// (all 2^7 x 2^23 of them checked against the division on the host, tests/host), and the
-// exponent range keeps every intermediate normal or exact.  The residual is formed as
-// -(q0 s - x) so that a zero x keeps its sign.  Outside that range of s, or for a
-// non-finite x, the callers divide.
+// (all 2^7 x 2^23 of them checked against the division on the host, tests/host), and
+// scaling both by powers of two keeps it while the steps stay normal.  Below |x| ~ 2^-103 the
+// residual is subnormal and inexact and the result may be off by one unit in the last place,
+// but then |x / s| < 2^-13 and both round to the same signed e4m3 zero; the quotient must not
+// overflow (q0 would be infinite and the result NaN), which the callers guarantee by deriving
+// s = amax / 448 from the values they cast.  Both corners are sampled on the host across all
+// exponents and signs.  The residual is formed as -(q0 s - x) so that a zero x keeps its
+// sign.  Outside that range of s, or for a non-finite x, the callers divide.
 #pragma once
 
 namespace fge {

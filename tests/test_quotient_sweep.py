@@ -34,3 +34,19 @@ def test_corrected_quotient_equals_the_division(tmp_path):
 def test_plain_reciprocal_product_is_not_the_division(tmp_path):
     pairs, bad = _run(tmp_path, "16", "plain")
     assert bad > 0
+
+
+
+@pytest.mark.parametrize("mode", ["amax", "wide"])
+def test_corrected_quotient_across_exponents(tmp_path, mode):
+    # random bf16 x (zeros, subnormals, both signs) and s across the range the kernels take
+    # the reciprocal path for: the e4m3 codes of the two quotients agree everywhere
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    exe = str(tmp_path / "quotient_range")
+    subprocess.run([cc, "-O2", "-ffp-contract=off", "-o", exe,
+                    os.path.join(HERE, "host", "quotient_range.c"), "-lm"], check=True)
+    out = subprocess.run([exe, "2000000", "7", mode], check=True, capture_output=True,
+                         text=True).stdout.split()
+    assert int(out[1]) == 2000000 and int(out[3]) == 0
