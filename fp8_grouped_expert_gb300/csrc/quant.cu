@@ -32,27 +32,6 @@ __device__ __forceinline__ void amax_fold8(const uint4& v, float& m, float& bad)
                        bf16_hi(v.w));
 }
 
-// The e4m3 codes of 8 bf16 values divided by s (the IEEE quotient, then round to nearest
-// even).  y = RN(1/s) and fast = quot_fast_ok(s), both from the caller: the quotient comes
-// from the reciprocal (quotient.cuh) when s is in that method's range, else by division.
-// A NaN value gives a NaN quotient either way.
-__device__ __forceinline__ uint2 cast8(const uint4& v, float s, float y, bool fast) {
-  const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                      bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-  float d[8];
-  if (fast) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) d[i] = quot_rn(f[i], s, y);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) d[i] = __fdiv_rn(f[i], s);
-  }
-  uint2 q;
-  q.x = cvt_e4m3x4(d[0], d[1], d[2], d[3]);
-  q.y = cvt_e4m3x4(d[4], d[5], d[6], d[7]);
-  return q;
-}
-
 __global__ void amax_kernel(const uint4* __restrict__ x, int64_t n8, uint32_t* __restrict__ amax_bits,
                             int32_t* status) {
   float m = 0.0f, bad = 0.0f;

@@ -14,7 +14,8 @@
 namespace fge {
 
 constexpr int kChunkTokens = 128;  // tokens per permutation chunk
-constexpr int kQuantPairs = 4;     // group pairs whose loads a warp keeps in flight
+constexpr int kQuantQuads = 2;     // group quads whose loads a warp keeps in flight
+constexpr int kQuantBlocks = 4;    // resident 256-thread blocks per SM (launch bounds)
 
 
 // ------------------------------------------------------------------------------ top-k
@@ -355,29 +356,82 @@ __global__ void permute_copy_kernel(const uint8_t* __restrict__ xq, const float*
   }
 }
 
-// The e4m3 codes of a lane's 8 values of one 128-value group, each the code of the IEEE
-// quotient x / sc: from one reciprocal of sc (quotient.cuh) unless sc is out of that
-// method's range or one of the lane's values is not finite (bad != 0), then by division.
-__device__ __forceinline__ uint2 cast8_g(const float (&f)[8], float sc, float bad) {
-  float d[8];
-  if (quot_fast_ok(sc) && bad == 0.0f) {
-    const float y = __frcp_rn(sc);
+// The magnitudes of a lane's 8 bfloat16 values, pairwise maxima packed two per word: the
+// low 15 bits of a bfloat16 order like its absolute value, so an unsigned maximum of
+// (w & 0x7fff) over values is the pattern of their largest |x|.  A pattern at or above 0x7f80
+// is an infinity or a NaN.
+__device__ __forceinline__ uint32_t mag_bits_pack(const uint4& v) {
+  return __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                  __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+}
+
+// amax of each 128-value group for U groups per lane group of a warp: a group's values are
+// spread over 16 / W adjacent lanes, W x 8 per lane, lane's share v[u W .. u W + W) for its
+// u-th group.  While every value the warp holds is finite, amax comes from the bit patterns.
+// Otherwise the whole warp takes the float path (the maximum over the finite values, as the
+// division-based quantizer defines it), and each lane holding an infinity or a NaN reports
+// it to status.  A group holding an infinity has amax = inf and so an infinite scale, which
+// sends its quotients to the division; a NaN gives a NaN code either way.  All 32 lanes call
+// it (the shuffles and the vote are warp-wide); the U reductions are interleaved.
+template <int U, int W>
+__device__ __forceinline__ void g128_amax(const uint4 (&v)[U * W], float (&amax)[U],
+                                          int32_t* status) {
+  uint32_t mb[U];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) d[i] = quot_rn(f[i], sc, y);
-  } else {
+  for (int u = 0; u < U; ++u) {
+    uint32_t m = mag_bits_pack(v[u * W]);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) d[i] = __fdiv_rn(f[i], sc);
+    for (int w = 1; w < W; ++w) m = __vmaxu2(m, mag_bits_pack(v[u * W + w]));
+    mb[u] = max(m & 0xFFFFu, m >> 16);
   }
-  uint2 q;
-  q.x = cvt_e4m3x4(d[0], d[1], d[2], d[3]);
-  q.y = cvt_e4m3x4(d[4], d[5], d[6], d[7]);
-  return q;
+#pragma unroll
+  for (int d = 8 / W; d > 0; d >>= 1)
+#pragma unroll
+    for (int u = 0; u < U; ++u) mb[u] = max(mb[u], __shfl_xor_sync(0xffffffffu, mb[u], d));
+  uint32_t top = 0;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    top = max(top, mb[u]);
+    amax[u] = __uint_as_float(mb[u] << 16);
+  }
+  if (!__any_sync(0xffffffffu, top >= 0x7F80u)) return;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    float a = 0.0f, b = 0.0f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const uint4& x = v[u * W + w];
+      const float f[8] = {bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y),
+                          bf16_lo(x.z), bf16_hi(x.z), bf16_lo(x.w), bf16_hi(x.w)};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        a = fmaxf(a, fabsf(f[i]));
+        b = nonfinite_fold(b, f[i]);
+      }
+    }
+    report_nonfinite(status, b);
+#pragma unroll
+    for (int d = 8 / W; d > 0; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));
+    amax[u] = a;
+  }
+}
+
+// The group's scale s = max(RN(amax / 448), 2^-126), 1 for an all-zero group: the quotient
+// by the correction step of quotient.cuh from the constant RN(1/448) = 0x1.24924ap-9.  The
+// product q0 * 448 = 7 q0 * 64 is a multiple of 64 ulp(q0), so the residual is exact for
+// every amax, and the result equals the division for every finite bfloat16 amax (all 2^15
+// magnitudes checked on the host).
+__device__ __forceinline__ float g128_scale(float amax) {
+  float s = quot_rn(amax, 448.0f, 0x1.24924ap-9f);
+  if (amax == 0.0f) s = 1.0f;
+  if (s < 0x1p-126f) s = 0x1p-126f;
+  return s;
 }
 
 // (4') quantize and copy in one pass: one warp per token reads its bf16 row once, quantizes
-// each 128-value group exactly as quant_g128_kernel does (16 lanes x 8 values, shuffle amax,
-// s = amax / 448, the IEEE quotient x / s, e4m3 round to nearest even) and writes the codes and the
-// scale to the token's k expert rows.  Two groups per warp step.
+// each 128-value group as quant_g128_kernel does (shuffle amax, s = amax / 448, the IEEE
+// quotient x / s, e4m3 round to nearest even; here 16 lanes x 8 values a group) and writes
+// the codes and the scale to the token's k expert rows.  Two groups per warp step.
 __global__ void permute_quant_copy_kernel(const uint4* __restrict__ x, int64_t T, int k,
                                           int64_t H, const int32_t* __restrict__ token_row,
                                           uint8_t* __restrict__ aq, float* __restrict__ as,
@@ -398,23 +452,14 @@ __global__ void permute_quant_copy_kernel(const uint4* __restrict__ x, int64_t T
         const int64_t g = g0 + 2 * u + half;
         v[u] = g < G ? __ldcs(x + (t * G + g) * 16 + hl) : make_uint4(0, 0, 0, 0);
       }
+      float amax[U];
+      g128_amax<U, 1>(v, amax, status);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int64_t g = g0 + 2 * u + half;
         const bool in = g < G;
-        const float f[8] = {bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y),
-                            bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w)};
-        float amax = 0.0f, bad = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          amax = fmaxf(amax, fabsf(f[i]));
-          bad = nonfinite_fold(bad, f[i]);
-        }
-        report_nonfinite(status, bad);
-#pragma unroll
-        for (int d = 8; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
-        const float sc = scale_from_amax(amax);
-        const uint2 q = cast8_g(f, sc, bad);
+        const float sc = g128_scale(amax[u]);
+        const uint2 q = cast8(v[u], sc, __frcp_rn(sc), quot_fast_ok(sc));
         for (int j = 0; j < k; ++j) {
           const int64_t r = __shfl_sync(0xffffffffu, my_row, j);
           if (in) {
@@ -665,44 +710,41 @@ cudaError_t launch_combine(const void* y, int y_f32, const int32_t* token_row,
 }
 
 // The stand-alone G128 activation quantization.  Rows hold whole groups (K % 128 == 0), so
-// the tensor is a flat array of M * K / 128 groups whose scales are stored in the same order;
-// each half-warp quantizes one group exactly as the quantizing copy above does, and the warps
-// stride over group pairs with kQuantPairs pairs' loads in flight, so that every warp gets
-// the same share of the tensor whatever M and K are.
-__global__ void __launch_bounds__(256, 5)
+// the tensor is a flat array of M * K / 128 groups whose scales are stored in the same order.
+// Each quarter-warp (8 lanes) quantizes one group, 16 values a lane (bytes [32 j, 32 j + 32)
+// of the group for lane j, and 16 code bytes out), so the per-group work -- the scale, its
+// reciprocal, the range test -- is spread over 16 values instead of the quantizing copy's 8,
+// with the same codes and scales.  The warps stride over group quads with kQuantQuads quads'
+// loads in flight, so every warp gets the same share of the tensor whatever M and K are.
+__global__ void __launch_bounds__(256, kQuantBlocks)
     quant_g128_kernel(const uint4* __restrict__ x, int64_t ngroups,
-                                  uint2* __restrict__ xq, float* __restrict__ xs,
-                                  int32_t* status) {
+                      uint4* __restrict__ xq, float* __restrict__ xs, int32_t* status) {
   const int lane = threadIdx.x & 31;
-  const int half = lane >> 4, hl = lane & 15;
+  const int quarter = lane >> 3, ql = lane & 7;
   const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  const int64_t npairs = (ngroups + 1) / 2;
-  for (int64_t p0 = wid; p0 < npairs; p0 += nw * kQuantPairs) {  // warp-uniform trips
-    uint4 v[kQuantPairs];
+  const int64_t nquads = (ngroups + 3) / 4;
+  for (int64_t p0 = wid; p0 < nquads; p0 += nw * kQuantQuads) {  // warp-uniform trips
+    uint4 v[2 * kQuantQuads];
 #pragma unroll
-    for (int u = 0; u < kQuantPairs; ++u) {
-      const int64_t g = 2 * (p0 + u * nw) + half;
-      v[u] = g < ngroups ? __ldcs(x + g * 16 + hl) : make_uint4(0, 0, 0, 0);
+    for (int u = 0; u < kQuantQuads; ++u) {
+      const int64_t g = 4 * (p0 + u * nw) + quarter;
+      const bool in = g < ngroups;
+      v[2 * u] = in ? __ldcs(x + g * 16 + 2 * ql) : make_uint4(0, 0, 0, 0);
+      v[2 * u + 1] = in ? __ldcs(x + g * 16 + 2 * ql + 1) : make_uint4(0, 0, 0, 0);
     }
+    float amax[kQuantQuads];
+    g128_amax<kQuantQuads, 2>(v, amax, status);
 #pragma unroll
-    for (int u = 0; u < kQuantPairs; ++u) {
-      const int64_t g = 2 * (p0 + u * nw) + half;
-      const float f[8] = {bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y),
-                          bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w)};
-      float amax = 0.0f, bad = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        amax = fmaxf(amax, fabsf(f[i]));
-        bad = nonfinite_fold(bad, f[i]);
-      }
-      report_nonfinite(status, bad);
-#pragma unroll
-      for (int d = 8; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
-      const float sc = scale_from_amax(amax);
+    for (int u = 0; u < kQuantQuads; ++u) {
+      const int64_t g = 4 * (p0 + u * nw) + quarter;
+      const float sc = g128_scale(amax[u]);
+      const float y = __frcp_rn(sc);
+      const bool fast = quot_fast_ok(sc);
       if (g < ngroups) {
-        __stcs(xq + g * 16 + hl, cast8_g(f, sc, bad));
-        if (hl == 0) xs[g] = sc;
+        const uint2 lo = cast8(v[2 * u], sc, y, fast), hi = cast8(v[2 * u + 1], sc, y, fast);
+        __stcs(xq + g * 8 + ql, make_uint4(lo.x, lo.y, hi.x, hi.y));
+        if (ql == 0) xs[g] = sc;
       }
     }
   }
@@ -712,12 +754,12 @@ cudaError_t launch_quant_g128(const uint16_t* x, int64_t M, int64_t K, uint8_t* 
                               int32_t* status, cudaStream_t s) {
   const int64_t ngroups = M * (K / 128);
   if (ngroups == 0) return cudaSuccess;
-  const int64_t pairs = (ngroups + 1) / 2;
-  // five blocks of 256 threads are resident per SM (launch bounds): one wave
+  const int64_t quads = (ngroups + 3) / 4;
+  // kQuantBlocks blocks of 256 threads are resident per SM (launch bounds): one wave
   const int grid = static_cast<int>(std::min<int64_t>(
-      (pairs + 8 * kQuantPairs - 1) / (8 * kQuantPairs), num_sms() * 5));
+      (quads + 8 * kQuantQuads - 1) / (8 * kQuantQuads), num_sms() * kQuantBlocks));
   quant_g128_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), ngroups,
-                                         reinterpret_cast<uint2*>(xq), xs, status);
+                                         reinterpret_cast<uint4*>(xq), xs, status);
   return cudaGetLastError();
 }
 

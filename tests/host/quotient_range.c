@@ -8,7 +8,10 @@
  * the IEEE quotient and either equals it or both lie below 2^-10, where every value rounds
  * to an e4m3 zero; so agreement means equal e4m3 codes.  (Below |x| ~ 2^-103 the residual
  * x - q0 s is no longer exact and the two may differ in the last place, always below 2^-10.)
- * Usage: quotient_range COUNT SEED amax|wide.  Prints "pairs N mismatches M". */
+ * Mode "scale" is exhaustive instead: the group scale max(RN(amax / 448), 2^-126) taken by
+ * the same correction step from the constant RN(1/448) must equal the one from the division
+ * for every finite bfloat16 amax (COUNT and SEED are ignored).
+ * Usage: quotient_range COUNT SEED amax|wide|scale.  Prints "pairs N mismatches M". */
 #include <math.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -36,6 +39,24 @@ int main(int argc, char** argv) {
   state = (argc > 2 ? strtoull(argv[2], NULL, 10) : 1) * 2654435761ULL + 1;
   const int wide = argc > 3 && strcmp(argv[3], "wide") == 0;
   long long bad = 0, pairs = 0;
+  if (argc > 3 && strcmp(argv[3], "scale") == 0) {
+    const float y448 = 0x1.24924ap-9f;
+    if (y448 != 1.0f / 448.0f) bad = 1; /* the constant is RN(1/448) */
+    for (uint32_t h = 0; h < 0x7F80u; ++h) {
+      const float amax = from_bits(h << 16);
+      const float q0 = amax * y448;
+      const float r = -fmaf(q0, 448.0f, -amax);
+      float s_fast = fmaf(r, y448, q0);
+      float s_div = amax / 448.0f;
+      if (amax == 0.0f) s_fast = s_div = 1.0f;
+      if (s_fast < 0x1p-126f) s_fast = 0x1p-126f;
+      if (s_div < 0x1p-126f) s_div = 0x1p-126f;
+      ++pairs;
+      if (s_fast != s_div) ++bad;
+    }
+    printf("pairs %lld mismatches %lld\n", pairs, bad);
+    return 0;
+  }
   while (pairs < n) {
     float x, s;
     if (wide) {

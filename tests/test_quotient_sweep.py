@@ -50,3 +50,17 @@ def test_corrected_quotient_across_exponents(tmp_path, mode):
     out = subprocess.run([exe, "2000000", "7", mode], check=True, capture_output=True,
                          text=True).stdout.split()
     assert int(out[1]) == 2000000 and int(out[3]) == 0
+
+
+def test_group_scale_by_constant_reciprocal(tmp_path):
+    # every finite bf16 amax: max(RN(amax / 448), 2^-126) from RN(1/448) and the correction
+    # step equals the one from the division
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    exe = str(tmp_path / "quotient_range")
+    subprocess.run([cc, "-O2", "-ffp-contract=off", "-o", exe,
+                    os.path.join(HERE, "host", "quotient_range.c"), "-lm"], check=True)
+    out = subprocess.run([exe, "0", "0", "scale"], check=True, capture_output=True,
+                         text=True).stdout.split()
+    assert int(out[1]) == 0x7F80 and int(out[3]) == 0
