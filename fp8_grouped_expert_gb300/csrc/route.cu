@@ -370,9 +370,9 @@ __device__ __forceinline__ uint32_t mag_bits_pack(const uint4& v) {
 // u-th group.  While every value the warp holds is finite, amax comes from the bit patterns.
 // Otherwise the whole warp takes the float path (the maximum over the finite values, as the
 // division-based quantizer defines it), and each lane holding an infinity or a NaN reports
-// it to status.  A group holding an infinity has amax = inf and so an infinite scale, which
-// sends its quotients to the division; a NaN gives a NaN code either way.  All 32 lanes call
-// it (the shuffles and the vote are warp-wide); the U reductions are interleaved.
+// it to status; the scale and codes of such a group are meaningless (an infinite amax
+// becomes a NaN scale in g128_scale).  All 32 lanes call it (the shuffles and the vote are
+// warp-wide); the U reductions are interleaved.
 template <int U, int W>
 __device__ __forceinline__ void g128_amax(const uint4 (&v)[U * W], float (&amax)[U],
                                           int32_t* status) {
@@ -420,7 +420,7 @@ __device__ __forceinline__ void g128_amax(const uint4 (&v)[U * W], float (&amax)
 // by the correction step of quotient.cuh from the constant RN(1/448) = 0x1.24924ap-9.  The
 // product q0 * 448 = 7 q0 * 64 is a multiple of 64 ulp(q0), so the residual is exact for
 // every amax, and the result equals the division for every finite bfloat16 amax (all 2^15
-// magnitudes checked on the host).
+// magnitudes checked on the host).  An infinite amax gives NaN.
 __device__ __forceinline__ float g128_scale(float amax) {
   float s = quot_rn(amax, 448.0f, 0x1.24924ap-9f);
   if (amax == 0.0f) s = 1.0f;
