@@ -11,8 +11,10 @@
 // overflow (q0 would be infinite and the result NaN), which the callers guarantee by deriving
 // s = amax / 448 from the values they cast.  Both corners are sampled on the host across all
 // exponents and signs.  The residual is formed as -(q0 s - x) so that a zero x keeps its
-// sign.  Outside that range of s, or for a non-finite x, the callers divide.  cast8 below is
-// the 8-value cast every e4m3 activation quantizer shares.
+// sign.  Outside that range of s the callers divide.  A NaN x gives NaN either way, and an
+// infinite x makes the caller's amax infinite and its s out of the range (the outputs for
+// non-finite inputs are meaningless; the quantizers report them).  cast8 below is the
+// 8-value cast every e4m3 activation quantizer shares.
 #pragma once
 
 #include "fge_device.cuh"
